@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of batched speculative-decoding verification on GB300.
+
+One step is one verification round: one call of the library over a whole
+batch of B sequences (the headline workload is sampling at B=256, V=128256,
+K=5).  The timed loop rotates through several input sets whose required bytes
+together exceed the L2 cache, so every step streams from HBM.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the
+host cores instead (the reference arm); under torchrun every rank runs its own
+batch (weak scaling) and the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify rounds/s and achieved HBM GB/s (% roofline) at B=256,V=128256,K=5"
+UNIT = "rounds/s"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_MODE = {1: "sample", 2: "greedy", 3: "sample", 4: "round", 5: "sample"}
+KERNEL_SOURCES = [
+    "speculative_decoding_verification_08_gb300/csrc/sv_device.cuh",
+    "speculative_decoding_verification_08_gb300/csrc/specverify.cu",
+]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--mode", choices=["sample", "greedy", "round"], default=None)
+    ap.add_argument("--sets", type=int, default=4, help="input sets rotated through")
+    ap.add_argument("--graph", action="store_true", help="replay the steps from a CUDA graph")
+    ap.add_argument("--segs-per-cta", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=60)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    a = ap.parse_args(argv)
+    if a.mode is None:
+        a.mode = DEFAULT_MODE[a.config]
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (host logic; covered by a gloo test)
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(cfg: int, set_index: int, rank: int) -> int:
+    """Seed of input set `set_index` on `rank`: every rank verifies its own batch."""
+    from speculative_decoding_verification_08_gb300.inputs import SEED_BASE
+    return SEED_BASE + cfg + 1000 * set_index + 100000 * rank
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Maximum of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_rounds_per_s(steps: int, world: int, max_elapsed_s: float) -> float:
+    """Whole-job rounds/s: every rank ran `steps` rounds of its own batch."""
+    return steps * world / max_elapsed_s
+
+
+# ---------------------------------------------------------------------------
+# required (algorithmic) bytes: the rows and gathers the rule must touch
+
+def required_bytes(mode_arr, n_arr, K: int, V: int) -> int:
+    """Greedy sequence: rows 0..n of p (4V each) + tokens + outputs.  Sampling
+    sequence: a 64-byte gather pair per tested position, the row pair p_n, q_n
+    (8V) on rejection or the row p_K (4V) when all K are accepted, tokens,
+    uniforms and outputs."""
+    total = 0
+    for m, n in zip(mode_arr, n_arr):
+        n = int(n)
+        if int(m) == 0:
+            total += (n + 1) * 4 * V + 4 * K + 8
+        else:
+            tested = min(n + 1, K)
+            rows = 8 * V if n < K else 4 * V
+            total += 64 * tested + rows + 4 * K + 4 * K + 8 + 8
+    return total
+
+
+def dense_bytes(mode_arr, K: int, V: int) -> int:
+    """Bytes of every row a rule could read (no early exit)."""
+    total = 0
+    for m in mode_arr:
+        total += (K + 1) * 4 * V + (K * 4 * V if int(m) == 1 else 0)
+    return total
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                self.samples.append(dict(t=ts + frac, sm=float(parts[2]), sm_max=float(parts[3]),
+                                         reasons=[r for r, v in zip(REASONS, parts[6:10])
+                                                  if v.lower().startswith("active")]))
+            except (ValueError, IndexError):
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1]
+        note = "samples inside the timed region"
+        if not inside:
+            inside = [s for s in self.samples if t0 - 0.25 <= s["t"] <= t1 + 0.25]
+            note = "timed region shorter than the sampling period; samples within 0.25 s of it"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.samples[-1]["sm_max"], "reasons": [],
+                    "samples": 0, "note": "no sample near the timed region"}
+        reasons = sorted({r for s in inside for r in s["reasons"]})
+        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+                "sm_max_mhz": max(s["sm_max"] for s in inside), "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# roofline denominators and ncu traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, mode: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel sources changed since it was taken or nothing matches."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    entry = d.get("entries", {}).get(f"{workload}|{mode}")
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+
+def host_inputs(cfg: int, seed: int):
+    import torch
+    from speculative_decoding_verification_08_gb300.inputs import make_inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    bt = make_inputs(cfg, dev, seed=seed)
+    host = bt.numpy()
+    del bt
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    return host
+
+
+def time_oracle(host, mode: str, K: int, seconds: float, nthreads: int, max_rounds=None,
+                seqs=None):
+    """Runs the oracle over (a subset of) the batch until `seconds` pass; returns
+    (rounds/s scaled to the full batch, sequences per round, rounds run)."""
+    import numpy as np
+    import oracle
+    p, q, t, ua, ur, md = host
+    B = p.shape[0]
+    if seqs is not None and seqs < B:
+        sl = slice(0, seqs)
+        p, t, ua, ur, md = p[sl], t[sl], ua[sl], ur[sl], md[sl]
+        q = None if q is None else q[sl]
+    nb = p.shape[0]
+    rounds = 0
+    t0 = time.perf_counter()
+    while True:
+        if mode == "greedy":
+            oracle.verify_greedy(p, t, nthreads=nthreads)
+        elif mode == "sample":
+            oracle.verify_sample(p, q, t, ua, ur, nthreads=nthreads)
+        else:
+            oracle.verify_round(md, p, q, t, ua, ur, nthreads=nthreads)
+        rounds += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_rounds is not None and rounds >= max_rounds):
+            break
+    return rounds * nb / B / el, nb, rounds, el
+
+
+def workload_config(args, B, K, V, extra=None):
+    from speculative_decoding_verification_08_gb300.inputs import CONFIGS
+    cfg = {"workload": CONFIGS[args.config]["name"], "B": B, "V": V, "K": K, "mode": args.mode,
+           "input_sets": args.sets}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on the host cores, same workload and metric."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from speculative_decoding_verification_08_gb300.inputs import CONFIGS
+    c = CONFIGS[args.config]
+    B, K, V = c["B"], c["K"], c["V"]
+    host = host_inputs(args.config, rank_seed(args.config, 0, 0))
+    ncpu = os.cpu_count() or 1
+    # calibrate: sequences per step so that warmup + steps stay within ~2 minutes
+    _, _, _, el = time_oracle(host, args.mode, K, 0.0, ncpu, max_rounds=1)
+    per_seq = el / B
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    seqs = int(max(ncpu, min(B, budget / max(per_seq, 1e-9))))
+    time_oracle(host, args.mode, K, 0.0, ncpu, max_rounds=args.warmup, seqs=seqs)
+    rps, nb, rounds, el = time_oracle(host, args.mode, K, float("inf"), ncpu,
+                                      max_rounds=args.steps, seqs=seqs)
+    sample = (f"{nb} of the {B} sequences of input set 0 per step, {rounds} steps, "
+              f"{el:.1f} s on {ncpu} threads; value scaled to full {B}-sequence rounds")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rps, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / rps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": workload_config(args, B, K, V),
+        "cpu_baseline": {"value": rps, "unit": UNIT, "cores": ncpu, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_08_gb300 as sv
+    from speculative_decoding_verification_08_gb300.inputs import CONFIGS, make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    sv.build()
+    lib = sv.load()
+    if args.segs_per_cta:
+        sv.set_segments_per_cta(args.segs_per_cta)
+
+    c = CONFIGS[args.config]
+    B, K, V = c["B"], c["K"], c["V"]
+    sets = [make_inputs(args.config, dev, seed=rank_seed(args.config, s, rank))
+            for s in range(args.sets)]
+    torch.cuda.empty_cache()
+    ws = sv.Workspace(B, K, V, dev)
+    outs = [(torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32,
+                                                                         device=dev))
+            for _ in sets]
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(dev)          # every timed launch goes to this stream
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda x: ctypes.c_void_p(0 if x is None else x.data_ptr())
+
+    # precomputed C-ABI argument lists: the timed loop is one C call per step
+    calls = []
+    for bt, (n, nx) in zip(sets, outs):
+        if args.mode == "greedy":
+            calls.append((lib.sv_verify_greedy,
+                          (P(bt.p), V, P(bt.t), B, K, V, P(n), P(nx), ws.ptr, ws.nbytes, sh)))
+        elif args.mode == "sample":
+            calls.append((lib.sv_verify_sample,
+                          (P(bt.p), V, P(bt.q), V, P(bt.t), P(bt.u_acc), P(bt.u_res), B, K, V,
+                           P(n), P(nx), ws.ptr, ws.nbytes, sh)))
+        else:
+            calls.append((lib.sv_verify_round,
+                          (P(bt.mode), P(bt.p), V, P(bt.q), V, P(bt.t), P(bt.u_acc),
+                           P(bt.u_res), B, K, V, P(n), P(nx), None, None, 0, ws.ptr,
+                           ws.nbytes, sh)))
+
+    def step(k):
+        fn, a = calls[k % len(calls)]
+        rc = fn(*a)
+        if rc != 0:
+            raise RuntimeError(f"verify call failed: {sv.status_string(rc)}")
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize(dev)
+    status = ws.status(stream)
+
+    # algorithmic bytes per launch, from each set's n_accepted
+    req, dense, nhist = [], [], np.zeros(K + 1, dtype=np.int64)
+    for bt, (n, _) in zip(sets, outs):
+        md = bt.mode.cpu().numpy() if args.mode == "round" else np.full(
+            B, 0 if args.mode == "greedy" else 1)
+        nn = n.cpu().numpy()
+        nhist += np.bincount(nn, minlength=K + 1)[:K + 1]
+        req.append(required_bytes(md, nn, K, V))
+        dense.append(dense_bytes(md, K, V))
+    req_per_launch = float(np.mean(req))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(len(calls)):
+                step(k)
+        graph = g
+
+    clocks = ClockSampler(dev.index or 0) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0.0)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    if graph is None:
+        for k in range(args.steps):
+            step(k)
+        launches = args.steps
+    else:
+        reps = max(1, args.steps // len(calls))
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                graph.replay()
+        launches = reps * len(calls)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier()
+    el_ms = e0.elapsed_time(e1)
+    max_ms = reduce_max(el_ms, dev)
+    if clocks:
+        clocks.stop()
+    steps_done = launches
+    rounds_per_s = aggregate_rounds_per_s(steps_done, world, max_ms / 1000.0)
+    ms_per_step = max_ms / steps_done
+    kernel_us = el_ms * 1000.0 / steps_done
+    achieved = req_per_launch / (kernel_us * 1e-6) / 1e9
+    peak, peak_kind = hbm_peak()
+    workload = c["name"]
+    traffic = ncu_traffic(workload, args.mode)
+
+    # end to end through the public API: pinned host inputs -> device -> result
+    e2e = None
+    if not args.no_e2e and rank == 0 and args.mode in ("sample", "greedy"):
+        hv = sv.HostVerifier(B, K, V, dev, sampling=args.mode == "sample")
+        bt = sets[0]
+        hp = bt.p.cpu().pin_memory()
+        hq = bt.q.cpu().pin_memory() if args.mode == "sample" else None
+        ht, hua, hur = (bt.t.cpu().pin_memory(), bt.u_acc.cpu().pin_memory(),
+                        bt.u_res.cpu().pin_memory())
+        run = (lambda: hv.sample(hp, hq, ht, hua, hur)) if args.mode == "sample" else (
+            lambda: hv.greedy(hp, ht))
+        for _ in range(3):
+            run()
+        n_e2e = max(1, min(args.e2e_steps, args.steps))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            run()
+        t1 = time.perf_counter()
+        assert np.array_equal(hv.n_host.numpy(), outs[0][0].cpu().numpy())
+        e2e = {"value": n_e2e / (t1 - t0), "unit": UNIT,
+               "h2d_bytes_per_step": hv.h2d_bytes(args.mode == "sample"),
+               "d2h_bytes_per_step": hv.d2h_bytes(), "steps": n_e2e}
+        del hv, hp, hq
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        host = sets[0].numpy()
+        ncpu = os.cpu_count() or 1
+        rps, nb, rounds, el = time_oracle(host, args.mode, K, args.cpu_seconds, ncpu)
+        cpu = {"value": rps, "unit": UNIT, "cores": ncpu, "kind": "oracle",
+               "sample": f"{rounds} full rounds ({nb} sequences each) of input set 0, "
+                         f"{el:.1f} s on {ncpu} threads"}
+
+    if rank == 0:
+        clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+        line = {
+            "metric": METRIC, "value": rounds_per_s, "unit": UNIT, "n_gpus": world,
+            "steps": steps_done, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; see inputs.py)",
+            "config": workload_config(args, B, K, V, {
+                "l2": (f"rotating {len(sets)} input sets; {len(sets) * req_per_launch / 1e6:.0f} MB"
+                       f" required bytes per rotation = {len(sets) * req_per_launch / l2:.1f}x "
+                       f"L2 ({l2 / 1e6:.0f} MB)"),
+                "launch": "cuda graph" if graph is not None else "one C-ABI call per step",
+                "grid_ctas": int(sv.last_grid_size())}),
+            "seq_rounds_per_s": rounds_per_s * B,
+            "achieved_gbs": achieved * world,
+            "required_bytes_per_round": req_per_launch,
+            "dense_bytes_per_round": float(np.mean(dense)),
+            "n_accepted_hist": nhist.tolist(),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "kernel_us": kernel_us},
+            "gpu_launches": launches,
+            "status_bits": status,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "impl": "gb300",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

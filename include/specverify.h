@@ -1,0 +1,157 @@
+/*
+ * specverify.h -- C ABI of the batched speculative-decoding verification
+ * library (libspecverify.so, CUDA, sm_103a).
+ *
+ * What the calls compute is defined on the "spec-verify" page (Hugging Face
+ * kernels page phanerozoic/spec-verify):
+ *   - section "Usage": n_accepted, next_token = verify_greedy(target_probs
+ *     [K+1, V], draft_tokens [K]); the caller keeps draft_tokens[:n_accepted]
+ *     and appends next_token;
+ *   - section "Method": the greedy rule and the speculative-sampling rule of
+ *     Leviathan et al. / Chen et al., with randomness entering only through
+ *     explicit uniforms;
+ *   - section "Correctness": probabilities need not be normalised and masses
+ *     are summed exactly;
+ *   - section "Requirements and limits": target_probs [K+1, V] f32 and, for
+ *     sampling, draft_probs [K, V] warped identically to the target.
+ * These entry points batch that operation over B independent sequences.
+ *
+ * Common conventions
+ *   Memory.  Every pointer argument is DEVICE memory on the current device,
+ *     owned by the caller, and must stay valid until the stream reaches the
+ *     end of the call.  Inputs are read-only; outputs must not alias inputs.
+ *     The library allocates no memory.
+ *   Layout.  p holds B*(K+1) rows of V f32 target probabilities; row (b, i),
+ *     i in [0, K], starts at p + (b*(K+1) + i) * p_row_stride.  q holds B*K
+ *     rows of draft probabilities; row (b, i), i in [0, K), starts at
+ *     q + (b*K + i) * q_row_stride.  Strides are in elements and >= V.  t,
+ *     u_accept are [B][K] row-major; u_resample, mode, n_accepted, next_token,
+ *     lengths are [B]; tokens is [B][max_len].  Rows whose start is 16-byte
+ *     aligned are read with 16-byte vector loads; others are still correct.
+ *   Values.  Probabilities are finite and >= 0 and need not sum to 1 (NaN or
+ *     negative entries give unspecified results).  u_accept in [0, 1) (f32),
+ *     u_resample in [0, 1) (f64).
+ *   Asynchrony.  Every call only enqueues work on `stream` (NULL = the legacy
+ *     default stream) and returns; nothing is synchronised and nothing is
+ *     copied to the host except by sv_get_status.
+ *   Workspace.  Scratch of sv_workspace_size(B, K, V) bytes, 256-byte
+ *     aligned, zeroed once with sv_workspace_init before its first use.  Each
+ *     call leaves it ready for the next one.  One workspace serves one call at
+ *     a time: calls that share a workspace must be ordered on one stream.
+ *   Return codes.  SV_OK, or a negative SV_E* code for errors detected on the
+ *     host before anything is enqueued (SV_EINVAL: a null pointer, B < 0,
+ *     K < 0 or K > SV_MAX_K, V < 1 or V > 2^31-1, a stride < V, max_len < 1;
+ *     SV_EWORKSPACE: workspace null, misaligned or too small; SV_ECUDA: the
+ *     launch failed).  B = 0 is a no-op.
+ *   Device-detected errors never trap.  The affected sequence gets
+ *     next_token = -1 and a status bit is OR-ed into the workspace's status
+ *     word, read (and cleared) by sv_get_status:
+ *       SV_STATUS_BAD_TOKEN  a draft id outside [0, V): n_accepted = 0,
+ *                            next_token = -1 for that sequence;
+ *       SV_STATUS_ZERO_MASS  the distribution to draw from has zero mass;
+ *       SV_STATUS_OVERFLOW   a commit would pass max_len (nothing written);
+ *       SV_STATUS_BAD_MODE   a round mode other than 0 or 1 (n = 0, next = -1).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *sv_stream_t;
+
+#define SV_OK 0
+#define SV_EINVAL (-1)
+#define SV_EWORKSPACE (-2)
+#define SV_ECUDA (-3)
+
+#define SV_STATUS_BAD_TOKEN 1u
+#define SV_STATUS_ZERO_MASS 2u
+#define SV_STATUS_OVERFLOW 4u
+#define SV_STATUS_BAD_MODE 8u
+
+#define SV_MAX_K 64
+
+/* Bytes of workspace the calls need for B sequences, K drafts, vocabulary V
+ * (0 for invalid sizes).  Covers greedy, sampling and mixed rounds alike. */
+size_t sv_workspace_size(int32_t B, int32_t K, int64_t V);
+
+/* Zeroes a workspace on `stream` (once, before its first use).  Returns
+ * SV_EWORKSPACE for a null or misaligned pointer, SV_ECUDA on failure. */
+int sv_workspace_init(void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* Greedy verification ("spec-verify", section "Method", greedy bullet):
+ * for each sequence b, accepts t[b][i] while it equals argmax(p row (b, i))
+ * (ties go to the lowest index); at the first miss i writes n_accepted[b] = i
+ * and next_token[b] = argmax(p row (b, i)); when all K match writes
+ * n_accepted[b] = K and next_token[b] = argmax(p row (b, K)).  Only the rows
+ * up to the first miss need to be read, and the kernel stops reading the
+ * others once a miss is known.  t may be NULL when K = 0. */
+int sv_verify_greedy(const float *p, int64_t p_row_stride, const int32_t *t,
+                     int32_t B, int32_t K, int64_t V,
+                     int32_t *n_accepted, int32_t *next_token,
+                     void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* Speculative-sampling verification ("spec-verify", section "Method",
+ * sampling bullet; Leviathan et al. / Chen et al.): for i = 0, 1, ... accepts
+ * t[b][i] iff u_accept[b][i] * q_i(t_i) < p_i(t_i), evaluated exactly (raw,
+ * unnormalised values).  At the first rejection i it draws next_token from
+ * max(0, p_i - q_i) by inverse CDF with u_resample[b]: the smallest v whose
+ * running mass exceeds u_resample[b] times the total; if that total is zero it
+ * draws from p_i instead.  When all K are accepted it draws the bonus from p_K
+ * with the same uniform.  Masses are summed with fp64-level accuracy (double
+ * fp32 arithmetic, relative error below 1e-10); the drawn token can differ
+ * from an exact fp64 sum only when u_resample * total lies within that error
+ * of a boundary between two tokens.  q, t, u_accept may be NULL when K = 0. */
+int sv_verify_sample(const float *p, int64_t p_row_stride,
+                     const float *q, int64_t q_row_stride,
+                     const int32_t *t, const float *u_accept, const double *u_resample,
+                     int32_t B, int32_t K, int64_t V,
+                     int32_t *n_accepted, int32_t *next_token,
+                     void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* One verification round over a mixed batch: mode[b] = 0 applies the greedy
+ * rule and mode[b] = 1 the sampling rule to sequence b (other values set
+ * SV_STATUS_BAD_MODE).  If tokens is not NULL the round is also committed
+ * ("spec-verify", section "Usage": keep draft_tokens[:n_accepted], append
+ * next_token): t[b][0..n) and next_token[b] are written to
+ * tokens[b][lengths[b] ..] and lengths[b] grows by n + 1.  A sequence whose
+ * next_token is -1 is not committed; one that would pass max_len is left
+ * unchanged and sets SV_STATUS_OVERFLOW.  q and u_accept are read only for
+ * sampling sequences but must be valid [B][K][..] arrays when K > 0. */
+int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride,
+                    const float *q, int64_t q_row_stride,
+                    const int32_t *t, const float *u_accept, const double *u_resample,
+                    int32_t B, int32_t K, int64_t V,
+                    int32_t *n_accepted, int32_t *next_token,
+                    int32_t *tokens, int32_t *lengths, int32_t max_len,
+                    void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* Waits for `stream`, copies the workspace's status bits to *flags (host
+ * memory) and clears them.  Returns SV_ECUDA if the stream reported an error. */
+int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags);
+
+/* Launch shape used by the calls above.  segs_per_cta is the number of
+ * 1024-element segments of a row one CTA streams (0 restores the automatic
+ * choice); the setting is process-wide and meant for tuning sweeps. */
+int sv_set_segments_per_cta(int32_t segs_per_cta);
+
+/* Number of CTAs the last call on this thread launched (its grid size). */
+int64_t sv_last_grid_size(void);
+
+/* Text for an SV_* return code or SV_STATUS_* bit. */
+const char *sv_status_string(int code);
+
+/* Library ABI version (this header: 1). */
+int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

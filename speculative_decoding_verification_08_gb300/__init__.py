@@ -1,0 +1,341 @@
+"""Batched speculative-decoding verification on GB300 (sm_103a).
+
+Python binding of ``libspecverify.so`` (C ABI in ``include/specverify.h``).
+This module only marshals arguments: torch CUDA tensors are checked for
+dtype, device and layout and their pointers, strides and the current CUDA
+stream are passed to the library, whose kernels do every step of the
+verification.  There is no CPU path: if the library is missing or a tensor is
+not on a CUDA device, the call raises.
+
+The operation is the one on the "spec-verify" page (Hugging Face kernels page
+phanerozoic/spec-verify), section "Usage":
+``n_accepted, next_token = verify_greedy(target_probs, draft_tokens)`` -- keep
+``draft_tokens[:n_accepted]`` and append ``next_token`` -- batched over B
+sequences, plus the speculative-sampling rule of section "Method".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+LIBRARY = _build.LIBRARY
+
+SV_OK = 0
+SV_EINVAL = -1
+SV_EWORKSPACE = -2
+SV_ECUDA = -3
+STATUS_BAD_TOKEN = 1
+STATUS_ZERO_MASS = 2
+STATUS_OVERFLOW = 4
+STATUS_BAD_MODE = 8
+MAX_K = 64
+
+# every symbol include/specverify.h declares
+EXPORTED = (
+    "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
+    "sv_verify_round", "sv_get_status", "sv_set_segments_per_cta", "sv_last_grid_size",
+    "sv_status_string", "sv_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compiles libspecverify.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def load():
+    """The ctypes handle of libspecverify.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIBRARY):
+            raise SpecVerifyError(
+                f"{LIBRARY} is missing: build it with "
+                "speculative_decoding_verification_08_gb300.build() (no CPU fallback exists)")
+        lib = ctypes.CDLL(LIBRARY)
+        P = ctypes.c_void_p
+        i32, i64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.sv_workspace_size.argtypes = [i32, i32, i64]
+        lib.sv_workspace_size.restype = sz
+        lib.sv_workspace_init.argtypes = [P, sz, P]
+        lib.sv_workspace_init.restype = ctypes.c_int
+        lib.sv_verify_greedy.argtypes = [P, i64, P, i32, i32, i64, P, P, P, sz, P]
+        lib.sv_verify_greedy.restype = ctypes.c_int
+        lib.sv_verify_sample.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P, sz, P]
+        lib.sv_verify_sample.restype = ctypes.c_int
+        lib.sv_verify_round.argtypes = [P, P, i64, P, i64, P, P, P, i32, i32, i64, P, P,
+                                        P, P, i32, P, sz, P]
+        lib.sv_verify_round.restype = ctypes.c_int
+        lib.sv_get_status.argtypes = [P, P, P]
+        lib.sv_get_status.restype = ctypes.c_int
+        lib.sv_set_segments_per_cta.argtypes = [i32]
+        lib.sv_set_segments_per_cta.restype = ctypes.c_int
+        lib.sv_last_grid_size.argtypes = []
+        lib.sv_last_grid_size.restype = i64
+        lib.sv_status_string.argtypes = [ctypes.c_int]
+        lib.sv_status_string.restype = ctypes.c_char_p
+        lib.sv_version.argtypes = []
+        lib.sv_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().sv_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != SV_OK:
+        raise SpecVerifyError(f"{what}: {status_string(rc)} (code {rc})")
+
+
+def workspace_size(B: int, K: int, V: int) -> int:
+    return int(load().sv_workspace_size(B, K, V))
+
+
+def set_segments_per_cta(n: int):
+    _check(load().sv_set_segments_per_cta(int(n)), "sv_set_segments_per_cta")
+
+
+def last_grid_size() -> int:
+    return int(load().sv_last_grid_size())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Workspace:
+    """Device scratch for B sequences, K drafts and vocabulary V (zeroed once)."""
+
+    def __init__(self, B: int, K: int, V: int, device=None, stream=None):
+        torch = _torch()
+        nbytes = workspace_size(B, K, V)
+        if nbytes == 0:
+            raise SpecVerifyError(f"invalid sizes B={B} K={K} V={V}")
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.B, self.K, self.V, self.nbytes = B, K, V, nbytes
+        _check(load().sv_workspace_init(self.ptr, nbytes, _stream_handle(stream)),
+               "sv_workspace_init")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    def fits(self, B, K, V) -> bool:
+        return workspace_size(B, K, V) <= self.nbytes
+
+    def status(self, stream=None) -> int:
+        """Waits for the stream and returns (and clears) the device status bits."""
+        out = ctypes.c_uint32(0)
+        _check(load().sv_get_status(self.ptr, _stream_handle(stream), ctypes.byref(out)),
+               "sv_get_status")
+        return int(out.value)
+
+
+_ws_cache = {}
+
+
+def _workspace(ws, B, K, V, device):
+    if ws is not None:
+        if not ws.fits(B, K, V):
+            raise SpecVerifyError("workspace too small for these sizes")
+        return ws
+    key = (str(device), B, K, V)
+    w = _ws_cache.get(key)
+    if w is None:
+        w = Workspace(B, K, V, device)
+        _ws_cache[key] = w
+    return w
+
+
+def _rows3(x, rows, name, dtype):
+    """(tensor viewed as [B][rows][V], B, V, row stride) with the library's layout."""
+    torch = _torch()
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise SpecVerifyError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise SpecVerifyError(f"{name} must be {dtype}, got {x.dtype}")
+    if x.dim() == 2:
+        x = x.unsqueeze(0)
+    if x.dim() != 3 or x.shape[1] != rows:
+        raise SpecVerifyError(f"{name}: expected [B][{rows}][V], got {tuple(x.shape)}")
+    B, _, V = x.shape
+    if x.stride(2) != 1:
+        raise SpecVerifyError(f"{name}: the vocabulary dimension must be contiguous")
+    rs = x.stride(1) if rows > 1 else (x.stride(0) if B > 1 else V)
+    if rows > 1 and B > 1 and x.stride(0) != rows * rs:
+        raise SpecVerifyError(f"{name}: rows of all sequences must be evenly strided")
+    if rs < V:
+        raise SpecVerifyError(f"{name}: row stride {rs} < V={V}")
+    return x, B, V, rs
+
+
+def _vec(x, n, name, dtype, device):
+    torch = _torch()
+    if x is None:
+        return None
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.device != device:
+        raise SpecVerifyError(f"{name} must be a CUDA tensor on {device}")
+    if x.dtype != dtype:
+        raise SpecVerifyError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous() or x.numel() != n:
+        raise SpecVerifyError(f"{name}: expected {n} contiguous elements")
+    return x
+
+
+def _ptr(x):
+    return ctypes.c_void_p(0 if x is None else x.data_ptr())
+
+
+def _outputs(B, device, n_out, next_out):
+    torch = _torch()
+    if n_out is None:
+        n_out = torch.empty(B, dtype=torch.int32, device=device)
+    if next_out is None:
+        next_out = torch.empty(B, dtype=torch.int32, device=device)
+    _vec(n_out, B, "n_accepted", torch.int32, device)
+    _vec(next_out, B, "next_token", torch.int32, device)
+    return n_out, next_out
+
+
+def verify_greedy(p, t, *, ws=None, n_out=None, next_out=None, stream=None):
+    """Greedy verification.  p: [B][K+1][V] (or [K+1][V]) f32, t: [B][K] (or [K])
+    int32 -> (n_accepted [B] int32, next_token [B] int32) on the same device."""
+    torch = _torch()
+    K = t.shape[-1]
+    p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
+    dev = p.device
+    t = _vec(t, B * K, "t", torch.int32, dev)
+    n_out, next_out = _outputs(B, dev, n_out, next_out)
+    w = _workspace(ws, B, K, V, dev)
+    rc = load().sv_verify_greedy(_ptr(p), ps, _ptr(t), B, K, V, _ptr(n_out), _ptr(next_out),
+                                 w.ptr, w.nbytes, _stream_handle(stream))
+    _check(rc, "sv_verify_greedy")
+    return n_out, next_out
+
+
+def verify_sample(p, q, t, u_acc, u_res, *, ws=None, n_out=None, next_out=None, stream=None):
+    """Speculative-sampling verification.  p: [B][K+1][V] f32, q: [B][K][V] f32,
+    t: [B][K] int32, u_acc: [B][K] f32, u_res: [B] f64 -> (n_accepted, next_token)."""
+    torch = _torch()
+    K = t.shape[-1]
+    p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
+    dev = p.device
+    q, Bq, Vq, qs = _rows3(q, K, "q", torch.float32) if K > 0 else (None, B, V, V)
+    if (Bq, Vq) != (B, V):
+        raise SpecVerifyError("q does not match p")
+    t = _vec(t, B * K, "t", torch.int32, dev)
+    u_acc = _vec(u_acc, B * K, "u_acc", torch.float32, dev)
+    u_res = _vec(u_res, B, "u_res", torch.float64, dev)
+    n_out, next_out = _outputs(B, dev, n_out, next_out)
+    w = _workspace(ws, B, K, V, dev)
+    rc = load().sv_verify_sample(_ptr(p), ps, _ptr(q), qs, _ptr(t), _ptr(u_acc), _ptr(u_res),
+                                 B, K, V, _ptr(n_out), _ptr(next_out), w.ptr, w.nbytes,
+                                 _stream_handle(stream))
+    _check(rc, "sv_verify_sample")
+    return n_out, next_out
+
+
+def verify_round(mode, p, q, t, u_acc, u_res, *, tokens=None, lengths=None, ws=None,
+                 n_out=None, next_out=None, stream=None):
+    """Mixed round: mode [B] uint8 (0 greedy, 1 sampling) picks each sequence's
+    rule.  With tokens [B][max_len] int32 and lengths [B] int32 the round is
+    committed in place (t[b][:n] then next appended)."""
+    torch = _torch()
+    K = t.shape[-1]
+    p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
+    dev = p.device
+    q, Bq, Vq, qs = _rows3(q, K, "q", torch.float32) if K > 0 else (None, B, V, V)
+    if (Bq, Vq) != (B, V):
+        raise SpecVerifyError("q does not match p")
+    mode = _vec(mode, B, "mode", torch.uint8, dev)
+    t = _vec(t, B * K, "t", torch.int32, dev)
+    u_acc = _vec(u_acc, B * K, "u_acc", torch.float32, dev)
+    u_res = _vec(u_res, B, "u_res", torch.float64, dev)
+    max_len = 0
+    if tokens is not None:
+        if tokens.dim() != 2 or tokens.shape[0] != B:
+            raise SpecVerifyError("tokens must be [B][max_len]")
+        max_len = tokens.shape[1]
+        _vec(tokens, B * max_len, "tokens", torch.int32, dev)
+        _vec(lengths, B, "lengths", torch.int32, dev)
+    n_out, next_out = _outputs(B, dev, n_out, next_out)
+    w = _workspace(ws, B, K, V, dev)
+    rc = load().sv_verify_round(_ptr(mode), _ptr(p), ps, _ptr(q), qs, _ptr(t), _ptr(u_acc),
+                                _ptr(u_res), B, K, V, _ptr(n_out), _ptr(next_out), _ptr(tokens),
+                                _ptr(lengths), max_len, w.ptr, w.nbytes, _stream_handle(stream))
+    _check(rc, "sv_verify_round")
+    return n_out, next_out
+
+
+class HostVerifier:
+    """Verification of host-resident inputs: each call copies the inputs from
+    (pinned) host tensors into device buffers, runs the kernels and copies
+    (n_accepted, next_token) back, on one stream, and waits for the result."""
+
+    def __init__(self, B: int, K: int, V: int, device=None, sampling: bool = True):
+        torch = _torch()
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.B, self.K, self.V, self.device = B, K, V, dev
+        self.p = torch.empty(B, K + 1, V, dtype=torch.float32, device=dev)
+        self.q = torch.empty(B, K, V, dtype=torch.float32, device=dev) if sampling else None
+        self.t = torch.empty(B, K, dtype=torch.int32, device=dev)
+        self.u_acc = torch.empty(B, K, dtype=torch.float32, device=dev)
+        self.u_res = torch.empty(B, dtype=torch.float64, device=dev)
+        self.n = torch.empty(B, dtype=torch.int32, device=dev)
+        self.next = torch.empty(B, dtype=torch.int32, device=dev)
+        self.n_host = torch.empty(B, dtype=torch.int32, pin_memory=True)
+        self.next_host = torch.empty(B, dtype=torch.int32, pin_memory=True)
+        self.ws = Workspace(B, K, V, dev)
+
+    def h2d_bytes(self, sampling=True) -> int:
+        n = self.p.numel() * 4 + self.t.numel() * 4
+        if sampling:
+            n += self.q.numel() * 4 + self.u_acc.numel() * 4 + self.u_res.numel() * 8
+        return n
+
+    def d2h_bytes(self) -> int:
+        return self.B * 8
+
+    def sample(self, p, q, t, u_acc, u_res):
+        self.p.copy_(p, non_blocking=True)
+        self.q.copy_(q, non_blocking=True)
+        self.t.copy_(t, non_blocking=True)
+        self.u_acc.copy_(u_acc, non_blocking=True)
+        self.u_res.copy_(u_res, non_blocking=True)
+        verify_sample(self.p, self.q, self.t, self.u_acc, self.u_res, ws=self.ws,
+                      n_out=self.n, next_out=self.next)
+        return self._finish()
+
+    def greedy(self, p, t):
+        self.p.copy_(p, non_blocking=True)
+        self.t.copy_(t, non_blocking=True)
+        verify_greedy(self.p, self.t, ws=self.ws, n_out=self.n, next_out=self.next)
+        return self._finish()
+
+    def _finish(self):
+        torch = _torch()
+        self.n_host.copy_(self.n, non_blocking=True)
+        self.next_host.copy_(self.next, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return self.n_host, self.next_host

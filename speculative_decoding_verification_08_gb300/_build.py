@@ -1,0 +1,45 @@
+"""Builds libspecverify.so in-tree with nvcc for sm_103a."""
+from __future__ import annotations
+
+import os
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+INCLUDE = os.path.join(ROOT, "include")
+CSRC = os.path.join(PKG, "csrc")
+SOURCES = [os.path.join(CSRC, "specverify.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(INCLUDE, "specverify.h")]
+LIBRARY = os.path.join(PKG, "libspecverify.so")
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-lineinfo", "-O3", "-std=c++17",
+    "-Xcompiler", "-fPIC", "-shared",
+]
+
+
+def nvcc() -> str:
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    path = os.path.join(home, "bin", "nvcc")
+    return path if os.path.exists(path) else "nvcc"
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIBRARY):
+        return False
+    t = os.path.getmtime(LIBRARY)
+    return all(os.path.getmtime(f) <= t for f in DEPENDS)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles the CUDA library (a few seconds) unless it is up to date."""
+    if not force and up_to_date():
+        return LIBRARY
+    tmp = LIBRARY + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-o", tmp, *SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIBRARY)
+    return LIBRARY

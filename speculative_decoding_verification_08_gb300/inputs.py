@@ -143,12 +143,12 @@ def _cfg2(B, V, K, gen, device):
     p = torch.softmax(torch.randn(B, K + 1, V, generator=gen, device=device) * 3.0, dim=-1)
     a = p.argmax(dim=-1)                                     # [B][K+1]
     hit = torch.rand(B, K, generator=gen, device=device) < 0.7
-    other = (a[:, :K] + torch.randint(1, V, (B, K), generator=gen, device=device)) % V
+    other = (a[:, :K] + torch.randint(1, max(V, 2), (B, K), generator=gen, device=device)) % V
     t = torch.where(hit, a[:, :K], other)
     # exact duplicate of the row maximum at a random other index in 5% of rows
     rows = B * (K + 1)
     planted = torch.rand(rows, generator=gen, device=device) < 0.05
-    d = (a.reshape(-1) + torch.randint(1, V, (rows,), generator=gen, device=device)) % V
+    d = (a.reshape(-1) + torch.randint(1, max(V, 2), (rows,), generator=gen, device=device)) % V
     flip = torch.rand(rows, generator=gen, device=device) < 0.5
     pf = p.view(rows, V)
     idx = planted.nonzero().squeeze(1)
@@ -197,7 +197,7 @@ def _cfg5(B, V, K, gen, device):
         # (q > p there, so that drafting y can be rejected)
         ns = single.numel()
         x = torch.randint(0, V, (ns, K), generator=gen, device=device)
-        y = (x + torch.randint(1, V, (ns, K), generator=gen, device=device)) % V
+        y = (x + torch.randint(1, max(V, 2), (ns, K), generator=gen, device=device)) % V
         rows = p[single, :K].clone()
         px = rows.gather(2, x.unsqueeze(2))
         py = rows.gather(2, y.unsqueeze(2))
@@ -237,7 +237,7 @@ def make_inputs(cfg: int, device="cpu", seed: Optional[int] = None, *, B=None, V
         else:
             out = _cfg5(B, V, K, gen, device)
     p, q, t, u_acc, u_res, mode, meta = out
-    meta.update(seed=seed, name=c["name"])
+    meta.update(seed=seed, name=c["name"].split(" ")[0] + f" B={B} V={V} K={K}")
     return Batch(cfg, B, K, V, p.contiguous(), t.contiguous(),
                  None if q is None else q.contiguous(), u_acc.contiguous(),
                  u_res.contiguous(), mode.contiguous(), meta)

@@ -1,0 +1,307 @@
+"""CUDA path against the CPU oracle, element by element, on the same seeded
+inputs: greedy outputs and accept decisions bit-exact, drawn tokens exact up
+to counted boundary cases (oracle/compare.py).  Needs a GPU (-m gpu)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_08_gb300 as sv
+from speculative_decoding_verification_08_gb300.inputs import make_inputs
+from oracle.compare import compare
+
+pytestmark = pytest.mark.gpu
+
+BOUNDARY_REPORT = []
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sv.build()
+    sv.load()
+    yield
+    if BOUNDARY_REPORT:
+        print("\nboundary-explained resample mismatches:", BOUNDARY_REPORT)
+
+
+def _free():
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def gpu_greedy(bt):
+    n, nx = sv.verify_greedy(bt.p, bt.t)
+    ws = sv._workspace(None, bt.B, bt.K, bt.V, bt.p.device)
+    st = ws.status()
+    return n.cpu().numpy(), nx.cpu().numpy(), st
+
+
+def gpu_sample(bt):
+    n, nx = sv.verify_sample(bt.p, bt.q, bt.t, bt.u_acc, bt.u_res)
+    ws = sv._workspace(None, bt.B, bt.K, bt.V, bt.p.device)
+    st = ws.status()
+    return n.cpu().numpy(), nx.cpu().numpy(), st
+
+
+def gpu_round(bt, mode=None, tokens=None, lengths=None):
+    mode = bt.mode if mode is None else mode
+    n, nx = sv.verify_round(mode, bt.p, bt.q, bt.t, bt.u_acc, bt.u_res, tokens=tokens,
+                            lengths=lengths)
+    ws = sv._workspace(None, bt.B, bt.K, bt.V, bt.p.device)
+    st = ws.status()
+    return n.cpu().numpy(), nx.cpu().numpy(), st
+
+
+def check_greedy(bt, host=None):
+    p, q, t, ua, ur, md = host if host is not None else bt.numpy()
+    n0, x0, s0 = oracle.verify_greedy(p, t, nthreads=8)
+    n1, x1, s1 = gpu_greedy(bt)
+    compare(p, q, ur, 0, bt.K, n0, x0, n1, x1, s0, s1)
+    return n0
+
+
+def check_sample(bt, host=None, label=""):
+    p, q, t, ua, ur, md = host if host is not None else bt.numpy()
+    n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
+    n1, x1, s1 = gpu_sample(bt)
+    bnd = compare(p, q, ur, 1, bt.K, n0, x0, n1, x1, s0, s1)
+    if bnd:
+        BOUNDARY_REPORT.append((label or bt.meta.get("name"), bnd))
+    return n0
+
+
+# ---------------------------------------------------------------------------
+# scaled-down workloads: several segments and CTAs, ragged tails
+
+@pytest.mark.parametrize("V", [1, 3, 31, 1000, 1024, 1025, 4099, 20000 + 37])
+def test_greedy_scaled_ragged(V):
+    bt = make_inputs(2, "cuda", seed=100 + V, B=24, V=V, K=4)
+    check_greedy(bt)
+
+
+@pytest.mark.parametrize("V", [1, 2, 5, 1023, 1024, 1025, 3 * 1024 + 7, 50000 + 3])
+def test_sample_scaled_ragged(V):
+    bt = make_inputs(3, "cuda", seed=200 + V, B=33, V=V, K=5)
+    check_sample(bt, label=f"scaled V={V}")
+
+
+@pytest.mark.parametrize("K", [0, 1, 2, 7, 16, 33, 64])
+def test_draft_lengths(K):
+    bt = make_inputs(4, "cuda", seed=300 + K, B=20, V=2500, K=K)
+    check_greedy(bt)
+    check_sample(bt, label=f"K={K}")
+    p, q, t, ua, ur, md = bt.numpy()
+    n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur)
+    n1, x1, s1 = gpu_round(bt)
+    compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1)
+
+
+def test_edge_distributions_scaled():
+    """Unnormalised rows, q == p, one-hot targets, single-token residuals."""
+    bt = make_inputs(5, "cuda", seed=5000, B=60, V=9000, K=16)
+    n = check_sample(bt, label="edge scaled")
+    check_greedy(bt)
+    same = bt.meta["same"]
+    assert np.all(n[same] == 16)
+
+
+@pytest.mark.parametrize("spc", [1, 2, 3, 8, 16, 64])
+def test_launch_shapes_agree(spc):
+    bt = make_inputs(3, "cuda", seed=777, B=40, V=40000, K=5)
+    host = bt.numpy()
+    try:
+        sv.set_segments_per_cta(spc)
+        check_sample(bt, host, label=f"spc={spc}")
+        check_greedy(bt, host)
+    finally:
+        sv.set_segments_per_cta(0)
+
+
+def test_unaligned_rows_and_strides():
+    """Rows that do not start on 16 bytes take the scalar path; results agree."""
+    B, K, V = 9, 3, 5003
+    bt = make_inputs(3, "cuda", seed=31, B=B, V=V, K=K)
+    p, q, t, ua, ur, md = bt.numpy()
+    n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur)
+    g0 = oracle.verify_greedy(p, t)
+    for pad in (1, 2, 3, 4):
+        Pbig = torch.zeros(B, K + 1, V + pad, device="cuda")
+        Qbig = torch.zeros(B, K, V + pad, device="cuda")
+        Pbig[:, :, :V] = bt.p
+        Qbig[:, :, :V] = bt.q
+        pv, qv = Pbig[:, :, :V], Qbig[:, :, :V]
+        n1, x1 = sv.verify_sample(pv, qv, bt.t, bt.u_acc, bt.u_res)
+        compare(p, q, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy())
+        n2, x2 = sv.verify_greedy(pv, bt.t)
+        compare(p, q, ur, 0, K, g0[0], g0[1], n2.cpu().numpy(), x2.cpu().numpy())
+    # base pointer offset by one element
+    flat = torch.zeros(B * (K + 1) * V + 1, device="cuda")
+    flat[1:] = bt.p.reshape(-1)
+    pv = flat[1:].view(B, K + 1, V)
+    n3, x3 = sv.verify_greedy(pv, bt.t)
+    compare(p, q, ur, 0, K, g0[0], g0[1], n3.cpu().numpy(), x3.cpu().numpy())
+
+
+def test_repeated_calls_are_identical_and_clean():
+    bt = make_inputs(3, "cuda", seed=41, B=50, V=30000, K=5)
+    a = gpu_sample(bt)
+    for _ in range(3):
+        b = gpu_sample(bt)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and b[2] == 0
+    g = gpu_greedy(bt)
+    for _ in range(3):
+        h = gpu_greedy(bt)
+        assert np.array_equal(g[0], h[0]) and np.array_equal(g[1], h[1]) and h[2] == 0
+
+
+def test_error_statuses():
+    B, K, V = 6, 3, 700
+    bt = make_inputs(3, "cuda", seed=51, B=B, V=V, K=K)
+    t = bt.t.clone()
+    t[1, 2] = V
+    t[3, 0] = -5
+    bt.t = t
+    p, q, tt, ua, ur, md = bt.numpy()
+    n0, x0, s0 = oracle.verify_sample(p, q, tt, ua, ur)
+    n1, x1, s1 = gpu_sample(bt)
+    assert s0 == s1 == sv.STATUS_BAD_TOKEN
+    compare(p, q, ur, 1, K, n0, x0, n1, x1)
+    g0 = oracle.verify_greedy(p, tt)
+    n2, x2, s2 = gpu_greedy(bt)
+    assert s2 == sv.STATUS_BAD_TOKEN
+    compare(p, q, ur, 0, K, g0[0], g0[1], n2, x2)
+    # invalid modes
+    mode = torch.tensor([0, 1, 2, 255, 1, 0], dtype=torch.uint8, device="cuda")
+    bt.t = bt.t.clamp(0, V - 1)
+    p, q, tt, ua, ur, md = bt.numpy()
+    n0, x0, s0 = oracle.verify_round(mode.cpu().numpy(), p, q, tt, ua, ur)
+    n1, x1, s1 = gpu_round(bt, mode=mode)
+    assert s0 == s1 == sv.STATUS_BAD_MODE
+    compare(p, q, ur, mode.cpu().numpy(), K, n0, x0, n1, x1)
+
+
+def test_zero_mass_paths():
+    """Rejection with zero residual falls back to p_i; all-zero rows give -1."""
+    B, K, V = 4, 2, 3000
+    p = torch.rand(B, K + 1, V, device="cuda")
+    q = p[:, :K] * 2.0                     # p <= q everywhere: residual mass is zero
+    p[2, 0] = 0.0                           # sequence 2: zero residual and zero p_0
+    p[3, K] = 0.0                           # sequence 3: q == p below, bonus row empty
+    q[3] = p[3, :K]
+    t = torch.randint(0, V, (B, K), device="cuda", dtype=torch.int32)
+    ua = torch.full((B, K), 0.999, device="cuda")
+    ur = torch.rand(B, dtype=torch.float64, device="cuda")
+    n1, x1 = sv.verify_sample(p, q, t, ua, ur)
+    st = sv._workspace(None, B, K, V, p.device).status()
+    n0, x0, s0 = oracle.verify_sample(p.cpu().numpy(), q.cpu().numpy(), t.cpu().numpy(),
+                                      ua.cpu().numpy(), ur.cpu().numpy())
+    assert s0 == st == sv.STATUS_ZERO_MASS
+    compare(p.cpu().numpy(), q.cpu().numpy(), ur.cpu().numpy(), 1, K, n0, x0,
+            n1.cpu().numpy(), x1.cpu().numpy())
+    assert x1[2].item() == -1 and x1[3].item() == -1 and n1[3].item() == K
+
+
+def test_commit_matches_oracle():
+    B, K, V, L = 64, 6, 5000, 20
+    bt = make_inputs(4, "cuda", seed=61, B=B, V=V, K=K)
+    p, q, t, ua, ur, md = bt.numpy()
+    rng = np.random.default_rng(3)
+    lengths0 = rng.integers(0, 15, size=B).astype(np.int32)
+    tokens0 = np.full((B, L), -9, np.int32)
+    n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur)
+    tok_ref, len_ref = tokens0.copy(), lengths0.copy()
+    sc = oracle.commit(t, n0, x0, tok_ref, len_ref)
+    tok = torch.from_numpy(tokens0).cuda()
+    lens = torch.from_numpy(lengths0).cuda()
+    n1, x1, s1 = gpu_round(bt, tokens=tok, lengths=lens)
+    bnd = compare(p, q, ur, md, K, n0, x0, n1, x1)
+    assert s1 == (s0 | sc)
+    if not bnd:
+        assert np.array_equal(tok.cpu().numpy(), tok_ref)
+        assert np.array_equal(lens.cpu().numpy(), len_ref)
+
+
+def test_boundary_thresholds_are_counted_not_wrong():
+    """Uniforms placed exactly on the oracle's CDF boundaries: the GPU may pick
+    either neighbour, and every difference must be boundary-explained."""
+    B, K, V = 64, 1, 4096
+    g = torch.Generator(device="cuda").manual_seed(9)
+    p = torch.rand(B, K + 1, V, device="cuda", generator=g)
+    q = torch.rand(B, K, V, device="cuda", generator=g)
+    t = torch.zeros(B, K, dtype=torch.int32, device="cuda")
+    q[:, 0, 0] = 10.0                       # draft token 0 is always rejected
+    ua = torch.full((B, K), 0.5, device="cuda")
+    ph, qh = p.cpu().numpy(), q.cpu().numpy()
+    ur = np.empty(B)
+    rng = np.random.default_rng(2)
+    for b in range(B):
+        C, R = oracle.residual_cumsum(ph[b, 0], qh[b, 0])
+        k = int(rng.integers(1, V - 1))
+        ur[b] = C[k] / R
+    u = torch.from_numpy(ur).cuda()
+    n1, x1 = sv.verify_sample(p, q, t, ua, u)
+    n0, x0, s0 = oracle.verify_sample(ph, qh, t.cpu().numpy(), ua.cpu().numpy(), ur)
+    bnd = compare(ph, qh, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy())
+    BOUNDARY_REPORT.append(("boundary stress", len(bnd)))
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads (the bench's launch configuration), every output checked
+
+def test_single_sequence_600_rounds():
+    """The single-sequence workload: 600 independent B=1 rounds, greedy and sampling."""
+    bt = make_inputs(1, "cuda", seed=20261201, B=600)
+    check_sample(bt, label="single-seq batch")
+    check_greedy(bt)
+    p, q, t, ua, ur, md = bt.numpy()
+    n0, x0, _ = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
+    for r in range(0, 600, 37):      # the B=1 launch itself
+        n1, x1 = sv.verify_sample(bt.p[r:r + 1], bt.q[r:r + 1], bt.t[r:r + 1],
+                                  bt.u_acc[r:r + 1], bt.u_res[r:r + 1])
+        compare(p[r:r + 1], q[r:r + 1], ur[r:r + 1], 1, 4, n0[r:r + 1], x0[r:r + 1],
+                n1.cpu().numpy(), x1.cpu().numpy())
+
+
+def test_greedy_batched_full():
+    bt = make_inputs(2, "cuda")
+    n = check_greedy(bt)
+    assert bt.meta["planted_rows"] > 0 and bt.meta["higher_dup_drafts"] > 0
+    assert len(set(n.tolist())) > 2
+    del bt
+    _free()
+
+
+def test_sampling_batched_full():
+    """Headline workload B=256, V=128256, K=5: every output against the oracle."""
+    bt = make_inputs(3, "cuda")
+    host = bt.numpy()
+    check_sample(bt, host, label="sampling B=256 V=128256 K=5")
+    check_greedy(bt, host)
+    del bt
+    _free()
+
+
+def test_mixed_round_full():
+    bt = make_inputs(4, "cuda")
+    p, q, t, ua, ur, md = bt.numpy()
+    n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur, nthreads=16)
+    n1, x1, s1 = gpu_round(bt)
+    bnd = compare(p, q, ur, md, bt.K, n0, x0, n1, x1, s0, s1)
+    if bnd:
+        BOUNDARY_REPORT.append(("mixed B=1024", bnd))
+    counts = np.bincount(n0, minlength=bt.K + 1)
+    assert counts[0] > 0 and counts[bt.K] > 0
+    del bt
+    _free()
+
+
+def test_edge_full():
+    bt = make_inputs(5, "cuda")
+    host = bt.numpy()
+    n = check_sample(bt, host, label="edge B=128 V=262144 K=16")
+    check_greedy(bt, host)
+    assert np.all(n[bt.meta["same"]] == 16)
+    del bt
+    _free()
