@@ -132,6 +132,36 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride,
                     int32_t *tokens, int32_t *lengths, int32_t max_len,
                     void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
+/* Allocation-free sampling verification.  The pages have no counterpart to
+ * this entry point; it exists for callers that cannot allocate device memory
+ * at call time: code that enqueues work from inside a framework hook or
+ * plugin interface that forbids allocation while enqueuing, and serving loops
+ * that must not call cudaMalloc because it can synchronise the device or fail
+ * under memory pressure at the worst moment.
+ *
+ * It computes exactly what sv_verify_sample computes (same kernel, same
+ * arguments minus the workspace) but takes its scratch from a fixed array of
+ * SV_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the library: every GPU that
+ * loads the library holds that array until the process exits.  Sizes whose
+ * sv_workspace_size(B, K, V) exceeds it are rejected with SV_ETOOLARGE before
+ * anything is enqueued (at V = 128256, K = 5 that is about 3900 sequences).
+ * The call allocates nothing: it issues one cudaMemsetAsync that clears the
+ * part of the array that must start at zero, then the kernel launch.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array, which keeps the previous call's
+ * contents: two calls whose work overlaps on the GPU (different streams, or
+ * different host threads without ordering) race on it and give wrong results.
+ * Device-detected errors show up as next_token = -1; their status bits are not
+ * reported by this entry point. */
+#define SV_ETOOLARGE (-4)
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
+int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride,
+                             const float *q, int64_t q_row_stride,
+                             const int32_t *t, const float *u_accept,
+                             const double *u_resample, int32_t B, int32_t K, int64_t V,
+                             int32_t *n_accepted, int32_t *next_token, sv_stream_t stream);
+
 /* Waits for `stream`, copies the workspace's status bits to *flags (host
  * memory) and clears them.  Returns SV_ECUDA if the stream reported an error. */
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags);

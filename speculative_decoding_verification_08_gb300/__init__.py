@@ -27,6 +27,8 @@ SV_OK = 0
 SV_EINVAL = -1
 SV_EWORKSPACE = -2
 SV_ECUDA = -3
+SV_ETOOLARGE = -4
+NOALLOC_SCRATCH_BYTES = 4 << 20
 STATUS_BAD_TOKEN = 1
 STATUS_ZERO_MASS = 2
 STATUS_OVERFLOW = 4
@@ -37,7 +39,7 @@ MAX_K = 64
 EXPORTED = (
     "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
     "sv_verify_round", "sv_get_status", "sv_set_segments_per_cta", "sv_last_grid_size",
-    "sv_status_string", "sv_version",
+    "sv_status_string", "sv_version", "sv_verify_sample_noalloc",
 )
 
 _lock = threading.Lock()
@@ -87,6 +89,8 @@ def load():
         lib.sv_status_string.restype = ctypes.c_char_p
         lib.sv_version.argtypes = []
         lib.sv_version.restype = ctypes.c_int
+        lib.sv_verify_sample_noalloc.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P]
+        lib.sv_verify_sample_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -253,6 +257,32 @@ def verify_sample(p, q, t, u_acc, u_res, *, ws=None, n_out=None, next_out=None, 
                                  B, K, V, _ptr(n_out), _ptr(next_out), w.ptr, w.nbytes,
                                  _stream_handle(stream))
     _check(rc, "sv_verify_sample")
+    return n_out, next_out
+
+
+def verify_sample_noalloc(p, q, t, u_acc, u_res, *, n_out=None, next_out=None, stream=None):
+    """verify_sample without a workspace, for callers that cannot allocate
+    device memory while enqueueing work (framework hooks or plugin interfaces
+    that forbid allocation, serving loops that must not risk a synchronising
+    or failing cudaMalloc).  The scratch is a fixed 4 MiB array inside the
+    library; larger sizes raise (SV_ETOOLARGE).  Calls share that array, so
+    calls that overlap on the GPU race.  Pass n_out/next_out to avoid the two
+    output allocations this wrapper would otherwise make."""
+    torch = _torch()
+    K = t.shape[-1]
+    p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
+    dev = p.device
+    q, Bq, Vq, qs = _rows3(q, K, "q", torch.float32) if K > 0 else (None, B, V, V)
+    if (Bq, Vq) != (B, V):
+        raise SpecVerifyError("q does not match p")
+    t = _vec(t, B * K, "t", torch.int32, dev)
+    u_acc = _vec(u_acc, B * K, "u_acc", torch.float32, dev)
+    u_res = _vec(u_res, B, "u_res", torch.float64, dev)
+    n_out, next_out = _outputs(B, dev, n_out, next_out)
+    rc = load().sv_verify_sample_noalloc(_ptr(p), ps, _ptr(q), qs, _ptr(t), _ptr(u_acc),
+                                         _ptr(u_res), B, K, V, _ptr(n_out), _ptr(next_out),
+                                         _stream_handle(stream))
+    _check(rc, "sv_verify_sample_noalloc")
     return n_out, next_out
 
 

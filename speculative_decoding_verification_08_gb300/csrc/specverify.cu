@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "sv_device.cuh"
 #include "specverify.h"
@@ -216,6 +217,7 @@ int64_t sv_last_grid_size(void) { return g_last_grid; }
 
 const char *sv_status_string(int code) {
     switch (code) {
+        case SV_ETOOLARGE: return "sizes exceed the 4 MiB static scratch of sv_verify_sample_noalloc";
         case SV_OK: return "ok";
         case SV_EINVAL: return "invalid argument";
         case SV_EWORKSPACE: return "workspace missing, misaligned or too small";
@@ -231,3 +233,60 @@ const char *sv_status_string(int code) {
 int sv_version(void) { return 1; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: the sampling kernel with its scratch in a fixed
+// device array instead of a caller-provided workspace, for callers that cannot
+// allocate device memory while they enqueue work.
+
+static __device__ __align__(256) unsigned char sv_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of sv_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a host-side stand-in, so
+// the kernel must be given this address, never the name.
+int noalloc_scratch_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return SV_ECUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, sv_noalloc_scratch) != cudaSuccess || !ptr)
+            return SV_ECUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return SV_OK;
+}
+
+}  // namespace
+
+extern "C" int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride, const float *q,
+                                        int64_t q_row_stride, const int32_t *t,
+                                        const float *u_accept, const double *u_resample,
+                                        int32_t B, int32_t K, int64_t V, int32_t *n_accepted,
+                                        int32_t *next_token, sv_stream_t stream) {
+    int rc = common_checks(p, p_row_stride, t, B, K, V, n_accepted, next_token);
+    if (rc != SV_OK || B == 0) return rc;
+    if (!u_resample) return SV_EINVAL;
+    if (K > 0 && (!q || !u_accept || q_row_stride < V)) return SV_EINVAL;
+    const Layout L = layout(B, K, V);
+    if (L.total > (size_t)SV_NOALLOC_SCRATCH_BYTES) return SV_ETOOLARGE;
+    void *scratch = nullptr;
+    if ((rc = noalloc_scratch_address(&scratch)) != SV_OK) return rc;
+    // status, tickets, miss flags and keys must start at zero; the array keeps
+    // whatever the previous call (possibly with other sizes) left there
+    if (cudaMemsetAsync(scratch, 0, L.seg, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return SV_ECUDA;
+    sv::Params P = make_params(p, p_row_stride, q, q_row_stride, t, u_accept, u_resample,
+                               nullptr, B, K, V, n_accepted, next_token);
+    if ((rc = bind_workspace(P, scratch, SV_NOALLOC_SCRATCH_BYTES)) != SV_OK) return rc;
+    return launch(sv::kSample, P, stream);
+}
