@@ -33,6 +33,8 @@ FALLBACK_HBM_GBS = 6800.0
 DEFAULT_MODE = {1: "sample", 2: "greedy", 3: "sample", 4: "round", 5: "sample"}
 KERNEL_SOURCES = [
     "speculative_decoding_verification_08_gb300/csrc/sv_device.cuh",
+    "speculative_decoding_verification_08_gb300/csrc/sv_tma.cuh",
+    "speculative_decoding_verification_08_gb300/csrc/sv_seq.cuh",
     "speculative_decoding_verification_08_gb300/csrc/specverify.cu",
 ]
 
@@ -47,7 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--mode", choices=["sample", "greedy", "round"], default=None)
     ap.add_argument("--sets", type=int, default=4, help="input sets rotated through")
     ap.add_argument("--graph", action="store_true", help="replay the steps from a CUDA graph")
-    ap.add_argument("--segs-per-cta", type=int, default=0)
+    ap.add_argument("--ctas-per-sm", type=int, default=0, help="persistent grid residency (0 = max)")
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -331,8 +333,8 @@ def main(argv=None):
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     sv.build()
     lib = sv.load()
-    if args.segs_per_cta:
-        sv.set_segments_per_cta(args.segs_per_cta)
+    if args.ctas_per_sm:
+        sv.set_ctas_per_sm(args.ctas_per_sm)
 
     c = CONFIGS[args.config]
     B, K, V = c["B"], c["K"], c["V"]

@@ -50,7 +50,9 @@
  *                            next_token = -1 for that sequence;
  *       SV_STATUS_ZERO_MASS  the distribution to draw from has zero mass;
  *       SV_STATUS_OVERFLOW   a commit would pass max_len (nothing written);
- *       SV_STATUS_BAD_MODE   a round mode other than 0 or 1 (n = 0, next = -1).
+ *       SV_STATUS_BAD_MODE   a round mode other than 0 or 1 (n = 0, next = -1);
+ *       SV_STATUS_TIMEOUT    a bounded wait inside a kernel gave up (the
+ *                            round's outputs are not meaningful).
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -74,6 +76,7 @@ typedef struct CUstream_st *sv_stream_t;
 #define SV_STATUS_ZERO_MASS 2u
 #define SV_STATUS_OVERFLOW 4u
 #define SV_STATUS_BAD_MODE 8u
+#define SV_STATUS_TIMEOUT 16u
 
 #define SV_MAX_K 64
 
@@ -144,7 +147,7 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride,
  * SV_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the library: every GPU that
  * loads the library holds that array until the process exits.  Sizes whose
  * sv_workspace_size(B, K, V) exceeds it are rejected with SV_ETOOLARGE before
- * anything is enqueued (at V = 128256, K = 5 that is about 3900 sequences).
+ * anything is enqueued (at V = 128256, K = 5 that is 457 sequences).
  * The call allocates nothing: it issues one cudaMemsetAsync that clears the
  * part of the array that must start at zero, then the kernel launch.
  * The first call on a device looks up the array's device address (with that
@@ -166,10 +169,12 @@ int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride,
  * memory) and clears them.  Returns SV_ECUDA if the stream reported an error. */
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags);
 
-/* Launch shape used by the calls above.  segs_per_cta is the number of
- * 1024-element segments of a row one CTA streams (0 restores the automatic
- * choice); the setting is process-wide and meant for tuning sweeps. */
-int sv_set_segments_per_cta(int32_t segs_per_cta);
+/* Launch shape used by the calls above.  The kernels are persistent: their
+ * grid holds ctas_per_sm CTAs of 256 threads per SM (0, the default, uses the
+ * largest count the SMs can hold at once), and each warp works through
+ * 1024-element segments of the batch.  The setting is process-wide and meant
+ * for tuning sweeps. */
+int sv_set_ctas_per_sm(int32_t ctas_per_sm);
 
 /* Number of CTAs the last call on this thread launched (its grid size). */
 int64_t sv_last_grid_size(void);

@@ -33,12 +33,13 @@ STATUS_BAD_TOKEN = 1
 STATUS_ZERO_MASS = 2
 STATUS_OVERFLOW = 4
 STATUS_BAD_MODE = 8
+STATUS_TIMEOUT = 16
 MAX_K = 64
 
 # every symbol include/specverify.h declares
 EXPORTED = (
     "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
-    "sv_verify_round", "sv_get_status", "sv_set_segments_per_cta", "sv_last_grid_size",
+    "sv_verify_round", "sv_get_status", "sv_set_ctas_per_sm", "sv_last_grid_size",
     "sv_status_string", "sv_version", "sv_verify_sample_noalloc",
 )
 
@@ -81,8 +82,8 @@ def load():
         lib.sv_verify_round.restype = ctypes.c_int
         lib.sv_get_status.argtypes = [P, P, P]
         lib.sv_get_status.restype = ctypes.c_int
-        lib.sv_set_segments_per_cta.argtypes = [i32]
-        lib.sv_set_segments_per_cta.restype = ctypes.c_int
+        lib.sv_set_ctas_per_sm.argtypes = [i32]
+        lib.sv_set_ctas_per_sm.restype = ctypes.c_int
         lib.sv_last_grid_size.argtypes = []
         lib.sv_last_grid_size.restype = i64
         lib.sv_status_string.argtypes = [ctypes.c_int]
@@ -108,8 +109,9 @@ def workspace_size(B: int, K: int, V: int) -> int:
     return int(load().sv_workspace_size(B, K, V))
 
 
-def set_segments_per_cta(n: int):
-    _check(load().sv_set_segments_per_cta(int(n)), "sv_set_segments_per_cta")
+def set_ctas_per_sm(n: int):
+    """Persistent-grid residency override (0 = as many CTAs as the SMs hold)."""
+    _check(load().sv_set_ctas_per_sm(int(n)), "sv_set_ctas_per_sm")
 
 
 def last_grid_size() -> int:

@@ -9,7 +9,9 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "specverify.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(INCLUDE, "specverify.h")]
+DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "sv_tma.cuh"),
+                     os.path.join(CSRC, "sv_seq.cuh"),
+                     os.path.join(INCLUDE, "specverify.h")]
 LIBRARY = os.path.join(PKG, "libspecverify.so")
 
 NVCC_FLAGS = [

@@ -7,11 +7,19 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
 #include "sv_device.cuh"
+#include "sv_seq.cuh"
 #include "specverify.h"
+
+// 1: large batches of 16-byte-aligned rows run as one sequence-per-CTA launch;
+// 0: they take the three-launch chunked path.  Both give identical results.
+#ifndef SV_SEQ_PATH
+#define SV_SEQ_PATH 1
+#endif
 
 namespace {
 
@@ -25,72 +33,210 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
     return B >= 0 && K >= 0 && K <= SV_MAX_K && V >= 1 && V <= INT32_MAX;
 }
 
-// Workspace layout: [status | ticket[B] | miss[B] | best[B][K+1] | seg[B][nseg]],
-// every region 256-byte aligned.
+// Workspace layout:
+// [status, queue | miss[B] | nstate[B] | ptok[B][K] | best[B][K+1] | seg[B][nseg] |
+//  blk[B][nseg][8] | udd[B]], every region 256-byte aligned; everything before
+// seg must start at zero (and every call leaves it so).
 struct Layout {
-    size_t status, ticket, miss, best, seg, total;
+    size_t status, queue, miss, nstate, ptok, best, seg, blk, udd, total;
 };
 
 Layout layout(int32_t B, int32_t K, int64_t V) {
     Layout L;
     size_t off = 0;
     L.status = off;
+    L.queue = off + sizeof(uint32_t);
     off += kAlign;
-    L.ticket = off;
-    off += round_up((size_t)B * sizeof(uint32_t));
     L.miss = off;
     off += round_up((size_t)B * sizeof(int32_t));
+    L.nstate = off;
+    off += round_up((size_t)B * sizeof(int32_t));
+    L.ptok = off;
+    off += round_up((size_t)B * (size_t)K * sizeof(float));
     L.best = off;
     off += round_up((size_t)B * (size_t)(K + 1) * sizeof(unsigned long long));
     L.seg = off;
     off += round_up((size_t)B * (size_t)num_segments(V) * sizeof(float2));
+    L.blk = off;
+    off += round_up((size_t)B * (size_t)num_segments(V) * sv::kBlocks * sizeof(float2));
+    L.udd = off;
+    off += round_up((size_t)B * sizeof(float2));
     L.total = off;
     return L;
 }
 
-std::atomic<int32_t> g_segs_per_cta{0};
+std::atomic<int32_t> g_ctas_per_sm{0};
 thread_local int64_t g_last_grid = 0;
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 152;
+struct DeviceInfo {
+    int sms = 0;
+    int occupancy[3] = {0, 0, 0};      // resident CTAs per SM, register stream kernels
+    int tma_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, bulk-copy stream kernels
+    int seq_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, sequence-per-CTA kernels
+};
+
+template <int kRule>
+int seq_occupancy_of() {
+    if (cudaFuncSetAttribute(sv::seq_round_kernel<kRule>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sv::kSeqSmemBytes) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv::seq_round_kernel<kRule>,
+                                                      sv::kSeqThreads,
+                                                      sv::kSeqSmemBytes) != cudaSuccess)
+        return 0;
     return n;
 }
 
-// Segments per CTA: 16 (two per warp) when the batch alone fills the GPU a few
-// times over, fewer when B is small so that every SM still gets work.
-int32_t choose_spc(int32_t B, int64_t nseg) {
-    int32_t forced = g_segs_per_cta.load();
-    if (forced > 0) return forced;
-    const int64_t want_ctas = (int64_t)sm_count() * 8;
-    int64_t spc = 16;
-    while (spc > 1 && (int64_t)B * ((nseg + spc - 1) / spc) < want_ctas) spc >>= 1;
-    return (int32_t)spc;
+template <int kRule>
+int tma_occupancy_of() {
+    if (cudaFuncSetAttribute(sv::tma_stream_kernel<kRule>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sv::kTmaSmemBytes) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv::tma_stream_kernel<kRule>,
+                                                      sv::kTmaThreads,
+                                                      sv::kTmaSmemBytes) != cudaSuccess)
+        return 0;
+    return n;
 }
 
+std::mutex g_info_mu;
+DeviceInfo g_info[64];
+
+template <int kRule>
+int occupancy_of() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv::stream_kernel<kRule>, sv::kThreads,
+                                                      0) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// SM count and per-kernel residency of the current device, queried once.
+bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *seq_occ) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(g_info_mu);
+    DeviceInfo &d = g_info[dev];
+    if (d.sms == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return false;
+        d.occupancy[sv::kGreedy] = occupancy_of<sv::kGreedy>();
+        d.occupancy[sv::kSample] = occupancy_of<sv::kSample>();
+        d.occupancy[sv::kPerSequence] = occupancy_of<sv::kPerSequence>();
+        d.tma_occupancy[sv::kGreedy] = tma_occupancy_of<sv::kGreedy>();
+        d.tma_occupancy[sv::kSample] = tma_occupancy_of<sv::kSample>();
+        d.tma_occupancy[sv::kPerSequence] = tma_occupancy_of<sv::kPerSequence>();
+        d.seq_occupancy[sv::kGreedy] = seq_occupancy_of<sv::kGreedy>();
+        d.seq_occupancy[sv::kSample] = seq_occupancy_of<sv::kSample>();
+        d.seq_occupancy[sv::kPerSequence] = seq_occupancy_of<sv::kPerSequence>();
+        d.sms = n;
+    }
+    *sms = d.sms;
+    *occ = d.occupancy[rule] > 0 ? d.occupancy[rule] : 1;
+    *tma_occ = d.tma_occupancy[rule];
+    *seq_occ = d.seq_occupancy[rule];
+    return true;
+}
+
+// Launches kernel on stream st as a programmatic dependent of the previous
+// launch: it may be scheduled while that grid's CTAs retire and waits on the
+// device (griddepcontrol.wait) before it reads their results.
+template <class Kernel>
+int launch_dependent(Kernel kernel, unsigned grid, unsigned threads, size_t smem,
+                     const sv::Params &P, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, P) == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+bool aligned_rows(const float *base, int64_t stride) {
+    return base && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && (stride & 3) == 0;
+}
+
+// One round: three kernels chained on the stream -- scan (per-sequence data),
+// stream (the bulk-copy pipeline when every row is 16-byte aligned, else the
+// register path), decide.  The later two are programmatic dependents.
+template <int kRule>
+int launch_round(const sv::Params &P, bool tma, unsigned grid, cudaStream_t st) {
+    const unsigned per_seq = (unsigned)((P.B + sv::kWarps - 1) / sv::kWarps);
+    sv::scan_kernel<kRule><<<per_seq, sv::kThreads, 0, st>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
+    const int rc = tma ? launch_dependent(sv::tma_stream_kernel<kRule>, grid, sv::kTmaThreads,
+                                          sv::kTmaSmemBytes, P, st)
+                       : launch_dependent(sv::stream_kernel<kRule>, grid, sv::kThreads, 0, P, st);
+    if (rc != SV_OK) return rc;
+    const unsigned decide_grid = (unsigned)((P.B + sv::kDecideWarps - 1) / sv::kDecideWarps);
+    return launch_dependent(sv::decide_kernel<kRule>, decide_grid, sv::kDecideWarps * 32, 0, P, st);
+}
+
+// Picks the round's kernels.  With every row 16-byte aligned and at least one
+// sequence per SM: one persistent kernel in which each CTA owns whole
+// sequences.  With aligned rows and fewer sequences: scan -> bulk-copy stream
+// over chunks of segments -> decide.  Otherwise: scan -> register stream ->
+// decide.  Persistent grids hold as many CTAs as the SMs fit at once (or the
+// tuning override), never more than there is work for.
 int launch(int rule, sv::Params P, sv_stream_t stream) {
     const int64_t nseg = num_segments(P.V);
+    const int64_t items = (int64_t)P.B * nseg;
+    if (items > INT32_MAX / 2) return SV_EINVAL;
     P.nseg = (int32_t)nseg;
-    P.spc = choose_spc(P.B, nseg);
-    P.chunks = (int32_t)((nseg + P.spc - 1) / P.spc);
-    const int64_t grid = (int64_t)P.B * P.chunks;
-    if (grid > INT32_MAX) return SV_EINVAL;
-    g_last_grid = grid;
+    P.items = (int32_t)items;
+    const int64_t cps = (nseg + sv::kChunkSegs - 1) / sv::kChunkSegs;
+    P.nchunks = (int32_t)((int64_t)P.B * cps);
+    int sms = 0, occ = 0, tma_occ = 0, seq_occ = 0;
+    if (!device_info(rule, &sms, &occ, &tma_occ, &seq_occ)) return SV_ECUDA;
+    const bool aligned = aligned_rows(P.p, P.ps) &&
+                         (rule == sv::kGreedy || P.K == 0 || aligned_rows(P.q, P.qs));
+    const int32_t forced = g_ctas_per_sm.load();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    switch (rule) {
-        case sv::kGreedy:
-            sv::verify_kernel<sv::kGreedy><<<(unsigned)grid, sv::kThreads, 0, st>>>(P);
-            break;
-        case sv::kSample:
-            sv::verify_kernel<sv::kSample><<<(unsigned)grid, sv::kThreads, 0, st>>>(P);
-            break;
-        default:
-            sv::verify_kernel<sv::kPerSequence><<<(unsigned)grid, sv::kThreads, 0, st>>>(P);
-            break;
+    if (SV_SEQ_PATH && aligned && seq_occ > 0 && P.B >= sms) {
+        const int64_t grid = (int64_t)sms * (forced > 0 ? std::min<int64_t>(forced, seq_occ) : seq_occ);
+        P.warps = (int32_t)(grid * sv::kWarps);
+        g_last_grid = grid;
+        switch (rule) {
+            case sv::kGreedy:
+                sv::seq_round_kernel<sv::kGreedy><<<(unsigned)grid, sv::kSeqThreads, sv::kSeqSmemBytes, st>>>(P);
+                break;
+            case sv::kSample:
+                sv::seq_round_kernel<sv::kSample><<<(unsigned)grid, sv::kSeqThreads, sv::kSeqSmemBytes, st>>>(P);
+                break;
+            default:
+                sv::seq_round_kernel<sv::kPerSequence>
+                    <<<(unsigned)grid, sv::kSeqThreads, sv::kSeqSmemBytes, st>>>(P);
+                break;
+        }
+        return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
     }
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+    const bool tma = aligned && tma_occ > 0;
+    int64_t grid;
+    if (tma) {
+        grid = (int64_t)sms * (forced > 0 ? std::min<int64_t>(forced, tma_occ) : tma_occ);
+        if (grid > P.nchunks) grid = P.nchunks;
+    } else {
+        grid = (int64_t)sms * (forced > 0 ? forced : occ);
+        const int64_t needed = (items + sv::kWarps - 1) / sv::kWarps;
+        if (grid > needed) grid = needed;
+    }
+    P.warps = (int32_t)(grid * sv::kWarps);
+    g_last_grid = grid;
+    switch (rule) {
+        case sv::kGreedy: return launch_round<sv::kGreedy>(P, tma, (unsigned)grid, st);
+        case sv::kSample: return launch_round<sv::kSample>(P, tma, (unsigned)grid, st);
+        default: return launch_round<sv::kPerSequence>(P, tma, (unsigned)grid, st);
+    }
 }
 
 int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
@@ -99,10 +245,14 @@ int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
     if (bytes < L.total) return SV_EWORKSPACE;
     char *base = static_cast<char *>(ws);
     P.status = reinterpret_cast<uint32_t *>(base + L.status);
-    P.ticket = reinterpret_cast<uint32_t *>(base + L.ticket);
     P.miss = reinterpret_cast<int32_t *>(base + L.miss);
+    P.nstate = reinterpret_cast<int32_t *>(base + L.nstate);
+    P.queue = reinterpret_cast<uint32_t *>(base + L.queue);
+    P.ptok = reinterpret_cast<float *>(base + L.ptok);
     P.best = reinterpret_cast<unsigned long long *>(base + L.best);
     P.seg = reinterpret_cast<float2 *>(base + L.seg);
+    P.blk = reinterpret_cast<float2 *>(base + L.blk);
+    P.udd = reinterpret_cast<float2 *>(base + L.udd);
     return SV_OK;
 }
 
@@ -207,9 +357,9 @@ int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags) {
     return SV_OK;
 }
 
-int sv_set_segments_per_cta(int32_t segs_per_cta) {
-    if (segs_per_cta < 0) return SV_EINVAL;
-    g_segs_per_cta.store(segs_per_cta);
+int sv_set_ctas_per_sm(int32_t ctas_per_sm) {
+    if (ctas_per_sm < 0) return SV_EINVAL;
+    g_ctas_per_sm.store(ctas_per_sm);
     return SV_OK;
 }
 
@@ -226,6 +376,7 @@ const char *sv_status_string(int code) {
         case (int)SV_STATUS_ZERO_MASS: return "distribution to draw from has zero mass";
         case (int)SV_STATUS_OVERFLOW: return "commit would pass max_len";
         case (int)SV_STATUS_BAD_MODE: return "round mode other than 0 (greedy) or 1 (sampling)";
+        case (int)SV_STATUS_TIMEOUT: return "a bounded wait inside a kernel gave up";
         default: return "unknown code";
     }
 }
@@ -280,7 +431,7 @@ extern "C" int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride, co
     if (L.total > (size_t)SV_NOALLOC_SCRATCH_BYTES) return SV_ETOOLARGE;
     void *scratch = nullptr;
     if ((rc = noalloc_scratch_address(&scratch)) != SV_OK) return rc;
-    // status, tickets, miss flags and keys must start at zero; the array keeps
+    // status, miss flags, cached n and keys must start at zero; the array keeps
     // whatever the previous call (possibly with other sizes) left there
     if (cudaMemsetAsync(scratch, 0, L.seg, reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)

@@ -1,29 +1,37 @@
 // sv_device.cuh -- device code of the batched speculative-decoding
 // verification kernels (sm_103a).
 //
-// One launch verifies B sequences.  The grid is B x C CTAs: CTA (b, c) owns
-// chunk c of every row of sequence b, where a row of V probabilities is cut
-// into 1024-element segments and a chunk is a run of consecutive segments.
-// Each warp streams whole segments with 16-byte loads; no CTA ever waits on
-// another.  The last CTA of a sequence to finish (atomic ticket) reads the
-// per-row or per-segment partials the others left in the workspace and writes
-// that sequence's (n_accepted, next_token).
+// One round is two launches on one stream.
 //
-//  * Greedy rule ("spec-verify" page, section "Method", greedy bullet): CTA
-//    (b, c) walks rows 0, 1, ... of sequence b, keeping for its chunk the
-//    largest value and its lowest index.  As soon as any lane has seen an
+// 1. The stream kernel.  A row of V probabilities is cut into 1024-element
+//    segments; the unit of work ("item") is one segment of one sequence,
+//    items are numbered sequence-major, and the launch is persistent: its
+//    grid is sized to what the SMs hold at once and warp w of W takes items
+//    w, w + W, w + 2W, ...  Warps work independently, stream their segment
+//    with 16-byte non-coherent loads and leave a partial result in the
+//    workspace.  Nothing on this path waits or fences: partials are plain
+//    stores or relaxed atomics.
+// 2. The decide kernel, one warp per sequence, launched as a programmatic
+//    dependent of the first (it starts when the stream kernel's CTAs retire
+//    and waits in griddepcontrol.wait until all their writes are visible).
+//    It reads the partials and writes (n_accepted, next_token).
+//
+//  * Greedy rule ("spec-verify" page, section "Method", greedy bullet): the
+//    warp owning segment s of sequence b walks rows 0, 1, ... of that segment,
+//    keeping the largest value and its lowest index.  When a lane has seen an
 //    element that beats the draft token t_i (larger, or equal at a lower
-//    index) it records "row i missed" in a per-sequence flag (atomicMax of an
-//    encoding that favours smaller rows); every warp re-reads the flag before
-//    each segment and every CTA before each row, so rows after the first miss
-//    are not streamed.  Only comparisons are involved, so the result is exact
-//    in any order.
-//  * Sampling rule (same section, sampling bullet): warp 0 of every CTA
-//    gathers p_i(t_i), q_i(t_i) for the K positions and finds the first
-//    rejection n with the exact fp64 test u*q < p.  The CTA then streams its
-//    chunk of the residual max(0, p_n - q_n) (or of p_K when all K were
-//    accepted) and stores one double-fp32 sum per segment.  The last CTA scans
-//    the segment sums, finds the segment where the running mass first exceeds
+//    index) the warp records "row i missed" in a per-sequence flag (atomicMax
+//    of an encoding that favours smaller rows).  Every row's loads are issued
+//    together with a read of that flag, and the walk stops after the first row
+//    known to have missed, so rows past the first miss are not streamed.  Each
+//    row's segment maximum goes into a per-row 64-bit key with atomicMax.
+//    Only comparisons are involved, so the result is exact in any order.
+//  * Sampling rule (same section, sampling bullet): the first rejection n is
+//    found by a lane-parallel gather of p_i(t_i), q_i(t_i) and the exact fp64
+//    test u*q < p, then cached per sequence.  The warp streams its segment of
+//    the residual max(0, p_n - q_n), or of p_K when all K were accepted, and
+//    stores its double-fp32 sum.  The decide kernel scans the segment sums,
+//    finds the segment where the running mass first exceeds
 //    T = u_resample * total, and re-reads only that segment to locate the token.
 //
 // Mass sums use error-free transformations in fp32 instead of fp64 (fp64
@@ -42,10 +50,26 @@ namespace sv {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSeg = 1024;                  // elements per segment (one warp task)
-constexpr int kVecPerLane = kSeg / 4 / 32;  // float4 loads per lane per segment
+constexpr int kSeg = 1024;                  // elements per segment (one item)
+constexpr int kVecPerLane = kSeg / 4 / 32;  // float4 loads per lane per segment row
+constexpr int kBlocks = kSeg / 128;         // 128-element blocks per segment
 constexpr int kMaxK = 64;
 constexpr int kFlagBase = kMaxK + 1;        // miss flag stores kFlagBase - row; 0 = none
+constexpr int32_t kNBad = 0x7fffffff;       // cached n: 0 unknown, n + 1, or kNBad
+
+// Occupancy targets (CTAs per SM the register budget must allow) and how many
+// 16-byte loads per row a lane keeps in flight in the sampling stream.
+#ifndef SV_MIN_CTAS_PER_SM
+#define SV_MIN_CTAS_PER_SM 4
+#endif
+#ifndef SV_GREEDY_MIN_CTAS_PER_SM
+#define SV_GREEDY_MIN_CTAS_PER_SM 5
+#endif
+#ifndef SV_SAMPLE_BATCH
+#define SV_SAMPLE_BATCH 4
+#endif
+constexpr int kSampleBatch = SV_SAMPLE_BATCH;
+static_assert(kVecPerLane % kSampleBatch == 0, "batch must divide the per-lane loads");
 
 constexpr uint32_t kStatusBadToken = 1u;
 constexpr uint32_t kStatusZeroMass = 2u;
@@ -65,20 +89,25 @@ struct Params {
     const uint8_t *mode;        // [B], per-sequence rule (kPerSequence only)
     int32_t B, K;
     int64_t V;
-    int32_t nseg;               // segments per row
-    int32_t chunks;             // CTAs per sequence
-    int32_t spc;                // segments per chunk
+    int32_t nseg;               // segments per row = items per sequence
+    int32_t items;              // B * nseg
+    int32_t warps;              // warps in the stream kernel's grid
     int32_t *n_out;
     int32_t *next_out;
     int32_t *tokens;            // optional commit target [B][max_len]
     int32_t *lengths;
     int32_t max_len;
+    int32_t nchunks;            // bulk-copy path: chunks of the batch
     // workspace
     uint32_t *status;
-    uint32_t *ticket;           // [B]
-    int32_t *miss;              // [B]
+    uint32_t *queue;            // bulk-copy path: next chunk to hand out
+    int32_t *miss;              // [B] greedy: kFlagBase - first missed row
+    int32_t *nstate;            // [B] first rejection + 1 (sampling), 1 (greedy), kNBad
+    float *ptok;                // [B][K] greedy: p_i(t_i)
     unsigned long long *best;   // [B][K+1] packed (value, index) keys
     float2 *seg;                // [B][nseg] double-fp32 segment sums
+    float2 *blk;                // [B][nseg][kBlocks] double-fp32 128-element block sums
+    float2 *udd;                // [B] u_resample split into two fp32 parts
 };
 
 // ---------------------------------------------------------------------------
@@ -111,12 +140,128 @@ __device__ __forceinline__ double dd_to_double(dd x) {
     return __dadd_rn((double)x.hi, (double)x.lo);
 }
 
+__device__ __forceinline__ dd shfl_dd(dd x, int src) {
+    return {__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
+}
+
 __device__ __forceinline__ dd shfl_xor_dd(dd x, int m) {
     return {__shfl_xor_sync(0xffffffffu, x.hi, m), __shfl_xor_sync(0xffffffffu, x.lo, m)};
 }
 
 __device__ __forceinline__ dd shfl_up_dd(dd x, int d) {
     return {__shfl_up_sync(0xffffffffu, x.hi, d), __shfl_up_sync(0xffffffffu, x.lo, d)};
+}
+
+// Inclusive warp scan in lane order.
+__device__ __forceinline__ dd warp_incl_scan(dd v, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        dd o = shfl_up_dd(v, d);
+        if (lane >= d) v = dd_add(o, v);
+    }
+    return v;
+}
+
+// Packed pairs of fp32 values in one 64-bit register, and Blackwell's packed
+// fp32x2 add/subtract (two results per instruction, each correctly rounded).
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float a, float b) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ void unpack2(f32x2 x, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Exact sum of the masses of four consecutive elements as a double-fp32
+// pair.  Residual masses max(0, p - q) come out exactly as hi + lo from
+// FastTwoSum(max(p, q), -q) -- exact because max(p, q) >= q >= 0, and exactly
+// zero when p <= q, so no compare or select is needed.  The four (hi, lo)
+// values are then added with a packed TwoSum tree ((x + y), (z + w)) and one
+// scalar TwoSum, every rounding error kept.
+template <bool kResidual>
+__device__ __forceinline__ dd quad_mass(float4 p, float4 q) {
+    f32x2 ha, hb, la, lb;
+    if (kResidual) {
+        const f32x2 ma = pack2(fmaxf(p.x, q.x), fmaxf(p.z, q.z));
+        const f32x2 mb = pack2(fmaxf(p.y, q.y), fmaxf(p.w, q.w));
+        const f32x2 qa = pack2(q.x, q.z), qb = pack2(q.y, q.w);
+        ha = sub2(ma, qa);
+        la = sub2(sub2(ma, ha), qa);
+        hb = sub2(mb, qb);
+        lb = sub2(sub2(mb, hb), qb);
+    } else {
+        ha = pack2(p.x, p.z);
+        hb = pack2(p.y, p.w);
+        la = lb = 0ull;
+    }
+    // packed TwoSum: (x + y, z + w) and its rounding errors
+    const f32x2 sum = add2(ha, hb);
+    const f32x2 bb = sub2(sum, ha);
+    const f32x2 err = add2(sub2(ha, sub2(sum, bb)), sub2(hb, bb));
+    const f32x2 low = kResidual ? add2(add2(la, lb), err) : err;
+    float s1, s2, c1, c2;
+    unpack2(sum, s1, s2);
+    unpack2(low, c1, c2);
+    const dd t = two_sum(s1, s2);
+    return fast_two_sum(t.hi, __fadd_rn(t.lo, __fadd_rn(c1, c2)));
+}
+
+// Reduce-scatter of eight per-lane block partials v[k] (k = 128-element
+// block of the segment): afterwards lane l holds the warp total of block
+// bk(l) = 4 * bit4(l) + 2 * bit3(l) + bit2(l) (lanes with l % 4 == 0 hold the
+// eight blocks), and every lane holds the segment total.  12 double-fp32
+// additions instead of 40 for eight separate warp reductions.
+__device__ __forceinline__ void reduce_blocks(const dd v[kBlocks], int lane, dd &blk, int &bk,
+                                              dd &total) {
+    const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4;
+    dd a[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const dd send = h4 ? v[j] : v[j + 4];
+        const dd keep = h4 ? v[j + 4] : v[j];
+        a[j] = dd_add(keep, shfl_xor_dd(send, 16));
+    }
+    dd c[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const dd send = h3 ? a[j] : a[j + 2];
+        const dd keep = h3 ? a[j + 2] : a[j];
+        c[j] = dd_add(keep, shfl_xor_dd(send, 8));
+    }
+    dd x = dd_add(h2 ? c[1] : c[0], shfl_xor_dd(h2 ? c[0] : c[1], 4));
+    x = dd_add(x, shfl_xor_dd(x, 2));
+    x = dd_add(x, shfl_xor_dd(x, 1));
+    blk = x;
+    bk = (h4 ? 4 : 0) + (h3 ? 2 : 0) + (h2 ? 1 : 0);
+    dd t = dd_add(x, shfl_xor_dd(x, 4));
+    t = dd_add(t, shfl_xor_dd(t, 8));
+    total = dd_add(t, shfl_xor_dd(t, 16));
+}
+
+// Stores segment s's total and its eight block totals.
+__device__ __forceinline__ void store_sums(float2 *seg, float2 *blk, int64_t s, const dd v[kBlocks],
+                                           int lane) {
+    dd b, total;
+    int bk;
+    reduce_blocks(v, lane, b, bk, total);
+    if ((lane & 3) == 0) blk[s * kBlocks + bk] = make_float2(b.hi, b.lo);
+    if (lane == 0) seg[s] = make_float2(total.hi, total.lo);
 }
 
 // Running per-lane sum of exact element masses (Sum2 cascade): s is the fp32
@@ -131,17 +276,16 @@ struct Acc {
     __device__ __forceinline__ dd value() const { return fast_two_sum(s, c); }
 };
 
-// Exact residual mass of one element: max(0, p - q) as hi + lo.  For
-// p > q >= 0, |p| >= |q|, so FastTwoSum(p, -q) is exact.  With kResidual
-// false the mass is p itself (bonus draw and the zero-residual fallback).
+// Exact residual mass of one element: max(0, p - q) as hi + lo, computed as
+// FastTwoSum(max(p, q), -q) -- exact since max(p, q) >= q >= 0, and exactly
+// zero when p <= q.  With kResidual false the mass is p itself (bonus draw and
+// the zero-residual fallback).
 template <bool kResidual>
 __device__ __forceinline__ void elem_mass(float p, float q, float &hi, float &lo) {
     if (kResidual) {
-        float d = __fsub_rn(p, q);
-        float e = __fsub_rn(__fsub_rn(p, d), q);
-        bool pos = p > q;
-        hi = pos ? d : 0.f;
-        lo = pos ? e : 0.f;
+        const float m = fmaxf(p, q);
+        hi = __fsub_rn(m, q);
+        lo = __fsub_rn(__fsub_rn(m, hi), q);
     } else {
         hi = p;
         lo = 0.f;
@@ -165,7 +309,7 @@ __device__ __forceinline__ float ld_stream1(const float *ptr) {
     return v;
 }
 
-// Loads that must see other CTAs' writes of this launch (L2, never L1).
+// Loads that must see other warps' writes of this launch (L2, never L1).
 template <class T>
 __device__ __forceinline__ T ld_l2(const T *ptr) {
     return __ldcg(ptr);
@@ -187,7 +331,8 @@ __device__ __forceinline__ uint32_t ordered_bits(float x) {
 // value at a lower index; 0 means "no element".
 __device__ __forceinline__ unsigned long long pack_key(float v, int32_t idx) {
     if (idx < 0) return 0ull;
-    return ((unsigned long long)ordered_bits(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+    return ((unsigned long long)ordered_bits(v) << 32) |
+           (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
 }
 
 __device__ __forceinline__ int32_t key_index(unsigned long long key) {
@@ -203,23 +348,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k)
     return k;
 }
 
-// ---------------------------------------------------------------------------
-// shared state of one CTA
-
-struct Shared {
-    int32_t tok[kMaxK];
-    int32_t n;
-    int32_t bad;
-    int32_t flag;
-    int32_t is_last;
-    int32_t cand;
-    int32_t pick;
-    int32_t zero;
-    unsigned long long wkey[kWarps];
-    dd wsum[kWarps];
-    dd base;
-};
-
 __device__ __forceinline__ const float *prow(const Params &P, int b, int i) {
     return P.p + ((int64_t)b * (P.K + 1) + i) * P.ps;
 }
@@ -228,20 +356,20 @@ __device__ __forceinline__ const float *qrow(const Params &P, int b, int i) {
     return P.q + ((int64_t)b * P.K + i) * P.qs;
 }
 
-// Loads t[b][0..K) into shared memory and flags out-of-range ids.
-__device__ __forceinline__ void load_tokens(const Params &P, int b, Shared &sh) {
-    if (threadIdx.x == 0) sh.bad = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < P.K; i += kThreads) {
-        int32_t x = P.t[(int64_t)b * P.K + i];
-        sh.tok[i] = x;
-        if (x < 0 || (int64_t)x >= P.V) sh.bad = 1;
-    }
-    __syncthreads();
+// Draft tokens of sequence b in two per-lane registers (positions lane and
+// lane + 32); returns true in every lane if one of them is outside [0, V).
+__device__ __forceinline__ bool load_tokens(const Params &P, int b, int lane, int32_t &t0,
+                                            int32_t &t1) {
+    const int32_t *tb = P.t + (int64_t)b * P.K;
+    t0 = lane < P.K ? tb[lane] : 0;
+    t1 = lane + 32 < P.K ? tb[lane + 32] : 0;
+    bool bad = (lane < P.K && (t0 < 0 || (int64_t)t0 >= P.V)) ||
+               (lane + 32 < P.K && (t1 < 0 || (int64_t)t1 >= P.V));
+    return __any_sync(0xffffffffu, bad);
 }
 
 // ---------------------------------------------------------------------------
-// greedy: argmax of one segment, lane view
+// greedy item: argmax of segment s over rows 0, 1, ... of sequence b
 
 __device__ __forceinline__ void take(float x, int32_t e, float &bv, int32_t &bi) {
     if (x > bv) {  // strict: within a lane indices only increase
@@ -251,8 +379,8 @@ __device__ __forceinline__ void take(float x, int32_t e, float &bv, int32_t &bi)
 }
 
 __device__ __forceinline__ void argmax_segment(const float *row, int64_t base, int64_t V,
-                                               bool vec, int lane, float &bv, int32_t &bi) {
-    if (vec && base + kSeg <= V) {
+                                               int lane, float &bv, int32_t &bi) {
+    if (aligned16(row) && base + kSeg <= V) {
         float4 x[kVecPerLane];
 #pragma unroll
         for (int k = 0; k < kVecPerLane; ++k) x[k] = ld_stream4(row + base + 4 * (lane + 32 * k));
@@ -282,413 +410,499 @@ __device__ __forceinline__ void argmax_segment(const float *row, int64_t base, i
     }
 }
 
-__device__ void greedy_body(const Params &P, int b, int c, Shared &sh) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    load_tokens(P, b, sh);
-    if (sh.bad) return;
-    const int s_lo = c * P.spc;
-    const int s_hi = min(P.nseg, s_lo + P.spc);
+__device__ void greedy_item(const Params &P, int b, int s, int lane) {
+    int32_t t0, t1;
+    if (load_tokens(P, b, lane, t0, t1)) return;  // the decide kernel reports it
+    const float pt0 = lane < P.K ? __ldg(prow(P, b, lane) + t0) : 0.f;
+    const float pt1 = lane + 32 < P.K ? __ldg(prow(P, b, lane + 32) + t1) : 0.f;
+    const int64_t base = (int64_t)s * kSeg;
     for (int i = 0; i <= P.K; ++i) {
-        if (threadIdx.x == 0) sh.flag = ld_l2(P.miss + b);
-        __syncthreads();
-        const int flag = sh.flag;
-        __syncthreads();
-        if (flag > kFlagBase - i) break;  // an earlier row already missed
-        const float *row = prow(P, b, i);
-        const bool vec = aligned16(row);
-        const bool has_t = i < P.K;
-        const int32_t ti = has_t ? sh.tok[i] : -1;
-        const float pt = has_t ? __ldg(row + ti) : 0.f;
-        bool signalled = !has_t;
+        int f = 0;
+        if (lane == 0) f = ld_l2(P.miss + b);  // waited for only after the row's loads
         float bv = -__int_as_float(0x7f800000);  // -inf
         int32_t bi = -1;
-        for (int s = s_lo + warp; s < s_hi; s += kWarps) {
-            if (s != s_lo + warp) {
-                int f = 0;
-                if (lane == 0) f = ld_l2(P.miss + b);
-                f = __shfl_sync(0xffffffffu, f, 0);
-                if (f > kFlagBase - i) break;
-            }
-            argmax_segment(row, (int64_t)s * kSeg, P.V, vec, lane, bv, bi);
-            if (!signalled) {
-                bool beats = bi >= 0 && (bv > pt || (bv == pt && bi < ti));
-                if (__any_sync(0xffffffffu, beats)) {
-                    if (lane == 0) atomicMax(P.miss + b, kFlagBase - i);
-                    signalled = true;
-                }
-            }
+        argmax_segment(prow(P, b, i), base, P.V, lane, bv, bi);
+        bool missed = false;
+        if (i < P.K) {
+            const float pti = __shfl_sync(0xffffffffu, i < 32 ? pt0 : pt1, i & 31);
+            const int32_t ti = __shfl_sync(0xffffffffu, i < 32 ? t0 : t1, i & 31);
+            const bool beats = bi >= 0 && (bv > pti || (bv == pti && bi < ti));
+            missed = __any_sync(0xffffffffu, beats);
+            if (missed && lane == 0) atomicMax(P.miss + b, kFlagBase - i);
         }
-        unsigned long long key = warp_max_u64(pack_key(bv, bi));
-        if (lane == 0) sh.wkey[warp] = key;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            unsigned long long k = sh.wkey[0];
-            for (int w = 1; w < kWarps; ++w) k = sh.wkey[w] > k ? sh.wkey[w] : k;
-            if (k) atomicMax(P.best + (int64_t)b * (P.K + 1) + i, k);
-        }
-        // the next iteration's leading barrier orders sh.wkey reuse
+        const unsigned long long key = warp_max_u64(pack_key(bv, bi));
+        if (lane == 0 && key) atomicMax(P.best + (int64_t)b * (P.K + 1) + i, key);
+        f = __shfl_sync(0xffffffffu, f, 0);
+        if (missed || f >= kFlagBase - i) break;  // a row <= i missed: no later row is needed
     }
 }
 
 // ---------------------------------------------------------------------------
-// sampling: accept scan (warp 0) and residual segment sums
+// sampling item: first rejection n, then one segment of the draw distribution
 
-__device__ void accept_scan(const Params &P, int b, Shared &sh) {
-    const int lane = threadIdx.x & 31;
-    if (threadIdx.x < 32) {
-        int n = P.K;
-        bool bad = false;
-        for (int i0 = 0; i0 < P.K; i0 += 32) {
-            const int i = i0 + lane;
-            bool rej = false;
-            if (i < P.K) {
-                const int32_t x = P.t[(int64_t)b * P.K + i];
-                if (x < 0 || (int64_t)x >= P.V) {
-                    bad = true;
-                } else {
-                    const float pt = __ldg(prow(P, b, i) + x);
-                    const float qt = __ldg(qrow(P, b, i) + x);
-                    const float u = __ldg(P.u_acc + (int64_t)b * P.K + i);
-                    // exact: the fp64 product of two fp32 values is exact
-                    rej = !(__dmul_rn((double)u, (double)qt) < (double)pt);
-                }
+// First rejection of sequence b as n + 1 (n = K when all K are accepted), or
+// kNBad when a draft id is outside [0, V): a lane-parallel gather of
+// p_i(t_i), q_i(t_i) and the exact fp64 accept test for every position.
+__device__ int32_t first_rejection(const Params &P, int b, int lane) {
+    int n = P.K;
+    bool bad = false;
+    for (int i0 = 0; i0 < P.K; i0 += 32) {
+        const int i = i0 + lane;
+        bool rej = false;
+        if (i < P.K) {
+            const int32_t x = P.t[(int64_t)b * P.K + i];
+            if (x < 0 || (int64_t)x >= P.V) {
+                bad = true;
+            } else {
+                const float pt = __ldg(prow(P, b, i) + x);
+                const float qt = __ldg(qrow(P, b, i) + x);
+                const float u = __ldg(P.u_acc + (int64_t)b * P.K + i);
+                // exact: the fp64 product of two fp32 values is exact
+                rej = !(__dmul_rn((double)u, (double)qt) < (double)pt);
             }
-            unsigned m = __ballot_sync(0xffffffffu, rej);
-            if (m && n == P.K) n = i0 + __ffs(m) - 1;
         }
-        bad = __any_sync(0xffffffffu, bad);
-        if (lane == 0) {
-            sh.n = n;
-            sh.bad = bad ? 1 : 0;
-        }
+        const unsigned m = __ballot_sync(0xffffffffu, rej);
+        if (m && n == P.K) n = i0 + __ffs(m) - 1;
     }
-    __syncthreads();
+    return __any_sync(0xffffffffu, bad) ? kNBad : n + 1;
 }
 
-// Sum of one segment's masses (lane-strided 16-byte loads); every lane gets
-// the warp total.
+// Masses of one segment (lane-strided 16-byte loads), summed per lane and per
+// 128-element block: lane l's k-th float4 holds elements 128k + 4l .. +3, and
+// on the scalar path its j-th element is 32j + l, in block j / 4.
 template <bool kResidual>
-__device__ __forceinline__ dd segment_sum(const float *pr, const float *qr, int64_t base,
-                                          int64_t V, bool vec, int lane) {
-    Acc acc;
-    if (vec && base + kSeg <= V) {
-        float4 a[kVecPerLane], d[kVecPerLane];
+__device__ __forceinline__ void segment_partials(const float *pr, const float *qr, int64_t base,
+                                                 int64_t V, int lane, dd v[kBlocks]) {
+    if (aligned16(pr) && (!kResidual || aligned16(qr)) && base + kSeg <= V) {
 #pragma unroll
-        for (int k = 0; k < kVecPerLane; ++k) {
-            a[k] = ld_stream4(pr + base + 4 * (lane + 32 * k));
-            if (kResidual) d[k] = ld_stream4(qr + base + 4 * (lane + 32 * k));
-        }
+        for (int h = 0; h < kVecPerLane; h += kSampleBatch) {
+            float4 a[kSampleBatch], d[kSampleBatch];
 #pragma unroll
-        for (int k = 0; k < kVecPerLane; ++k) {
-            float hi, lo;
-            float4 qq = kResidual ? d[k] : make_float4(0.f, 0.f, 0.f, 0.f);
-            elem_mass<kResidual>(a[k].x, qq.x, hi, lo); acc.add(hi, lo);
-            elem_mass<kResidual>(a[k].y, qq.y, hi, lo); acc.add(hi, lo);
-            elem_mass<kResidual>(a[k].z, qq.z, hi, lo); acc.add(hi, lo);
-            elem_mass<kResidual>(a[k].w, qq.w, hi, lo); acc.add(hi, lo);
+            for (int k = 0; k < kSampleBatch; ++k) {
+                a[k] = ld_stream4(pr + base + 4 * (lane + 32 * (h + k)));
+                if (kResidual) d[k] = ld_stream4(qr + base + 4 * (lane + 32 * (h + k)));
+            }
+#pragma unroll
+            for (int k = 0; k < kSampleBatch; ++k)
+                v[h + k] = quad_mass<kResidual>(a[k], kResidual ? d[k] : make_float4(0.f, 0.f, 0.f, 0.f));
         }
     } else {
-        int64_t end = base + kSeg < V ? base + kSeg : V;
-        for (int64_t e = base + lane; e < end; e += 32) {
-            float hi, lo;
-            elem_mass<kResidual>(ld_stream1(pr + e), kResidual ? ld_stream1(qr + e) : 0.f, hi, lo);
-            acc.add(hi, lo);
+        Acc acc[kBlocks];
+        const int64_t end = base + kSeg < V ? base + kSeg : V;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+            const int64_t e = base + lane + 32 * j;
+            if (e < end) {
+                float hi, lo;
+                elem_mass<kResidual>(ld_stream1(pr + e), kResidual ? ld_stream1(qr + e) : 0.f, hi, lo);
+                acc[j / 4].add(hi, lo);
+            }
         }
-    }
-    dd v = acc.value();
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) v = dd_add(v, shfl_xor_dd(v, m));
-    return v;
-}
-
-// Segment sums of segments [s_lo, s_hi) of one row, warp-strided, stored to
-// seg[] by lane 0 of the warp that computed them.
-template <bool kResidual>
-__device__ void stream_segments(const Params &P, const float *pr, const float *qr, float2 *seg,
-                                int s_lo, int s_hi) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool vec = aligned16(pr) && (!kResidual || aligned16(qr));
-    for (int s = s_lo + warp; s < s_hi; s += kWarps) {
-        dd v = segment_sum<kResidual>(pr, qr, (int64_t)s * kSeg, P.V, vec, lane);
-        if (lane == 0) seg[s] = make_float2(v.hi, v.lo);
+        for (int k = 0; k < kBlocks; ++k) v[k] = acc[k].value();
     }
 }
 
-__device__ void sample_body(const Params &P, int b, int c, Shared &sh) {
-    accept_scan(P, b, sh);
-    if (sh.bad) return;
-    const int n = sh.n;
-    const int s_lo = c * P.spc;
-    const int s_hi = min(P.nseg, s_lo + P.spc);
-    float2 *seg = P.seg + (int64_t)b * P.nseg;
-    if (n < P.K)
-        stream_segments<true>(P, prow(P, b, n), qrow(P, b, n), seg, s_lo, s_hi);
-    else
-        stream_segments<false>(P, prow(P, b, P.K), nullptr, seg, s_lo, s_hi);
-    __threadfence();  // segment sums visible before this CTA's ticket
+template <bool kResidual>
+__device__ __forceinline__ void segment_sum_store(const Params &P, int b, const float *pr,
+                                                  const float *qr, int s, int lane) {
+    dd v[kBlocks];
+    segment_partials<kResidual>(pr, qr, (int64_t)s * kSeg, P.V, lane, v);
+    store_sums(P.seg + (int64_t)b * P.nseg, P.blk + (int64_t)b * P.nseg * kBlocks, s, v, lane);
+}
+
+__device__ void sample_item(const Params &P, int b, int s, int32_t ns, int lane) {
+    if (ns == kNBad) return;  // the decide kernel reports it
+    const int n = ns - 1;
+    if (n < P.K) segment_sum_store<true>(P, b, prow(P, b, n), qrow(P, b, n), s, lane);
+    else segment_sum_store<false>(P, b, prow(P, b, P.K), nullptr, s, lane);
 }
 
 // ---------------------------------------------------------------------------
-// block-wide helpers for the deciding CTA
+// decisions (one warp, once per sequence)
 
-// Exclusive scan of one dd per thread (thread order); total to *total.
-__device__ dd block_excl_scan(dd v, dd *total, Shared &sh) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    dd inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        dd o = shfl_up_dd(inc, d);
-        if (lane >= d) inc = dd_add(o, inc);
-    }
-    if (lane == 31) sh.wsum[warp] = inc;
-    __syncthreads();
-    dd wbase = {0.f, 0.f}, all = {0.f, 0.f};
-    for (int w = 0; w < kWarps; ++w) {
-        if (w == warp) wbase = all;
-        all = dd_add(all, sh.wsum[w]);
-    }
-    __syncthreads();
-    *total = all;
-    dd lane_excl = shfl_up_dd(inc, 1);
-    if (lane == 0) lane_excl = {0.f, 0.f};
-    return dd_add(wbase, lane_excl);
+constexpr int kSegRegs = 8;  // segment sums a lane keeps in registers (V <= 262144)
+
+// Comparisons with the draw threshold are made in double-fp32: a > b for
+// normalised pairs (|lo| <= ulp(hi) / 2).
+__device__ __forceinline__ bool dd_gt(dd a, dd b) {
+    return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
 }
 
-__device__ int block_min_int(int v, Shared &sh) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, m));
-    if (lane == 0) sh.wkey[warp] = (unsigned long long)(uint32_t)v;
-    __syncthreads();
-    int r = (int)(uint32_t)sh.wkey[0];
-    for (int w = 1; w < kWarps; ++w) r = min(r, (int)(uint32_t)sh.wkey[w]);
-    __syncthreads();
-    return r;
+// u * R as a double-fp32 pair (u given as two fp32 parts; fmaf keeps the
+// products' rounding errors).
+__device__ __forceinline__ dd threshold(dd u, dd R) {
+    const float p = __fmul_rn(u.hi, R.hi);
+    float e = __fmaf_rn(u.hi, R.hi, -p);
+    e = __fmaf_rn(u.hi, R.lo, e);
+    e = __fmaf_rn(u.lo, R.hi, e);
+    return fast_two_sum(p, e);
 }
 
-__device__ int block_max_int(int v, Shared &sh) {
-    return -block_min_int(-v, sh);
-}
-
-// Rescans one segment with lane-contiguous 32-element blocks (warp 0 only):
-// returns the smallest index v in it whose running mass base + C_v exceeds T,
-// or the last index with non-zero mass if none does (a rounding boundary), or
-// -1 if the segment has no mass.
+// Within one 128-element block starting at element `base` of the row pair:
+// the smallest index whose running mass prefix + C_v exceeds T, or the last
+// index with mass if none does (a rounding boundary), or -1.  Lane l holds
+// elements 4l .. 4l + 3; one warp scan finds the lane, which walks its four.
 template <bool kResidual>
-__device__ int rescan_segment(const float *pr, const float *qr, int64_t base, int64_t V,
-                              dd prefix, double T) {
-    const int lane = threadIdx.x & 31;
-    const int64_t lo = base + 32 * lane;
-    const int64_t hi = lo + 32 < V ? lo + 32 : V;
-    const int64_t seg_end = base + kSeg < V ? base + kSeg : V;
-    float mh[32], ml[32];
-    Acc acc;
+__device__ int search_block(const float *pr, const float *qr, int64_t base, int64_t V, dd prefix,
+                            dd T, int lane) {
+    const int64_t n = V - base < 128 ? V - base : 128;
+    const int64_t e0 = 4 * lane;
+    float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (n == 128 && aligned16(pr + base) && (!kResidual || aligned16(qr + base))) {
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(pr + base + e0));
+        pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
+        if (kResidual) {
+            const float4 d = __ldcg(reinterpret_cast<const float4 *>(qr + base + e0));
+            qv[0] = d.x; qv[1] = d.y; qv[2] = d.z; qv[3] = d.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            pv[j] = e0 + j < n ? __ldcg(pr + base + e0 + j) : 0.f;
+            if (kResidual) qv[j] = e0 + j < n ? __ldcg(qr + base + e0 + j) : 0.f;
+        }
+    }
+    float mh[4], ml[4];
     int last_nz = -1;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int64_t e = lo + j;
-        float pv = 0.f, qv = 0.f;
-        if (e < hi) {
-            pv = __ldcg(pr + e);
-            if (kResidual) qv = __ldcg(qr + e);
-        }
-        elem_mass<kResidual>(pv, qv, mh[j], ml[j]);
-        if (e >= hi) mh[j] = ml[j] = 0.f;
-        if (mh[j] != 0.f) last_nz = (int)(e - base);
-        acc.add(mh[j], ml[j]);
+    for (int j = 0; j < 4; ++j) {
+        elem_mass<kResidual>(pv[j], qv[j], mh[j], ml[j]);
+        if (mh[j] != 0.f) last_nz = (int)e0 + j;
     }
-    (void)seg_end;
-    dd mine = acc.value();
-    // lane-exclusive prefix within the segment
-    dd inc = mine;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        dd o = shfl_up_dd(inc, d);
-        if (lane >= d) inc = dd_add(o, inc);
-    }
-    dd excl = shfl_up_dd(inc, 1);
-    if (lane == 0) excl = {0.f, 0.f};
-    dd start = dd_add(prefix, excl);
-    dd end = dd_add(prefix, inc);
-    const bool crosses = mine.hi != 0.f && dd_to_double(end) > T;
-    const unsigned m = __ballot_sync(0xffffffffu, crosses);
-    int pick = -1;
+    // the same four-element sum the stream kernels formed for the block sums
+    const dd mine = quad_mass<kResidual>(make_float4(pv[0], pv[1], pv[2], pv[3]),
+                                         make_float4(qv[0], qv[1], qv[2], qv[3]));
+    const dd inc = warp_incl_scan(mine, lane);
+    const unsigned m = __ballot_sync(0xffffffffu, mine.hi != 0.f && dd_gt(dd_add(prefix, inc), T));
     if (m) {
         const int L = __ffs(m) - 1;
+        dd excl = shfl_up_dd(inc, 1);
+        if (lane == 0) excl = {0.f, 0.f};
         int found = -1;
         if (lane == L) {
-            dd run = start;
+            dd run = dd_add(prefix, excl);
+            int lastj = -1;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 if (found < 0 && mh[j] != 0.f) {
+                    lastj = j;
                     run = dd_add(run, fast_two_sum(mh[j], ml[j]));
-                    if (dd_to_double(run) > T) found = (int)(lo + j - base);
+                    if (dd_gt(run, T)) found = (int)e0 + j;
                 }
             }
-            if (found < 0) found = last_nz;  // lane total crossed but steps did not
+            if (found < 0) found = (int)e0 + lastj;  // the lane crossed, its steps did not
         }
-        pick = __shfl_sync(0xffffffffu, found, L);
-    } else {
-        int l = last_nz;
-#pragma unroll
-        for (int mm = 16; mm > 0; mm >>= 1) l = max(l, __shfl_xor_sync(0xffffffffu, l, mm));
-        pick = l;
+        found = __shfl_sync(0xffffffffu, found, L);
+        return (int)(base + found);
     }
-    return pick < 0 ? -1 : (int)(base + pick);
+#pragma unroll
+    for (int mm = 16; mm > 0; mm >>= 1) last_nz = max(last_nz, __shfl_xor_sync(0xffffffffu, last_nz, mm));
+    return last_nz < 0 ? -1 : (int)(base + last_nz);
 }
 
-// Inverse-CDF draw over the segment sums seg[0..nseg) of the row pair
-// (pr, qr): returns the token, or -1 if the total mass is zero.
+// Given lanes holding consecutive sums v (lane order = index order) starting
+// at running mass `prefix`: the first lane whose inclusive sum exceeds T
+// (-1 if none) and the running mass before it.
+__device__ __forceinline__ int first_crossing(dd v, dd prefix, dd T, int lane, dd &before) {
+    const dd inc = warp_incl_scan(v, lane);
+    const unsigned m = __ballot_sync(0xffffffffu, v.hi != 0.f && dd_gt(dd_add(prefix, inc), T));
+    if (!m) return -1;
+    const int L = __ffs(m) - 1;
+    dd excl = shfl_up_dd(inc, 1);
+    if (lane == 0) excl = {0.f, 0.f};
+    before = shfl_dd(dd_add(prefix, excl), L);
+    return L;
+}
+
+// Inverse-CDF draw for sequence b over the segment sums seg[0..nseg) and
+// block sums blk of the row pair (pr, qr) (decide kernel, one warp): the token,
+// or -1 if the total mass is zero.  Three steps, each one load round trip:
+// the segment (lane l owns segments [l * per, (l + 1) * per)), the block
+// within it (lanes 0..7), the element within the block.
 template <bool kResidual>
-__device__ int draw_from_segments(const Params &P, const float2 *seg, const float *pr,
-                                  const float *qr, double u, Shared &sh) {
-    const int per = (P.nseg + kThreads - 1) / kThreads;
-    const int r0 = min(P.nseg, (int)threadIdx.x * per);
-    const int r1 = min(P.nseg, r0 + per);
-    dd run = {0.f, 0.f};
-    for (int s = r0; s < r1; ++s) {
-        float2 v = ld_l2(seg + s);
-        run = dd_add(run, dd{v.x, v.y});
-    }
-    dd total;
-    dd excl = block_excl_scan(run, &total, sh);
-    if (total.hi == 0.f) return -1;
-    const double T = __dmul_rn(u, dd_to_double(total));
-    int cand = 0x7fffffff;
-    dd acc = excl;
-    for (int s = r0; s < r1; ++s) {
-        float2 v = ld_l2(seg + s);
-        dd nxt = dd_add(acc, dd{v.x, v.y});
-        if (v.x != 0.f && dd_to_double(nxt) > T) {
-            cand = s;
-            break;
+__device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *blk,
+                              const float *pr, const float *qr, dd u, int lane) {
+    const int per = (P.nseg + 31) / 32;
+    const int r0 = min(P.nseg, lane * per), r1 = min(P.nseg, r0 + per);
+    dd v[kSegRegs];
+    dd own = {0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kSegRegs; ++r) {
+        v[r] = dd{0.f, 0.f};
+        if (r0 + r < r1) {
+            const float2 x = ld_l2(seg + r0 + r);
+            v[r] = dd{x.x, x.y};
         }
-        acc = nxt;
+        own = dd_add(own, v[r]);
     }
-    const int first = block_min_int(cand, sh);
-    if (first == cand && cand != 0x7fffffff) sh.base = acc;  // prefix before segment `first`
-    int target = first;
-    if (first == 0x7fffffff) {
-        // T reached the total through rounding: the last segment with mass
+    for (int s = r0 + kSegRegs; s < r1; ++s) {  // rows longer than 32 * kSegRegs segments
+        const float2 x = ld_l2(seg + s);
+        own = dd_add(own, dd{x.x, x.y});
+    }
+    const dd inc = warp_incl_scan(own, lane);
+    const dd total = shfl_dd(inc, 31);
+    if (total.hi == 0.f) return -1;
+    const dd T = threshold(u, total);
+    const dd zero = {0.f, 0.f};
+    dd before;
+    const int L = first_crossing(own, zero, T, lane, before);
+    // the segment, the running mass before it, and the time T is past every segment
+    int sg = -1;
+    dd sbefore = zero;
+    if (L >= 0) {
+        if (lane == L) {
+            dd acc = before, last_before = before;
+            int last = -1;
+            for (int s = r0; s < r1; ++s) {
+                const int r = s - r0;
+                dd x = zero;
+                if (r < kSegRegs) {
+#pragma unroll
+                    for (int i = 0; i < kSegRegs; ++i)
+                        if (i == r) x = v[i];
+                } else {
+                    const float2 y = ld_l2(seg + s);
+                    x = dd{y.x, y.y};
+                }
+                const dd nx = dd_add(acc, x);
+                if (x.hi != 0.f) {
+                    last = s;
+                    last_before = acc;
+                    if (dd_gt(nx, T)) {
+                        sg = s;
+                        sbefore = acc;
+                        break;
+                    }
+                }
+                acc = nx;
+            }
+            if (sg < 0) {
+                sg = last;
+                sbefore = last_before;
+            }
+        }
+        sg = __shfl_sync(0xffffffffu, sg, L);
+        sbefore = shfl_dd(sbefore, L);
+    }
+    dd Tt = T;
+    if (sg < 0) {
+        // T reached the total through rounding: the last segment with mass,
+        // searched with an infinite threshold (its last element with mass)
         int lastnz = -1;
         for (int s = r0; s < r1; ++s)
             if (ld_l2(seg + s).x != 0.f) lastnz = s;
-        target = block_max_int(lastnz, sh);
-        if (threadIdx.x == 0) sh.base = dd{0.f, 0.f};
+#pragma unroll
+        for (int mm = 16; mm > 0; mm >>= 1) lastnz = max(lastnz, __shfl_xor_sync(0xffffffffu, lastnz, mm));
+        sg = lastnz;
+        Tt = dd{__int_as_float(0x7f800000), 0.f};
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        // for the rounding fallback, T' = +inf forces "last non-zero element"
-        const double Tt = first == 0x7fffffff ? __longlong_as_double(0x7ff0000000000000ll) : T;
-        int j = rescan_segment<kResidual>(pr, qr, (int64_t)target * kSeg, P.V, sh.base, Tt);
-        if (threadIdx.x == 0) sh.pick = j;
+    // block within the segment
+    dd bv = zero;
+    if (lane < kBlocks) {
+        const float2 x = ld_l2(blk + (int64_t)sg * kBlocks + lane);
+        bv = dd{x.x, x.y};
     }
-    __syncthreads();
-    return sh.pick;
+    dd bbefore;
+    int bk = first_crossing(bv, sbefore, Tt, lane, bbefore);
+    if (bk < 0) {
+        // block sums and the segment sum disagree in the last bits: the last
+        // block with mass, with an infinite threshold
+        const unsigned nz = __ballot_sync(0xffffffffu, lane < kBlocks && bv.hi != 0.f);
+        bk = nz ? 31 - __clz(nz) : kBlocks - 1;
+        bbefore = zero;
+        Tt = dd{__int_as_float(0x7f800000), 0.f};
+    }
+    return search_block<kResidual>(pr, qr, (int64_t)sg * kSeg + 128 * bk, P.V, bbefore, Tt, lane);
 }
 
-// ---------------------------------------------------------------------------
-// decisions of the last CTA of a sequence
-
-__device__ void commit_round(const Params &P, int b, int n, int next, Shared &sh) {
+// Commit step of a round ("spec-verify", section "Usage": keep
+// draft_tokens[:n_accepted], append next_token).
+__device__ void commit_round(const Params &P, int b, int n, int next, int lane) {
     if (!P.tokens || next < 0) return;
-    if (threadIdx.x == 0) {
-        const int len = P.lengths[b];
+    int len = 0;
+    if (lane == 0) {
+        len = P.lengths[b];
         const bool ok = len >= 0 && (int64_t)len + n + 1 <= P.max_len;
-        sh.flag = ok ? len : -1;
-        if (!ok) atomicOr(P.status, kStatusOverflow);
-    }
-    __syncthreads();
-    const int len = sh.flag;
-    if (len >= 0) {
-        int32_t *row = P.tokens + (int64_t)b * P.max_len;
-        for (int i = threadIdx.x; i < n; i += kThreads) row[len + i] = P.t[(int64_t)b * P.K + i];
-        if (threadIdx.x == 0) {
-            row[len + n] = next;
-            P.lengths[b] = len + n + 1;
+        if (!ok) {
+            atomicOr(P.status, kStatusOverflow);
+            len = -1;
         }
     }
+    len = __shfl_sync(0xffffffffu, len, 0);
+    if (len < 0) return;
+    int32_t *row = P.tokens + (int64_t)b * P.max_len;
+    for (int i = lane; i < n; i += 32) row[len + i] = P.t[(int64_t)b * P.K + i];
+    if (lane == 0) {
+        row[len + n] = next;
+        P.lengths[b] = len + n + 1;
+    }
 }
 
-__device__ void greedy_decide(const Params &P, int b, Shared &sh) {
+__device__ void greedy_decide(const Params &P, int b, int lane) {
+    int32_t t0, t1;
+    const bool bad = load_tokens(P, b, lane, t0, t1);
     int n = 0, next = -1;
-    if (!sh.bad) {
+    if (!bad) {
         const int f = ld_l2(P.miss + b);
         n = f ? kFlagBase - f : P.K;
         const unsigned long long key = ld_l2(P.best + (int64_t)b * (P.K + 1) + n);
         next = key ? key_index(key) : 0;
     }
-    if (threadIdx.x == 0) {
-        if (sh.bad) atomicOr(P.status, kStatusBadToken);
+    if (lane == 0) {
+        if (bad) atomicOr(P.status, kStatusBadToken);
         P.n_out[b] = n;
         P.next_out[b] = next;
         P.miss[b] = 0;
+        P.nstate[b] = 0;
     }
-    for (int i = threadIdx.x; i <= P.K; i += kThreads) P.best[(int64_t)b * (P.K + 1) + i] = 0ull;
-    commit_round(P, b, n, next, sh);
+    for (int i = lane; i <= P.K; i += 32) P.best[(int64_t)b * (P.K + 1) + i] = 0ull;
+    commit_round(P, b, n, next, lane);
 }
 
-__device__ void sample_decide(const Params &P, int b, Shared &sh) {
+__device__ void sample_decide(const Params &P, int b, int lane) {
+    const int ns = ld_l2(P.nstate + b);
+    const float2 uf = ld_l2(P.udd + b);  // loaded alongside, used only if the sequence is valid
+    const dd u = {uf.x, uf.y};
+    const bool bad = ns == kNBad;
     int n = 0, next = -1;
-    if (!sh.bad) {
-        n = sh.n;
-        const double u = P.u_res[b];
-        float2 *seg = P.seg + (int64_t)b * P.nseg;
+    if (!bad) {
+        n = ns - 1;
+        const float2 *seg = P.seg + (int64_t)b * P.nseg;
+        const float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
         if (n < P.K) {
-            next = draw_from_segments<true>(P, seg, prow(P, b, n), qrow(P, b, n), u, sh);
+            next = draw_from_sums<true>(P, seg, blk, prow(P, b, n), qrow(P, b, n), u, lane);
             if (next < 0) {
                 // zero residual mass (unnormalised rows): draw from p_n itself
-                __syncthreads();
-                stream_segments<false>(P, prow(P, b, n), nullptr, seg, 0, P.nseg);
+                const float *pr = prow(P, b, n);
+                for (int s = 0; s < P.nseg; ++s) segment_sum_store<false>(P, b, pr, nullptr, s, lane);
                 __threadfence_block();
-                __syncthreads();
-                next = draw_from_segments<false>(P, seg, prow(P, b, n), nullptr, u, sh);
+                __syncwarp();
+                next = draw_from_sums<false>(P, seg, blk, pr, nullptr, u, lane);
             }
         } else {
-            next = draw_from_segments<false>(P, seg, prow(P, b, P.K), nullptr, u, sh);
+            next = draw_from_sums<false>(P, seg, blk, prow(P, b, P.K), nullptr, u, lane);
         }
     }
-    if (threadIdx.x == 0) {
-        if (sh.bad) atomicOr(P.status, kStatusBadToken);
+    if (lane == 0) {
+        if (bad) atomicOr(P.status, kStatusBadToken);
         else if (next < 0) atomicOr(P.status, kStatusZeroMass);
-        P.n_out[b] = sh.bad ? 0 : n;
+        P.n_out[b] = n;
         P.next_out[b] = next;
+        P.nstate[b] = 0;
     }
-    commit_round(P, b, sh.bad ? 0 : n, next, sh);
+    commit_round(P, b, n, next, lane);
 }
 
-// Returns true in every thread of the CTA that arrives last for sequence b.
-__device__ __forceinline__ bool arrive_last(const Params &P, int b, Shared &sh) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(P.ticket + b, 1u);
-        sh.is_last = prev == (uint32_t)(P.chunks - 1);
-        if (sh.is_last) __threadfence();
+// ---------------------------------------------------------------------------
+// kernels
+
+__device__ __forceinline__ void grid_dependents_may_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_for_primary_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// One warp per sequence, cached in the workspace for the later kernels: the
+// first rejection of a sampling sequence; for a greedy sequence, whether its
+// draft ids are valid and the target probability of each draft token.
+template <int kRule>
+__global__ void __launch_bounds__(kThreads) scan_kernel(const Params P) {
+    grid_dependents_may_launch();
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (b >= P.B) return;
+    const int rule = kRule == kPerSequence ? (int)P.mode[b] : kRule;
+    int32_t ns = 0;
+    if (rule == kSample) {
+        ns = first_rejection(P, b, lane);
+        if (lane == 0) {
+            const double u = P.u_res[b];
+            const float uh = __double2float_rn(u);
+            P.udd[b] = make_float2(uh, __double2float_rn(__dsub_rn(u, (double)uh)));
+        }
+    } else if (rule == kGreedy) {
+        int32_t t0, t1;
+        const bool bad = load_tokens(P, b, lane, t0, t1);
+        if (!bad) {
+            float *pt = P.ptok + (int64_t)b * P.K;
+            if (lane < P.K) pt[lane] = __ldg(prow(P, b, lane) + t0);
+            if (lane + 32 < P.K) pt[lane + 32] = __ldg(prow(P, b, lane + 32) + t1);
+        }
+        ns = bad ? kNBad : 1;
+    } else {
+        return;
     }
-    __syncthreads();
-    return sh.is_last != 0;
+    if (lane == 0) P.nstate[b] = ns;
 }
 
 template <int kRule>
-__global__ void __launch_bounds__(kThreads) verify_kernel(const Params P) {
-    __shared__ Shared sh;
-    const int b = blockIdx.x / P.chunks;
-    const int c = blockIdx.x - b * P.chunks;
+__device__ __forceinline__ void stream_body(const Params &P) {
+    // the decide kernel may be scheduled as soon as this grid's CTAs retire
+    grid_dependents_may_launch();
+    // the scan kernel's cached per-sequence data
+    wait_for_primary_grid();
+    const int lane = threadIdx.x & 31;
+    const int w = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    // per-item sequence data is fetched one item ahead
+    int item = w;
+    int32_t ns_next = 0, rule_next = kRule;
+    if (item < P.items && lane == 0) {
+        const int b = item / P.nseg;
+        if (kRule == kPerSequence) rule_next = P.mode[b];
+        if (kRule != kGreedy) ns_next = ld_l2(P.nstate + b);
+    }
+    for (; item < P.items; item += P.warps) {
+        const int b = item / P.nseg;
+        const int s = item - b * P.nseg;
+        const int rule = __shfl_sync(0xffffffffu, rule_next, 0);
+        const int32_t ns = __shfl_sync(0xffffffffu, ns_next, 0);
+        const int nxt = item + P.warps;
+        if (nxt < P.items && lane == 0) {
+            const int bn = nxt / P.nseg;
+            if (kRule == kPerSequence) rule_next = P.mode[bn];
+            if (kRule != kGreedy) ns_next = ld_l2(P.nstate + bn);
+        }
+        if (rule == kGreedy) greedy_item(P, b, s, lane);
+        else if (rule == kSample) sample_item(P, b, s, ns, lane);
+    }
+}
+
+template <int kRule>
+__global__ void __launch_bounds__(kThreads, SV_MIN_CTAS_PER_SM) stream_kernel(const Params P) {
+    stream_body<kRule>(P);
+}
+
+// The greedy stream needs fewer registers, so more warps fit per SM.
+template <>
+__global__ void __launch_bounds__(kThreads, SV_GREEDY_MIN_CTAS_PER_SM)
+stream_kernel<kGreedy>(const Params P) {
+    stream_body<kGreedy>(P);
+}
+
+// One warp per sequence: turns the partials into (n_accepted, next_token),
+// commits a round if asked, and leaves the workspace zeroed for the next call.
+constexpr int kDecideWarps = 2;  // small CTAs spread the per-sequence work over the SMs
+
+template <int kRule>
+__global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(const Params P) {
+    wait_for_primary_grid();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *P.queue = 0u;  // the stream kernel is done with it
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
+    if (b >= P.B) return;
     const int rule = kRule == kPerSequence ? (int)P.mode[b] : kRule;
-    if (rule == kGreedy) greedy_body(P, b, c, sh);
-    else if (rule == kSample) sample_body(P, b, c, sh);
-    if (!arrive_last(P, b, sh)) return;
     if (rule == kGreedy) {
-        greedy_decide(P, b, sh);
+        greedy_decide(P, b, lane);
     } else if (rule == kSample) {
-        sample_decide(P, b, sh);
-    } else if (threadIdx.x == 0) {
+        sample_decide(P, b, lane);
+    } else if (lane == 0) {
         atomicOr(P.status, kStatusBadMode);
         P.n_out[b] = 0;
         P.next_out[b] = -1;
     }
-    if (threadIdx.x == 0) P.ticket[b] = 0u;
 }
 
 }  // namespace sv

@@ -40,7 +40,7 @@ def test_host_only_calls(lib):
     assert sv.status_string(0) == "ok"
     assert "invalid" in sv.status_string(-1)
     assert "outside" in sv.status_string(1)
-    # workspace: 256-byte header, then B tickets, B flags, B*(K+1) keys, B*nseg pairs
+    # workspace: 256-byte header, then B miss flags, B cached n, B*(K+1) keys, B*nseg pairs
     n = sv.workspace_size(256, 5, 128256)
     assert n % 256 == 0 and n >= 256 + 256 * 4 * 2 + 256 * 6 * 8 + 256 * 126 * 8
     assert sv.workspace_size(0, 0, 1) == 256      # just the status header
@@ -84,5 +84,5 @@ def test_invalid_arguments_rejected_on_host(lib):
                                dummy, dummy, None, 8, ws, big, None) == -1
     assert lib.sv_verify_round(dummy, dummy, 10, dummy, 10, dummy, dummy, dummy, 2, 3, 10, dummy,
                                dummy, dummy, dummy, 0, ws, big, None) == -1
-    assert lib.sv_set_segments_per_cta(-1) == -1
+    assert lib.sv_set_ctas_per_sm(-1) == -1
     assert lib.sv_get_status(None, None, None) == -1

@@ -107,16 +107,21 @@ def test_edge_distributions_scaled():
     assert np.all(n[same] == 16)
 
 
-@pytest.mark.parametrize("spc", [1, 2, 3, 8, 16, 64])
-def test_launch_shapes_agree(spc):
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5, 0])
+def test_launch_shapes_agree(ctas):
+    """Grids from one CTA per SM (many items per warp) to full residency."""
     bt = make_inputs(3, "cuda", seed=777, B=40, V=40000, K=5)
     host = bt.numpy()
     try:
-        sv.set_segments_per_cta(spc)
-        check_sample(bt, host, label=f"spc={spc}")
+        sv.set_ctas_per_sm(ctas)
+        check_sample(bt, host, label=f"ctas={ctas}")
         check_greedy(bt, host)
+        p, q, t, ua, ur, md = host
+        n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur)
+        n1, x1, s1 = gpu_round(bt)
+        compare(p, q, ur, md, bt.K, n0, x0, n1, x1, s0, s1)
     finally:
-        sv.set_segments_per_cta(0)
+        sv.set_ctas_per_sm(0)
 
 
 def test_unaligned_rows_and_strides():
@@ -281,6 +286,29 @@ def test_sampling_batched_full():
     check_greedy(bt, host)
     del bt
     _free()
+
+
+def test_sampling_full_fresh_and_reused_workspace():
+    """Headline workload on three more seeds, each on a freshly zeroed workspace
+    and again on one still holding the previous batch's sums: every stage must
+    be reduced before the draw reads its sums, so neither zeros nor another
+    batch's sums may reach an output."""
+    reused = None
+    for seed in (11, 12, 13):
+        bt = make_inputs(3, "cuda", seed=seed)
+        p, q, t, ua, ur, md = bt.numpy()
+        n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
+        fresh = sv.Workspace(bt.B, bt.K, bt.V)
+        if reused is None:
+            reused = sv.Workspace(bt.B, bt.K, bt.V)
+        for ws in (fresh, reused):
+            n1, x1 = sv.verify_sample(bt.p, bt.q, bt.t, bt.u_acc, bt.u_res, ws=ws)
+            bnd = compare(p, q, ur, 1, bt.K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(),
+                          s0, ws.status())
+            if bnd:
+                BOUNDARY_REPORT.append((f"sampling seed {seed}", bnd))
+        del bt, fresh
+        _free()
 
 
 def test_mixed_round_full():
