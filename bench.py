@@ -34,7 +34,7 @@ DEFAULT_MODE = {1: "sample", 2: "greedy", 3: "sample", 4: "round", 5: "sample"}
 KERNEL_SOURCES = [
     "speculative_decoding_verification_08_gb300/csrc/sv_device.cuh",
     "speculative_decoding_verification_08_gb300/csrc/sv_tma.cuh",
-    "speculative_decoding_verification_08_gb300/csrc/sv_seq.cuh",
+    "speculative_decoding_verification_08_gb300/csrc/sv_item.cuh",
     "speculative_decoding_verification_08_gb300/csrc/specverify.cu",
 ]
 

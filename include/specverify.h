@@ -85,7 +85,12 @@ typedef struct CUstream_st *sv_stream_t;
 size_t sv_workspace_size(int32_t B, int32_t K, int64_t V);
 
 /* Zeroes a workspace on `stream` (once, before its first use).  Returns
- * SV_EWORKSPACE for a null or misaligned pointer, SV_ECUDA on failure. */
+ * SV_EWORKSPACE for a null or misaligned pointer, SV_ECUDA on failure.
+ * Afterwards the workspace serves any calls it is large enough for, one at a
+ * time in stream order: every call leaves its per-sequence state zeroed, and a
+ * call whose sizes differ from the previous call's on the same workspace first
+ * clears that state (one memset on its stream).  After a call reported
+ * SV_STATUS_TIMEOUT the state is undefined: initialise the workspace again. */
 int sv_workspace_init(void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* Greedy verification ("spec-verify", section "Method", greedy bullet):

@@ -10,7 +10,7 @@ INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "specverify.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "sv_tma.cuh"),
-                     os.path.join(CSRC, "sv_seq.cuh"),
+                     os.path.join(CSRC, "sv_item.cuh"),
                      os.path.join(INCLUDE, "specverify.h")]
 LIBRARY = os.path.join(PKG, "libspecverify.so")
 

@@ -10,15 +10,28 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "sv_device.cuh"
-#include "sv_seq.cuh"
+#include "sv_item.cuh"
 #include "specverify.h"
 
-// 1: large batches of 16-byte-aligned rows run as one sequence-per-CTA launch;
-// 0: they take the three-launch chunked path.  Both give identical results.
-#ifndef SV_SEQ_PATH
-#define SV_SEQ_PATH 1
+// 1: batches of 16-byte-aligned rows with at least one sequence per SM run as
+// one launch over (sequence, chunk) items; 0: they take the three-launch
+// chunked path.  Both give identical results.
+#ifndef SV_ITEM_PATH
+#define SV_ITEM_PATH 1
+#endif
+// Segments (1024 elements) per item of the single-launch kernel: sampling
+// rows are streamed whole by one CTA (a draw then needs no other CTA's sums
+// early, and an item switch costs the producer more than the finer balance
+// gains); greedy rows in chunks, so that a miss found in one chunk stops the
+// others and the batch's bytes spread over every SM.
+#ifndef SV_ITEM_SEGS_SAMPLE
+#define SV_ITEM_SEGS_SAMPLE 128
+#endif
+#ifndef SV_ITEM_SEGS
+#define SV_ITEM_SEGS 32
 #endif
 
 namespace {
@@ -34,11 +47,11 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
 }
 
 // Workspace layout:
-// [status, queue | miss[B] | nstate[B] | ptok[B][K] | best[B][K+1] | seg[B][nseg] |
-//  blk[B][nseg][8] | udd[B]], every region 256-byte aligned; everything before
-// seg must start at zero (and every call leaves it so).
+// [status, queue, exit | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] |
+//  seg[B][nseg] | blk[B][nseg][8] | udd[B]], every region 256-byte aligned;
+// everything before seg must start at zero (and every call leaves it so).
 struct Layout {
-    size_t status, queue, miss, nstate, ptok, best, seg, blk, udd, total;
+    size_t status, queue, miss, nstate, done, ptok, best, seg, blk, udd, total;
 };
 
 Layout layout(int32_t B, int32_t K, int64_t V) {
@@ -50,6 +63,8 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     L.miss = off;
     off += round_up((size_t)B * sizeof(int32_t));
     L.nstate = off;
+    off += round_up((size_t)B * sizeof(int32_t));
+    L.done = off;
     off += round_up((size_t)B * sizeof(int32_t));
     L.ptok = off;
     off += round_up((size_t)B * (size_t)K * sizeof(float));
@@ -72,19 +87,19 @@ struct DeviceInfo {
     int sms = 0;
     int occupancy[3] = {0, 0, 0};      // resident CTAs per SM, register stream kernels
     int tma_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, bulk-copy stream kernels
-    int seq_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, sequence-per-CTA kernels
+    int item_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, single-launch item kernels
 };
 
 template <int kRule>
-int seq_occupancy_of() {
-    if (cudaFuncSetAttribute(sv::seq_round_kernel<kRule>,
+int item_occupancy_of() {
+    if (cudaFuncSetAttribute(sv::item_round_kernel<kRule>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sv::kSeqSmemBytes) != cudaSuccess)
+                             sv::kItemSmemBytes) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv::seq_round_kernel<kRule>,
-                                                      sv::kSeqThreads,
-                                                      sv::kSeqSmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv::item_round_kernel<kRule>,
+                                                      sv::kItemThreads,
+                                                      sv::kItemSmemBytes) != cudaSuccess)
         return 0;
     return n;
 }
@@ -116,7 +131,7 @@ int occupancy_of() {
 }
 
 // SM count and per-kernel residency of the current device, queried once.
-bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *seq_occ) {
+bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *item_occ) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     std::lock_guard<std::mutex> lock(g_info_mu);
@@ -131,15 +146,15 @@ bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *seq_occ) {
         d.tma_occupancy[sv::kGreedy] = tma_occupancy_of<sv::kGreedy>();
         d.tma_occupancy[sv::kSample] = tma_occupancy_of<sv::kSample>();
         d.tma_occupancy[sv::kPerSequence] = tma_occupancy_of<sv::kPerSequence>();
-        d.seq_occupancy[sv::kGreedy] = seq_occupancy_of<sv::kGreedy>();
-        d.seq_occupancy[sv::kSample] = seq_occupancy_of<sv::kSample>();
-        d.seq_occupancy[sv::kPerSequence] = seq_occupancy_of<sv::kPerSequence>();
+        d.item_occupancy[sv::kGreedy] = item_occupancy_of<sv::kGreedy>();
+        d.item_occupancy[sv::kSample] = item_occupancy_of<sv::kSample>();
+        d.item_occupancy[sv::kPerSequence] = item_occupancy_of<sv::kPerSequence>();
         d.sms = n;
     }
     *sms = d.sms;
     *occ = d.occupancy[rule] > 0 ? d.occupancy[rule] : 1;
     *tma_occ = d.tma_occupancy[rule];
-    *seq_occ = d.seq_occupancy[rule];
+    *item_occ = d.item_occupancy[rule];
     return true;
 }
 
@@ -183,11 +198,11 @@ int launch_round(const sv::Params &P, bool tma, unsigned grid, cudaStream_t st) 
 }
 
 // Picks the round's kernels.  With every row 16-byte aligned and at least one
-// sequence per SM: one persistent kernel in which each CTA owns whole
-// sequences.  With aligned rows and fewer sequences: scan -> bulk-copy stream
-// over chunks of segments -> decide.  Otherwise: scan -> register stream ->
-// decide.  Persistent grids hold as many CTAs as the SMs fit at once (or the
-// tuning override), never more than there is work for.
+// sequence per SM: one persistent launch over (sequence, chunk) items.  With
+// aligned rows and fewer sequences: scan -> bulk-copy stream over chunks of
+// segments -> decide.  Otherwise: scan -> register stream -> decide.
+// Persistent grids hold as many CTAs as the SMs fit at once (or the tuning
+// override), never more than there is work for.
 int launch(int rule, sv::Params P, sv_stream_t stream) {
     const int64_t nseg = num_segments(P.V);
     const int64_t items = (int64_t)P.B * nseg;
@@ -196,26 +211,29 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
     P.items = (int32_t)items;
     const int64_t cps = (nseg + sv::kChunkSegs - 1) / sv::kChunkSegs;
     P.nchunks = (int32_t)((int64_t)P.B * cps);
-    int sms = 0, occ = 0, tma_occ = 0, seq_occ = 0;
-    if (!device_info(rule, &sms, &occ, &tma_occ, &seq_occ)) return SV_ECUDA;
+    P.isegs = (int32_t)std::min<int64_t>(nseg, rule == sv::kSample ? SV_ITEM_SEGS_SAMPLE : SV_ITEM_SEGS);
+    P.ichunks = (int32_t)((nseg + P.isegs - 1) / P.isegs);
+    int sms = 0, occ = 0, tma_occ = 0, item_occ = 0;
+    if (!device_info(rule, &sms, &occ, &tma_occ, &item_occ)) return SV_ECUDA;
     const bool aligned = aligned_rows(P.p, P.ps) &&
                          (rule == sv::kGreedy || P.K == 0 || aligned_rows(P.q, P.qs));
     const int32_t forced = g_ctas_per_sm.load();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (SV_SEQ_PATH && aligned && seq_occ > 0 && P.B >= sms) {
-        const int64_t grid = (int64_t)sms * (forced > 0 ? std::min<int64_t>(forced, seq_occ) : seq_occ);
+    if (SV_ITEM_PATH && aligned && item_occ > 0 && P.B >= sms) {
+        int64_t grid = (int64_t)sms * (forced > 0 ? std::min<int64_t>(forced, item_occ) : item_occ);
+        grid = std::min<int64_t>(grid, (int64_t)P.B * P.ichunks);
         P.warps = (int32_t)(grid * sv::kWarps);
         g_last_grid = grid;
         switch (rule) {
             case sv::kGreedy:
-                sv::seq_round_kernel<sv::kGreedy><<<(unsigned)grid, sv::kSeqThreads, sv::kSeqSmemBytes, st>>>(P);
+                sv::item_round_kernel<sv::kGreedy><<<(unsigned)grid, sv::kItemThreads, sv::kItemSmemBytes, st>>>(P);
                 break;
             case sv::kSample:
-                sv::seq_round_kernel<sv::kSample><<<(unsigned)grid, sv::kSeqThreads, sv::kSeqSmemBytes, st>>>(P);
+                sv::item_round_kernel<sv::kSample><<<(unsigned)grid, sv::kItemThreads, sv::kItemSmemBytes, st>>>(P);
                 break;
             default:
-                sv::seq_round_kernel<sv::kPerSequence>
-                    <<<(unsigned)grid, sv::kSeqThreads, sv::kSeqSmemBytes, st>>>(P);
+                sv::item_round_kernel<sv::kPerSequence>
+                    <<<(unsigned)grid, sv::kItemThreads, sv::kItemSmemBytes, st>>>(P);
                 break;
         }
         return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
@@ -239,6 +257,41 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
     }
 }
 
+// The sizes each workspace's per-sequence state was last laid out for.  A
+// call leaves that state zeroed, but for its own sizes: the regions move with
+// B, K and V, so a call with other sizes first clears everything between the
+// status word and the sums.  A workspace seen by sv_workspace_init is known to
+// be all zero.
+struct StateKey {
+    int32_t B = -1, K = -1;
+    int64_t V = -1;
+    bool zeroed = false;
+};
+std::mutex g_ws_mu;
+std::unordered_map<uintptr_t, StateKey> g_ws_state;
+
+void note_zeroed(const void *ws) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    StateKey k;
+    k.zeroed = true;
+    g_ws_state[reinterpret_cast<uintptr_t>(ws)] = k;
+}
+
+int prepare_state(const sv::Params &P, void *ws, cudaStream_t st) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    StateKey &k = g_ws_state[reinterpret_cast<uintptr_t>(ws)];
+    if (!k.zeroed && (k.B != P.B || k.K != P.K || k.V != P.V)) {
+        const Layout L = layout(P.B, P.K, P.V);
+        if (cudaMemsetAsync(static_cast<char *>(ws) + L.queue, 0, L.seg - L.queue, st) != cudaSuccess)
+            return SV_ECUDA;
+    }
+    k.zeroed = false;
+    k.B = P.B;
+    k.K = P.K;
+    k.V = P.V;
+    return SV_OK;
+}
+
 int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return SV_EWORKSPACE;
     const Layout L = layout(P.B, P.K, P.V);
@@ -247,6 +300,7 @@ int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
     P.status = reinterpret_cast<uint32_t *>(base + L.status);
     P.miss = reinterpret_cast<int32_t *>(base + L.miss);
     P.nstate = reinterpret_cast<int32_t *>(base + L.nstate);
+    P.done = reinterpret_cast<int32_t *>(base + L.done);
     P.queue = reinterpret_cast<uint32_t *>(base + L.queue);
     P.ptok = reinterpret_cast<float *>(base + L.ptok);
     P.best = reinterpret_cast<unsigned long long *>(base + L.best);
@@ -298,7 +352,9 @@ int sv_workspace_init(void *workspace, size_t workspace_bytes, sv_stream_t strea
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return SV_EWORKSPACE;
     cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes,
                                     reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SV_OK : SV_ECUDA;
+    if (e != cudaSuccess) return SV_ECUDA;
+    note_zeroed(workspace);
+    return SV_OK;
 }
 
 int sv_verify_greedy(const float *p, int64_t p_row_stride, const int32_t *t, int32_t B, int32_t K,
@@ -309,6 +365,7 @@ int sv_verify_greedy(const float *p, int64_t p_row_stride, const int32_t *t, int
     sv::Params P = make_params(p, p_row_stride, nullptr, 0, t, nullptr, nullptr, nullptr, B, K, V,
                                n_accepted, next_token);
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kGreedy, P, stream);
 }
 
@@ -323,6 +380,7 @@ int sv_verify_sample(const float *p, int64_t p_row_stride, const float *q, int64
     sv::Params P = make_params(p, p_row_stride, q, q_row_stride, t, u_accept, u_resample, nullptr,
                                B, K, V, n_accepted, next_token);
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kSample, P, stream);
 }
 
@@ -342,6 +400,7 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride, c
     P.lengths = lengths;
     P.max_len = max_len;
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kPerSequence, P, stream);
 }
 

@@ -98,11 +98,14 @@ struct Params {
     int32_t *lengths;
     int32_t max_len;
     int32_t nchunks;            // bulk-copy path: chunks of the batch
+    int32_t ichunks;            // item kernel: items (chunks) per sequence
+    int32_t isegs;              // item kernel: segments per item
     // workspace
     uint32_t *status;
     uint32_t *queue;            // bulk-copy path: next chunk to hand out
     int32_t *miss;              // [B] greedy: kFlagBase - first missed row
     int32_t *nstate;            // [B] first rejection + 1 (sampling), 1 (greedy), kNBad
+    int32_t *done;              // [B] item kernel: items of the sequence retired this round
     float *ptok;                // [B][K] greedy: p_i(t_i)
     unsigned long long *best;   // [B][K+1] packed (value, index) keys
     float2 *seg;                // [B][nseg] double-fp32 segment sums
@@ -291,6 +294,81 @@ __device__ __forceinline__ void elem_mass(float p, float q, float &hi, float &lo
         lo = 0.f;
     }
 }
+
+// ---------------------------------------------------------------------------
+// mbarrier, bulk-copy and timing primitives (inline PTX)
+
+constexpr uint32_t kStatusTimeout = 16u;
+constexpr uint64_t kWaitLimitNs = 250000000ull;  // any single wait gives up after 250 ms
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
+    asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try(unsigned long long *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// kWaitLimitNs of wall-clock time.  The clock is read only once a first try
+// has failed: a phase that is already complete costs one try_wait.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              unsigned long long *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Idle-wait bookkeeping: idle() returns false once no progress has been made
+// for kWaitLimitNs.
+struct IdleClock {
+    uint64_t since = 0;
+    __device__ void progress() { since = 0; }
+    __device__ bool idle() {
+        const uint64_t now = global_ns();
+        if (since == 0) since = now;
+        if (now - since > kWaitLimitNs) return false;
+        __nanosleep(128);
+        return true;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // memory helpers
@@ -601,11 +679,10 @@ __device__ int search_block(const float *pr, const float *qr, int64_t base, int6
     return last_nz < 0 ? -1 : (int)(base + last_nz);
 }
 
-// Given lanes holding consecutive sums v (lane order = index order) starting
-// at running mass `prefix`: the first lane whose inclusive sum exceeds T
-// (-1 if none) and the running mass before it.
-__device__ __forceinline__ int first_crossing(dd v, dd prefix, dd T, int lane, dd &before) {
-    const dd inc = warp_incl_scan(v, lane);
+// Given lanes holding consecutive sums v (lane order = index order) and their
+// inclusive warp scan inc, starting at running mass `prefix`: the first lane
+// whose inclusive sum exceeds T (-1 if none) and the running mass before it.
+__device__ __forceinline__ int crossing_of_scan(dd v, dd inc, dd prefix, dd T, int lane, dd &before) {
     const unsigned m = __ballot_sync(0xffffffffu, v.hi != 0.f && dd_gt(dd_add(prefix, inc), T));
     if (!m) return -1;
     const int L = __ffs(m) - 1;
@@ -615,18 +692,36 @@ __device__ __forceinline__ int first_crossing(dd v, dd prefix, dd T, int lane, d
     return L;
 }
 
+__device__ __forceinline__ int first_crossing(dd v, dd prefix, dd T, int lane, dd &before) {
+    return crossing_of_scan(v, warp_incl_scan(v, lane), prefix, T, lane, before);
+}
+
+__device__ __forceinline__ dd split_uniform(double ur) {
+    const float uh = __double2float_rn(ur);
+    return {uh, __double2float_rn(__dsub_rn(ur, (double)uh))};
+}
+
+// Where a draw finds the sequence's uniform and its block sums.
+struct DrawInputs {
+    dd u;                     // the uniform split into two fp32 parts, unless u_res is set
+    const double *u_res;      // else: loaded here once the segment loads are out
+    const float2 *blk_sh;     // block sums staged in shared memory (else read from blk) ...
+    unsigned long long *bar;  // ... by a bulk copy completing on this mbarrier phase
+    uint32_t parity;
+};
+
 // Inverse-CDF draw for sequence b over the segment sums seg[0..nseg) and
-// block sums blk of the row pair (pr, qr) (decide kernel, one warp): the token,
-// or -1 if the total mass is zero.  Three steps, each one load round trip:
-// the segment (lane l owns segments [l * per, (l + 1) * per)), the block
-// within it (lanes 0..7), the element within the block.
+// block sums blk of the row pair (pr, qr) (one warp): the token, -1 if the
+// total mass is zero, -2 if the staged block sums never arrived.  The segment
+// (lane l owns segments [l * per, (l + 1) * per)), the block within it (lanes
+// 0..7), the element within the block: one load round trip each, or two in
+// all when the block sums were staged while the segment sums loaded.
 template <bool kResidual>
 __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *blk,
-                              const float *pr, const float *qr, dd u, int lane) {
+                              const float *pr, const float *qr, const DrawInputs &in, int lane) {
     const int per = (P.nseg + 31) / 32;
     const int r0 = min(P.nseg, lane * per), r1 = min(P.nseg, r0 + per);
     dd v[kSegRegs];
-    dd own = {0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < kSegRegs; ++r) {
         v[r] = dd{0.f, 0.f};
@@ -634,19 +729,24 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
             const float2 x = ld_l2(seg + r0 + r);
             v[r] = dd{x.x, x.y};
         }
-        own = dd_add(own, v[r]);
     }
+    const dd u = in.u_res ? split_uniform(__ldg(in.u_res)) : in.u;
+    dd own = {0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kSegRegs; ++r) own = dd_add(own, v[r]);
     for (int s = r0 + kSegRegs; s < r1; ++s) {  // rows longer than 32 * kSegRegs segments
         const float2 x = ld_l2(seg + s);
         own = dd_add(own, dd{x.x, x.y});
     }
     const dd inc = warp_incl_scan(own, lane);
     const dd total = shfl_dd(inc, 31);
+    // the staged copy has to land before this warp returns, whatever the outcome
+    if (in.blk_sh && !__all_sync(0xffffffffu, mbar_wait(in.bar, in.parity))) return -2;
     if (total.hi == 0.f) return -1;
     const dd T = threshold(u, total);
     const dd zero = {0.f, 0.f};
     dd before;
-    const int L = first_crossing(own, zero, T, lane, before);
+    const int L = crossing_of_scan(own, inc, zero, T, lane, before);
     // the segment, the running mass before it, and the time T is past every segment
     int sg = -1;
     dd sbefore = zero;
@@ -700,7 +800,8 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
     // block within the segment
     dd bv = zero;
     if (lane < kBlocks) {
-        const float2 x = ld_l2(blk + (int64_t)sg * kBlocks + lane);
+        const float2 x = in.blk_sh ? in.blk_sh[sg * kBlocks + lane]
+                                   : ld_l2(blk + (int64_t)sg * kBlocks + lane);
         bv = dd{x.x, x.y};
     }
     dd bbefore;
@@ -763,7 +864,8 @@ __device__ void greedy_decide(const Params &P, int b, int lane) {
 __device__ void sample_decide(const Params &P, int b, int lane) {
     const int ns = ld_l2(P.nstate + b);
     const float2 uf = ld_l2(P.udd + b);  // loaded alongside, used only if the sequence is valid
-    const dd u = {uf.x, uf.y};
+    DrawInputs in = {};
+    in.u = dd{uf.x, uf.y};
     const bool bad = ns == kNBad;
     int n = 0, next = -1;
     if (!bad) {
@@ -771,17 +873,17 @@ __device__ void sample_decide(const Params &P, int b, int lane) {
         const float2 *seg = P.seg + (int64_t)b * P.nseg;
         const float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
         if (n < P.K) {
-            next = draw_from_sums<true>(P, seg, blk, prow(P, b, n), qrow(P, b, n), u, lane);
+            next = draw_from_sums<true>(P, seg, blk, prow(P, b, n), qrow(P, b, n), in, lane);
             if (next < 0) {
                 // zero residual mass (unnormalised rows): draw from p_n itself
                 const float *pr = prow(P, b, n);
                 for (int s = 0; s < P.nseg; ++s) segment_sum_store<false>(P, b, pr, nullptr, s, lane);
                 __threadfence_block();
                 __syncwarp();
-                next = draw_from_sums<false>(P, seg, blk, pr, nullptr, u, lane);
+                next = draw_from_sums<false>(P, seg, blk, pr, nullptr, in, lane);
             }
         } else {
-            next = draw_from_sums<false>(P, seg, blk, prow(P, b, P.K), nullptr, u, lane);
+            next = draw_from_sums<false>(P, seg, blk, prow(P, b, P.K), nullptr, in, lane);
         }
     }
     if (lane == 0) {

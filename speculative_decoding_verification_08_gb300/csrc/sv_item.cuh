@@ -1,0 +1,755 @@
+// sv_item.cuh -- a whole verification round as one persistent kernel over
+// (sequence, chunk) work items (sm_103a); used when every row starts on a
+// 16-byte boundary and the batch has at least one sequence per SM.
+//
+// A work item is `ichunks`-th part of one sequence: `isegs` consecutive
+// 1024-element segments of the rows that sequence needs.  Items are handed out
+// in order from a device-wide counter, so every CTA streams until the batch is
+// done and no SM is left with a larger share of the bytes than the others.
+// Each CTA runs three roles:
+//  * a producer warp takes the next item, finds what the item needs one item
+//    ahead of use (sampling: the first rejection n from gathered p_i(t_i),
+//    q_i(t_i) and the exact fp64 accept test; greedy: the draft tokens and
+//    p_i(t_i)), and streams the item's row segments into a ring of
+//    shared-memory stages with cp.async.bulk;
+//  * eight consumer warps reduce the stages -- the double-fp32 segment and
+//    block sums of a residual (or bonus) row, stored to the workspace, or a
+//    greedy segment's maximum folded into the item's per-row key in shared
+//    memory, a draft-token miss raising the sequence's flag;
+//  * a retire warp frees an item whose stages are all consumed: it merges the
+//    item's greedy keys into the sequence's keys and counts the item as done
+//    (after a device-scope fence that also publishes the consumers' sums);
+//    the CTA whose item completes a sequence queues the sequence for
+//  * a decide warp, which turns it into (n_accepted, next_token) and clears the
+//    sequence's state for the next round.  Nothing waits for another CTA: the
+//    last item to finish decides, and retiring never waits for a decision.
+//
+// Greedy items stream their rows in order and stop before a row once a miss in
+// an earlier row is known (seen by this CTA, or recorded for the sequence by
+// any CTA), and after a row once this CTA has seen a miss in it.  Every wait is
+// bounded by kWaitLimitNs of wall-clock time (then SV_STATUS_TIMEOUT is set,
+// the warp leaves its loop, and the workspace has to be initialised again
+// before its next use).
+#pragma once
+
+#include "sv_tma.cuh"
+
+namespace sv {
+
+// Items a CTA holds at once: the one streaming, ones whose stages are still in
+// the ring, and ones waiting for the retire warp.
+#ifndef SV_ITEM_SLOTS
+#define SV_ITEM_SLOTS 4
+#endif
+constexpr int kItemSlots = SV_ITEM_SLOTS;
+constexpr int kItemDecideWarps = 2;
+constexpr int kItemThreads = (kTmaConsumers + 2 + kItemDecideWarps) * 32;
+// Warp w issues on scheduler w % 4.  The producer's issue rate bounds the
+// stream, so it shares its scheduler only with the two decide warps (mostly
+// idle); the eight consumers and the retire warp fill the other three.
+#ifndef SV_ROLE_MAP
+#define SV_ROLE_MAP 1
+#endif
+#if SV_ROLE_MAP
+constexpr int kItemProducerWarp = 0;
+constexpr int kItemDecideWarpA = 4;
+constexpr int kItemDecideWarpB = 8;
+constexpr int kItemRetireWarp = 11;
+#else
+constexpr int kItemProducerWarp = 8;
+constexpr int kItemDecideWarpA = 10;
+constexpr int kItemDecideWarpB = 11;
+constexpr int kItemRetireWarp = 9;
+#endif
+static_assert(kItemThreads == 12 * 32, "role map assumes twelve warps");
+constexpr int kDecideQueue = 16;  // sequences a CTA has completed but not yet decided
+
+struct ItemSlot {
+    int state;     // 0 free, 1 streaming, 2 every stage issued (`issued` final)
+    int b;
+    int rule;
+    int ns;        // sampling: n + 1; greedy: 1; kNBad: invalid draft ids; 0: bad mode
+    int issued;
+    int consumed;
+    int miss;      // greedy: kFlagBase - first missed row seen in this item
+    int pad;
+    unsigned long long keys[kMaxK + 1];  // greedy: packed (value, index) maximum per row
+};
+
+// What a consumer needs to know about a stage beyond its item slot (the
+// sequence, n and hence the row pointers live there): 32 bytes, written with
+// two 16-byte stores.
+struct __align__(16) ItemMeta {
+    int s;       // first segment of the stage
+    int slot;    // item slot the stage belongs to
+    int kind;    // StageKind
+    int nparts;  // segments in the stage (kMass, kArgmax: 1 or 2)
+    int row;     // greedy: row index
+    int tok;     // greedy: the row's draft token, -1 for the bonus row
+    float pt;    // greedy: p_row(tok)
+    int pad;
+};
+
+struct ItemShared {
+    int ticket;  // next stage a consumer takes (ring position = ticket % kStages)
+    unsigned long long full[kStages];
+    unsigned long long empty[kStages];
+    ItemMeta meta[kStages];
+    ItemSlot slot[kItemSlots];
+    int producer_done;
+    int retire_done;          // 1 once the retire warp has left (2: after a timeout)
+    int dq_head;              // decide queue: entries pushed so far (retire warp only)
+    int dq_claim;             // entries claimed by the decide warps
+    int4 dq[kDecideQueue];    // (b, rule, ns, h + 1 while entry h waits; 0 once read)
+    unsigned long long dbar[kItemDecideWarps];  // each decide warp's staging copy
+};
+
+// Dynamic shared memory: the header, each decide warp's block-sum buffer (rows
+// of up to kDecideSegs segments), the stage ring.
+constexpr int kItemHeaderBytes = 4096;
+constexpr int kDecideSegs = 128;
+constexpr int kDecideBytes = kDecideSegs * kBlocks * 8;
+constexpr int kItemBufOffset = kItemHeaderBytes + kItemDecideWarps * kDecideBytes;
+static_assert(sizeof(ItemShared) <= kItemHeaderBytes, "shared header too large");
+constexpr int kItemSmemBytes = kItemBufOffset + kStages * kStageBytes;
+
+__device__ __forceinline__ int ld_volatile(const int32_t *p) {
+    return *reinterpret_cast<const volatile int32_t *>(p);
+}
+
+// Loads of read-only inputs issued where they stand: a volatile asm statement
+// keeps its place among the producer's other asm (barrier waits, copies), so
+// the compiler cannot sink it to the value's first use an item later, and the
+// warp waits only if the value is still missing when it is used.
+__device__ __forceinline__ int32_t ld_early(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_early(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint8_t ld_early(const uint8_t *p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    return (uint8_t)v;
+}
+
+// ---------------------------------------------------------------------------
+// producer
+
+// Per-lane view of an item's sequence: draft positions lane and lane + 32.
+struct ItemPre {
+    int b;  // >= P.B: no item
+    int s0, s1;  // the item's segments [s0, s1)
+    int rule;
+    int32_t t0, t1;
+    float u0, u1, pt0, pt1, qt0, qt1;
+    bool bad;
+};
+
+__device__ __forceinline__ int seg_len(int64_t V, int s) {
+    const int64_t rem = V - (int64_t)s * kSeg;
+    return (int)(rem < kSeg ? rem : kSeg);
+}
+
+struct ItemProducer {
+    const Params &P;
+    ItemShared &sh;
+    unsigned char *buf;
+    int lane;
+    // ring position, its phase and the stages filled so far (lane 0's copies)
+    int k = 0;
+    uint32_t phase = 0;
+    int fills = 0;
+    bool ok = true;
+
+    __device__ ItemProducer(const Params &P_, ItemShared &sh_, unsigned char *buf_, int lane_)
+        : P(P_), sh(sh_), buf(buf_), lane(lane_) {}
+
+    // Lane 0 only: waits (bounded) for the next ring position, writes its
+    // record and copies c0 elements from g0 and c1 from g1 into it.
+    __device__ bool put(const ItemMeta &m, const float *g0, int c0, const float *g1, int c1) {
+        if (!mbar_wait(&sh.empty[k], phase ^ 1u)) return false;
+        uint4 *dst = reinterpret_cast<uint4 *>(&sh.meta[k]);
+        dst[0] = make_uint4((uint32_t)m.s, (uint32_t)m.slot, (uint32_t)m.kind, (uint32_t)m.nparts);
+        dst[1] = make_uint4((uint32_t)m.row, (uint32_t)m.tok, __float_as_uint(m.pt), 0u);
+        mbar_arrive_expect_tx(&sh.full[k], 4u * (uint32_t)(c0 + c1));
+        unsigned char *d = buf + (size_t)k * kStageBytes;
+        if (c0) bulk_copy_g2s(d, g0, 4u * c0, &sh.full[k]);
+        if (c1) bulk_copy_g2s(d + kPartBytes, g1, 4u * c1, &sh.full[k]);
+        ++fills;
+        if (++k == kStages) {
+            k = 0;
+            phase ^= 1u;
+        }
+        return true;
+    }
+
+    // Lane 0's verdict to the warp; the status bit is raised once.
+    __device__ void sync_ok() {
+        const bool was = ok;
+        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+        (void)was;
+    }
+
+    // CTA c starts with items c, c + G and c + 2G (G = gridDim.x); later ones
+    // come from the counter.  take() returns the oldest of two items fetched
+    // ahead and issues the next atomic, whose value is read two items later:
+    // under a saturated memory system a round trip can outlast one item.
+    int pending = 0, pending2 = 0;
+    __device__ int take() {
+        const int got = __shfl_sync(0xffffffffu, pending, 0);
+        pending = pending2;
+        if (lane == 0) pending2 = 3 * (int)gridDim.x + (int)atomicAdd(P.queue, 1u);
+        return got;
+    }
+
+    // The item's sequence, segment range and per-position data (loads issued,
+    // not waited for).
+    template <int kRule>
+    __device__ ItemPre begin(int item) {
+        ItemPre x = {};
+        x.b = P.B;
+        if (item >= P.B * P.ichunks) return x;
+        const int b = item / P.ichunks, c = item - b * P.ichunks;
+        x.b = b;
+        x.s0 = c * P.isegs;
+        x.s1 = min(P.nseg, x.s0 + P.isegs);
+        x.rule = kRule == kPerSequence ? (int)ld_early(P.mode + b) : kRule;
+        const int64_t tb = (int64_t)b * P.K;
+        if (lane < P.K) x.t0 = ld_early(P.t + tb + lane);
+        if (lane + 32 < P.K) x.t1 = ld_early(P.t + tb + lane + 32);
+        if (kRule != kGreedy && P.u_acc) {  // (loaded for every rule in a mixed round)
+            if (lane < P.K) x.u0 = ld_early(P.u_acc + tb + lane);
+            if (lane + 32 < P.K) x.u1 = ld_early(P.u_acc + tb + lane + 32);
+        }
+        return x;
+    }
+
+    __device__ void gather(ItemPre &x) {
+        if (x.b >= P.B || (x.rule != kSample && x.rule != kGreedy)) return;
+        const bool b0 = lane < P.K && (x.t0 < 0 || (int64_t)x.t0 >= P.V);
+        const bool b1 = lane + 32 < P.K && (x.t1 < 0 || (int64_t)x.t1 >= P.V);
+        x.bad = __any_sync(0xffffffffu, b0 || b1);
+        if (x.bad) return;
+        if (lane < P.K) x.pt0 = ld_early(prow(P, x.b, lane) + x.t0);
+        if (lane + 32 < P.K) x.pt1 = ld_early(prow(P, x.b, lane + 32) + x.t1);
+        if (x.rule == kSample) {
+            if (lane < P.K) x.qt0 = ld_early(qrow(P, x.b, lane) + x.t0);
+            if (lane + 32 < P.K) x.qt1 = ld_early(qrow(P, x.b, lane + 32) + x.t1);
+        }
+    }
+
+    // n + 1 for sampling (exact fp64 accept test), 1 for greedy, kNBad for
+    // invalid draft ids, 0 for an invalid mode.
+    __device__ int finish(const ItemPre &x) {
+        if (x.rule != kSample && x.rule != kGreedy) return 0;
+        if (x.bad) return kNBad;
+        if (x.rule == kGreedy) return 1;
+        const bool r0 = lane < P.K && !(__dmul_rn((double)x.u0, (double)x.qt0) < (double)x.pt0);
+        const bool r1 = lane + 32 < P.K && !(__dmul_rn((double)x.u1, (double)x.qt1) < (double)x.pt1);
+        const unsigned m0 = __ballot_sync(0xffffffffu, r0);
+        const unsigned m1 = __ballot_sync(0xffffffffu, r1);
+        const int n = m0 ? __ffs(m0) - 1 : (m1 ? 32 + __ffs(m1) - 1 : P.K);
+        return n + 1;
+    }
+
+    __device__ int copy_len(int s) const { return seg_len(P.V, s) & ~3; }
+
+    // Residual row pair (p_n, q_n) segment by segment, or the bonus row p_K
+    // two segments per stage.  The stage loop runs on lane 0 alone.
+    __device__ int stream_sample(const ItemPre &c, int n, int x) {
+        int stages = 0;
+        if (lane == 0 && ok) {
+            ItemMeta m = {};
+            m.slot = x;
+            m.tok = -1;
+            if (n < P.K) {
+                const float *pr = prow(P, c.b, n), *qr = qrow(P, c.b, n);
+                m.kind = kPair;
+                m.nparts = 2;
+                for (int s = c.s0; s < c.s1; ++s) {
+                    m.s = s;
+                    const int cc = copy_len(s);
+                    if (!put(m, pr + (int64_t)s * kSeg, cc, qr + (int64_t)s * kSeg, cc)) {
+                        ok = false;
+                        break;
+                    }
+                    ++stages;
+                }
+            } else {
+                const float *pr = prow(P, c.b, P.K);
+                m.kind = kMass;
+                for (int s = c.s0; s < c.s1; s += 2) {
+                    m.s = s;
+                    m.nparts = s + 1 < c.s1 ? 2 : 1;
+                    const int c1 = m.nparts == 2 ? copy_len(s + 1) : 0;
+                    if (!put(m, pr + (int64_t)s * kSeg, copy_len(s), pr + (int64_t)(s + 1) * kSeg, c1)) {
+                        ok = false;
+                        break;
+                    }
+                    ++stages;
+                }
+            }
+        }
+        sync_ok();
+        return __shfl_sync(0xffffffffu, stages, 0);
+    }
+
+    // Greedy rows 0..K of the item's segments, in order, two segments per
+    // stage.  The sequence's flag is read one row ahead of its use, so the
+    // check costs no wait.
+    __device__ int stream_greedy(const ItemPre &c, int x) {
+        int stages = 0;
+        int seen = 0;  // the sequence's flag as last read (lane 0)
+        bool stop = !ok;
+        for (int i = 0; i <= P.K && !stop; ++i) {
+            int tok = -1;
+            float pt = 0.f;
+            if (i < P.K) {
+                tok = __shfl_sync(0xffffffffu, i < 32 ? c.t0 : c.t1, i & 31);
+                pt = __shfl_sync(0xffffffffu, i < 32 ? c.pt0 : c.pt1, i & 31);
+            }
+            if (lane == 0) {
+                const int flag_now = seen;
+                seen = ld_volatile(P.miss + c.b);  // used at the next row
+                const float *pr = prow(P, c.b, i);
+                ItemMeta m = {};
+                m.kind = kArgmax;
+                m.slot = x;
+                m.row = i;
+                m.tok = tok;
+                m.pt = pt;
+                for (int s = c.s0; s < c.s1; s += 2) {
+                    if (max(*(volatile int *)&sh.slot[x].miss, flag_now) > kFlagBase - i) {
+                        stop = true;  // an earlier row missed
+                        break;
+                    }
+                    m.s = s;
+                    m.nparts = s + 1 < c.s1 ? 2 : 1;
+                    const int c1 = m.nparts == 2 ? copy_len(s + 1) : 0;
+                    if (!put(m, pr + (int64_t)s * kSeg, copy_len(s), pr + (int64_t)(s + 1) * kSeg, c1)) {
+                        ok = false;
+                        stop = true;
+                        break;
+                    }
+                    ++stages;
+                }
+                if (*(volatile int *)&sh.slot[x].miss >= kFlagBase - i) stop = true;
+            }
+            stop = __shfl_sync(0xffffffffu, stop, 0) != 0;
+        }
+        sync_ok();
+        return __shfl_sync(0xffffffffu, stages, 0);
+    }
+};
+
+template <int kRule>
+__device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf, int lane) {
+    ItemProducer pr(P, sh, buf, lane);
+    IdleClock clk;
+    // Items in flight: cur (gathered, streams now), nxt (gathered), nxt2
+    // (begun).  Each step's loads get at least one item's streaming time.
+    pr.pending = (int)(blockIdx.x + gridDim.x);
+    pr.pending2 = (int)(blockIdx.x + 2 * gridDim.x);
+    ItemPre cur = pr.begin<kRule>((int)blockIdx.x);
+    ItemPre nxt = pr.begin<kRule>(pr.take());
+    pr.gather(cur);
+    pr.gather(nxt);
+    ItemPre nxt2 = pr.begin<kRule>(pr.take());
+    while (pr.ok && cur.b < P.B) {
+        // a free item slot (the decider frees them)
+        int x = -1;
+        while (pr.ok) {
+            unsigned m = 0;
+#pragma unroll
+            for (int i = 0; i < kItemSlots; ++i)
+                if (*(volatile int *)&sh.slot[i].state == 0) m |= 1u << i;
+            if (m) {
+                x = __ffs(m) - 1;
+                clk.progress();
+                break;
+            }
+            if (!clk.idle()) pr.ok = false;
+        }
+        if (x < 0) break;
+        const ItemPre c = cur;
+        const int ns = pr.finish(c);
+        ItemSlot &sl = sh.slot[x];
+        for (int i = lane; i <= P.K; i += 32) sl.keys[i] = 0ull;
+        if (lane == 0) {
+            sl.b = c.b;
+            sl.rule = c.rule;
+            sl.ns = ns;
+            sl.issued = 0;
+            sl.consumed = 0;
+            sl.miss = 0;
+            __threadfence_block();
+            *(volatile int *)&sl.state = 1;
+        }
+        __syncwarp();
+        // later items' loads go out while this one streams
+        cur = nxt;
+        nxt = nxt2;
+        pr.gather(nxt);
+        nxt2 = pr.begin<kRule>(pr.take());
+        int stages = 0;
+        if (ns != 0 && ns != kNBad) {
+            if (c.rule == kSample) stages = pr.stream_sample(c, ns - 1, x);
+            else stages = pr.stream_greedy(c, x);
+        }
+        if (lane == 0) {
+            sl.issued = stages;
+            __threadfence_block();
+            *(volatile int *)&sl.state = 2;
+        }
+        __syncwarp();
+    }
+    // stop the consumers, then the retire warp
+    if (lane == 0 && pr.ok) {
+        ItemMeta m = {};
+        m.kind = kStop;
+        for (int i = 0; i < kTmaConsumers && pr.ok; ++i)  // one stop per consumer
+            pr.ok = pr.put(m, nullptr, 0, nullptr, 0);
+    }
+    pr.sync_ok();
+    if (!pr.ok && lane == 0) atomicOr(P.status, kStatusTimeout);
+    if (lane == 0) {
+        __threadfence_block();
+        *(volatile int *)&sh.producer_done = pr.ok ? 1 : 2;
+        // the last CTA to stop taking items resets the counter for the next round
+        __threadfence();
+        if (atomicAdd(P.queue + 1, 1u) == gridDim.x - 1) {
+            atomicExch(P.queue, 0u);
+            atomicExch(P.queue + 1, 0u);
+        }
+    }
+    if (!pr.ok && lane == 0) {
+        // a wait gave up: let the copies still in flight land before leaving
+        // (ring position i last held fill i + kStages * r, r = its round)
+        for (int i = 0; i < kStages && i < pr.fills; ++i) {
+            const int r = (pr.fills - 1 - i) / kStages;
+            mbar_wait(&sh.full[i], (uint32_t)r & 1u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumers
+
+__device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf, int lane) {
+    while (true) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&sh.ticket, 1);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        const int k = t % kStages;
+        const float *sp = reinterpret_cast<const float *>(buf + (size_t)k * kStageBytes);
+        const float *sq = reinterpret_cast<const float *>(buf + (size_t)k * kStageBytes + kPartBytes);
+        if (!__all_sync(0xffffffffu, wait_ticket(sh.full, sh.empty, t))) {
+            if (lane == 0) atomicOr(P.status, kStatusTimeout);
+            return;
+        }
+        const ItemMeta m = sh.meta[k];
+        if (m.kind == kStop) return;
+        ItemSlot &sl = sh.slot[m.slot];
+        const int b = sl.b;
+        const int n0 = seg_len(P.V, m.s), c0 = n0 & ~3;
+        const int n1 = m.nparts == 2 ? seg_len(P.V, m.s + 1) : 0, c1 = n1 & ~3;
+        if (m.kind == kPair || m.kind == kMass) {
+            float2 *seg = P.seg + (int64_t)b * P.nseg;
+            float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
+            dd v[kBlocks];
+            if (m.kind == kPair) {
+                const int n = sl.ns - 1;
+                const int64_t off = (int64_t)m.s * kSeg;
+                stage_partials<true>(sp, sq, n0, c0, c0, prow(P, b, n) + off, qrow(P, b, n) + off, lane, v);
+                release_stage(sh.empty, k, lane);
+                store_sums(seg, blk, m.s, v, lane);
+            } else {
+                const float *g = prow(P, b, P.K) + (int64_t)m.s * kSeg;
+                dd v1[kBlocks];
+                stage_partials<false>(sp, nullptr, n0, c0, 0, g, nullptr, lane, v);
+                if (m.nparts == 2)
+                    stage_partials<false>(sq, nullptr, n1, c1, 0, g + kSeg, nullptr, lane, v1);
+                release_stage(sh.empty, k, lane);
+                store_sums(seg, blk, m.s, v, lane);
+                if (m.nparts == 2) store_sums(seg, blk, m.s + 1, v1, lane);
+            }
+        } else {  // kArgmax
+            const float *g = prow(P, b, m.row) + (int64_t)m.s * kSeg;
+            float bv = -__int_as_float(0x7f800000);
+            int32_t bi = -1;
+            stage_argmax(sp, n0, c0, g, (int64_t)m.s * kSeg, lane, bv, bi);
+            if (m.nparts == 2)
+                stage_argmax(sq, n1, c1, g + kSeg, (int64_t)(m.s + 1) * kSeg, lane, bv, bi);
+            release_stage(sh.empty, k, lane);
+            if (m.tok >= 0) {
+                const bool beats = bi >= 0 && (bv > m.pt || (bv == m.pt && bi < m.tok));
+                if (__any_sync(0xffffffffu, beats) && lane == 0) {
+                    atomicMax(&sl.miss, kFlagBase - m.row);
+                    atomicMax(P.miss + b, kFlagBase - m.row);  // other CTAs stop sooner
+                }
+            }
+            const unsigned long long key = warp_max_u64(pack_key(bv, bi));
+            if (lane == 0 && key) atomicMax(&sl.keys[m.row], key);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            // this stage's results before its count; the retire warp's
+            // device-scope fence then publishes them to the deciding CTA
+            __threadfence_block();
+            atomicAdd(&sl.consumed, 1);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// decider
+
+// (n_accepted, next_token) of sequence b, all of whose items are done, then
+// its state cleared for the next round.  A sampling draw stages the row's
+// block sums into `blk_sh` (when they fit) while it loads the segment sums;
+// `dphase` is the parity of the decide warp's staging barrier.
+__device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, float2 *blk_sh,
+                                     uint32_t &dphase, int b, int rule, int ns, int lane) {
+    int n = 0, next = -1;
+    uint32_t st = 0;
+    unsigned long long *best = P.best + (int64_t)b * (P.K + 1);
+    if (rule == kGreedy) {
+        if (ns == kNBad) {
+            st = kStatusBadToken;
+        } else {
+            // the miss flag and every row's key in one round trip
+            const int f = __shfl_sync(0xffffffffu, lane == 0 ? ld_l2(P.miss + b) : 0, 0);
+            const unsigned long long k0 = lane <= P.K ? ld_l2(best + lane) : 0ull;
+            const unsigned long long k1 = lane + 32 <= P.K ? ld_l2(best + lane + 32) : 0ull;
+            const unsigned long long k2 = lane + 64 <= P.K ? ld_l2(best + lane + 64) : 0ull;
+            n = f ? kFlagBase - f : P.K;
+            const unsigned long long mine = n < 32 ? k0 : (n < 64 ? k1 : k2);
+            const unsigned long long key = __shfl_sync(0xffffffffu, mine, n & 31);
+            next = key ? key_index(key) : 0;
+        }
+    } else if (rule == kSample) {
+        if (ns == kNBad) {
+            st = kStatusBadToken;
+        } else {
+            n = ns - 1;
+            const float2 *seg = P.seg + (int64_t)b * P.nseg;
+            const float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
+            DrawInputs in = {};
+            in.u_res = P.u_res + b;
+            if (P.nseg <= kDecideSegs) {
+                const uint32_t bytes = (uint32_t)P.nseg * kBlocks * 8u;
+                if (lane == 0) {
+                    // other CTAs wrote these sums through the generic proxy
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    mbar_arrive_expect_tx(dbar, bytes);
+                    bulk_copy_g2s(blk_sh, blk, bytes, dbar);
+                }
+                in.blk_sh = blk_sh;
+                in.bar = dbar;
+                in.parity = dphase;
+                dphase ^= 1u;
+            }
+            const float *pr = prow(P, b, n < P.K ? n : P.K);
+            if (n < P.K) {
+                next = draw_from_sums<true>(P, seg, blk, pr, qrow(P, b, n), in, lane);
+                if (next == -1) {
+                    // zero residual mass (unnormalised rows): draw from p_n itself
+                    for (int s = 0; s < P.nseg; ++s) segment_sum_store<false>(P, b, pr, nullptr, s, lane);
+                    __threadfence_block();
+                    __syncwarp();
+                    in.blk_sh = nullptr;
+                    next = draw_from_sums<false>(P, seg, blk, pr, nullptr, in, lane);
+                }
+            } else {
+                next = draw_from_sums<false>(P, seg, blk, pr, nullptr, in, lane);
+            }
+            if (next == -2) st = kStatusTimeout;
+            else if (next < 0) st = kStatusZeroMass;
+            if (next < 0) next = -1;
+        }
+    } else {
+        st = kStatusBadMode;
+    }
+    if (lane == 0) {
+        if (st) atomicOr(P.status, st);
+        P.n_out[b] = n;
+        P.next_out[b] = next;
+    }
+    commit_round(P, b, n, next, lane);
+    // every item of b has retired, so nothing else touches its state now
+    if (rule == kGreedy)
+        for (int r = lane; r <= P.K; r += 32) best[r] = 0ull;
+    if (lane == 0) {
+        P.miss[b] = 0;
+        P.done[b] = 0;
+    }
+}
+
+// Lane l holds the item's keys of rows l, l + 32 and l + 64 (0 past row K).
+__device__ bool item_retire(const Params &P, int b, int rule, int ns, int miss,
+                            unsigned long long k0, unsigned long long k1, unsigned long long k2,
+                            int lane) {
+    if (rule == kGreedy && ns == 1) {
+        unsigned long long *best = P.best + (int64_t)b * (P.K + 1);
+        if (k0) atomicMax(best + lane, k0);
+        if (k1) atomicMax(best + lane + 32, k1);
+        if (k2) atomicMax(best + lane + 64, k2);
+        if (lane == 0 && miss) atomicMax(P.miss + b, miss);
+    }
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();  // this item's results before its count
+        last = atomicAdd(P.done + b, 1) == P.ichunks - 1;
+    }
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+__device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
+    IdleClock clk;
+    bool ok = true;
+    while (ok) {
+        bool did = false;
+#pragma unroll
+        for (int i = 0; i < kItemSlots; ++i) {
+            ItemSlot &sl = sh.slot[i];
+            if (*(volatile int *)&sl.state != 2) continue;
+            __threadfence_block();
+            if (*(volatile int *)&sl.consumed < *(volatile int *)&sl.issued) continue;
+            __threadfence_block();
+            const int b = sl.b, rule = sl.rule, ns = sl.ns, miss = sl.miss;
+            const unsigned long long k0 = lane <= P.K ? sl.keys[lane] : 0ull;
+            const unsigned long long k1 = lane + 32 <= P.K ? sl.keys[lane + 32] : 0ull;
+            const unsigned long long k2 = lane + 64 <= P.K ? sl.keys[lane + 64] : 0ull;
+            __syncwarp();
+            if (lane == 0) *(volatile int *)&sl.state = 0;  // the producer may refill it now
+            __syncwarp();
+            did = true;
+            if (!item_retire(P, b, rule, ns, miss, k0, k1, k2, lane)) continue;
+            // queue the sequence for the decide warps (once its entry's previous
+            // occupant has been read)
+            const int h = sh.dq_head;
+            int4 *e = &sh.dq[h % kDecideQueue];
+            IdleClock room;
+            while (*(volatile int *)&e->w != 0) {
+                if (!room.idle()) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) {
+                e->x = b;
+                e->y = rule;
+                e->z = ns;
+                __threadfence_block();
+                *(volatile int *)&e->w = h + 1;
+                *(volatile int *)&sh.dq_head = h + 1;
+            }
+            __syncwarp();
+        }
+        if (!ok) break;
+        if (did) {
+            clk.progress();
+            continue;
+        }
+        const int pd = *(volatile int *)&sh.producer_done;
+        bool busy = false;
+#pragma unroll
+        for (int i = 0; i < kItemSlots; ++i) busy |= *(volatile int *)&sh.slot[i].state != 0;
+        if (pd == 2) break;
+        if (pd && !busy) {
+            if (lane == 0) {
+                __threadfence_block();
+                *(volatile int *)&sh.retire_done = 1;
+            }
+            return;
+        }
+        if (!clk.idle()) ok = false;
+    }
+    if (lane == 0) {
+        atomicOr(P.status, kStatusTimeout);
+        *(volatile int *)&sh.retire_done = 2;
+    }
+}
+
+// A decide warp claims queue entries in turn and decides their sequences; it
+// leaves once the retire warp has left and its claim is past the last entry.
+__device__ void item_decide_loop(const Params &P, ItemShared &sh, unsigned long long *dbar,
+                                 float2 *blk_sh, int lane) {
+    uint32_t dphase = 0;
+    while (true) {
+        int c = 0;
+        if (lane == 0) c = atomicAdd(&sh.dq_claim, 1);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        int4 *e = &sh.dq[c % kDecideQueue];
+        IdleClock clk;
+        bool have = false;
+        while (true) {
+            if (*(volatile int *)&e->w == c + 1) {
+                have = true;
+                break;
+            }
+            const int rd = *(volatile int *)&sh.retire_done;
+            if (rd == 2) return;
+            if (rd == 1) {
+                __threadfence_block();
+                if (c >= *(volatile int *)&sh.dq_head) return;
+                continue;
+            }
+            if (!clk.idle()) {
+                if (lane == 0) atomicOr(P.status, kStatusTimeout);
+                return;
+            }
+        }
+        if (!have) return;
+        __threadfence_block();
+        const int b = e->x, rule = e->y, ns = e->z;
+        __syncwarp();
+        if (lane == 0) *(volatile int *)&e->w = 0;  // the entry may be reused
+        __threadfence();  // the other items' results after their counts
+        item_decide_sequence(P, dbar, blk_sh, dphase, b, rule, ns, lane);
+    }
+}
+
+template <int kRule>
+__global__ void __launch_bounds__(kItemThreads, 2) item_round_kernel(const Params P) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    ItemShared &sh = *reinterpret_cast<ItemShared *>(smem);
+    unsigned char *buf = smem + kItemBufOffset;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.empty[i], 1);
+        }
+        for (int i = 0; i < kItemDecideWarps; ++i) mbar_init(&sh.dbar[i], 1);
+        for (int i = 0; i < kDecideQueue; ++i) sh.dq[i] = make_int4(0, 0, 0, 0);
+        for (int i = 0; i < kItemSlots; ++i) sh.slot[i].state = 0;
+        sh.producer_done = 0;
+        sh.retire_done = 0;
+        sh.dq_head = 0;
+        sh.dq_claim = 0;
+        sh.ticket = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == kItemProducerWarp) item_produce<kRule>(P, sh, buf, lane);
+    else if (warp == kItemRetireWarp) item_retire_loop(P, sh, lane);
+    else if (warp == kItemDecideWarpA || warp == kItemDecideWarpB) {
+        const int d = warp == kItemDecideWarpA ? 0 : 1;
+        item_decide_loop(P, sh, &sh.dbar[d],
+                         reinterpret_cast<float2 *>(smem + kItemHeaderBytes + d * kDecideBytes), lane);
+    }
+    else item_consume(P, sh, buf, lane);
+}
+
+}  // namespace sv

@@ -31,8 +31,6 @@
 
 namespace sv {
 
-constexpr uint32_t kStatusTimeout = 16u;
-
 constexpr int kTmaConsumers = 8;
 constexpr int kProducerWarp = kTmaConsumers;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
@@ -40,7 +38,7 @@ constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 // shared ticket, so a stage's turn-around is copy latency plus the processing
 // time of whichever consumer is free, not of one fixed warp.
 #ifndef SV_STAGES
-#define SV_STAGES 12
+#define SV_STAGES 11
 #endif
 constexpr int kStages = SV_STAGES;
 constexpr int kPartBytes = kSeg * 4;        // one segment of one row
@@ -48,7 +46,6 @@ constexpr int kStageBytes = 2 * kPartBytes;
 constexpr int kChunkSegs = 8;               // segments per chunk
 constexpr int kChunkSlots = 32;             // greedy chunks a CTA tracks until they are consumed
 constexpr int kSlots = 4;                   // greedy chunks a producer keeps open
-constexpr uint64_t kWaitLimitNs = 250000000ull;  // any single wait gives up after 250 ms
 
 enum StageKind : int { kStop = 0, kPair = 1, kMass = 2, kArgmax = 3 };
 
@@ -82,72 +79,6 @@ struct TmaShared {
 constexpr int kTmaBufOffset = 4096;  // stage buffers start here in dynamic shared memory
 static_assert(sizeof(TmaShared) <= kTmaBufOffset, "shared header too large");
 constexpr int kTmaSmemBytes = kTmaBufOffset + kStages * kStageBytes;
-
-// ---------------------------------------------------------------------------
-// mbarrier, bulk-copy and timing primitives (inline PTX)
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
-    asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs of wall-clock time.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    while (true) {
-        uint32_t done;
-        asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-            : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
-                                              unsigned long long *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Idle-wait bookkeeping: idle() returns false once no progress has been made
-// for kWaitLimitNs.
-struct IdleClock {
-    uint64_t since = 0;
-    __device__ void progress() { since = 0; }
-    __device__ bool idle() {
-        const uint64_t now = global_ns();
-        if (since == 0) since = now;
-        if (now - since > kWaitLimitNs) return false;
-        __nanosleep(128);
-        return true;
-    }
-};
 
 // ---------------------------------------------------------------------------
 // producer
@@ -510,6 +441,14 @@ __device__ __forceinline__ bool wait_ticket(unsigned long long *full, unsigned l
     return mbar_wait(&empty[k], phase ^ 1u) && mbar_wait(&full[k], phase);
 }
 
+// Hands ring position k back to the producer once every lane of the warp has
+// read what it needs from it (the values are in registers by then), so the
+// next copy into it overlaps this warp's reduction and stores.
+__device__ __forceinline__ void release_stage(unsigned long long *empty, int k, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[k]);
+}
+
 __device__ void tma_consume(const Params &P, TmaShared &sh, unsigned char *buf, int w, int lane) {
     (void)w;
     while (true) {
@@ -532,21 +471,22 @@ __device__ void tma_consume(const Params &P, TmaShared &sh, unsigned char *buf, 
         if (m.kind == kPair) {
             dd v[kBlocks];
             stage_partials<true>(sp, sq, m.n0, m.c0, m.c1, m.g0, m.g1, lane, v);
+            release_stage(sh.empty, k, lane);
             store_sums(seg, blk, m.s, v, lane);
         } else if (m.kind == kMass) {
-            dd v[kBlocks];
+            dd v[kBlocks], v1[kBlocks];
             stage_partials<false>(sp, nullptr, m.n0, m.c0, 0, m.g0, nullptr, lane, v);
+            if (m.nparts == 2) stage_partials<false>(sq, nullptr, m.n1, m.c1, 0, m.g1, nullptr, lane, v1);
+            release_stage(sh.empty, k, lane);
             store_sums(seg, blk, m.s, v, lane);
-            if (m.nparts == 2) {
-                stage_partials<false>(sq, nullptr, m.n1, m.c1, 0, m.g1, nullptr, lane, v);
-                store_sums(seg, blk, m.s + 1, v, lane);
-            }
+            if (m.nparts == 2) store_sums(seg, blk, m.s + 1, v1, lane);
         } else {  // kArgmax
             float bv = -__int_as_float(0x7f800000);
             int32_t bi = -1;
             stage_argmax(sp, m.n0, m.c0, m.g0, (int64_t)m.s * kSeg, lane, bv, bi);
             if (m.nparts == 2)
                 stage_argmax(sq, m.n1, m.c1, m.g1, (int64_t)(m.s + 1) * kSeg, lane, bv, bi);
+            release_stage(sh.empty, k, lane);
             if (m.tok >= 0) {
                 const bool beats = bi >= 0 && (bv > m.pt || (bv == m.pt && bi < m.tok));
                 if (__any_sync(0xffffffffu, beats) && lane == 0) {
@@ -558,12 +498,9 @@ __device__ void tma_consume(const Params &P, TmaShared &sh, unsigned char *buf, 
             if (lane == 0 && key) atomicMax(P.best + (int64_t)m.b * (P.K + 1) + m.row, key);
         }
         __syncwarp();
-        if (lane == 0) {
-            if (m.cslot >= 0) {
-                __threadfence_block();  // this stage's results before its count
-                atomicAdd(&sh.cs_consumed[m.cslot], 1);
-            }
-            mbar_arrive(&sh.empty[k]);
+        if (lane == 0 && m.cslot >= 0) {
+            __threadfence_block();  // this stage's results before its count
+            atomicAdd(&sh.cs_consumed[m.cslot], 1);
         }
     }
 }

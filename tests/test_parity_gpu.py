@@ -311,6 +311,31 @@ def test_sampling_full_fresh_and_reused_workspace():
         _free()
 
 
+def test_workspace_reused_across_sizes():
+    """One workspace serves calls of several sizes and both launch paths in turn
+    (per-sequence state is laid out by size, so a change of sizes must clear it)."""
+    shapes = [(160, 20000, 5), (170, 30000, 3), (40, 50000, 5), (160, 20000, 5), (200, 9000, 8)]
+    big = max(sv.workspace_size(B, K, V) for B, V, K in shapes)
+    ws = sv.Workspace(1, 1, 1)
+    ws.buf = torch.empty(big, dtype=torch.uint8, device="cuda")
+    ws.nbytes = big
+    assert sv.load().sv_workspace_init(ws.ptr, big, None) == 0
+    for i, (B, V, K) in enumerate(shapes):
+        bt = make_inputs(4, "cuda", seed=900 + i, B=B, V=V, K=K)
+        p, q, t, ua, ur, md = bt.numpy()
+        if i % 2 == 0:
+            n0, x0, s0 = oracle.verify_greedy(p, t, nthreads=8)
+            n1, x1 = sv.verify_greedy(bt.p, bt.t, ws=ws)
+            compare(p, q, ur, 0, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(), s0, ws.status())
+        else:
+            n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
+            n1, x1 = sv.verify_sample(bt.p, bt.q, bt.t, bt.u_acc, bt.u_res, ws=ws)
+            bnd = compare(p, q, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(), s0,
+                          ws.status())
+            if bnd:
+                BOUNDARY_REPORT.append((f"reused workspace {B}x{V}", bnd))
+
+
 def test_mixed_round_full():
     bt = make_inputs(4, "cuda")
     p, q, t, ua, ur, md = bt.numpy()
