@@ -224,19 +224,20 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
         grid = std::min<int64_t>(grid, (int64_t)P.B * P.ichunks);
         P.warps = (int32_t)(grid * sv::kWarps);
         g_last_grid = grid;
+        // a programmatic dependent of whatever precedes it on the stream: its
+        // CTAs may be placed while that grid drains, and wait for it to end
+        // before they touch global memory
         switch (rule) {
             case sv::kGreedy:
-                sv::item_round_kernel<sv::kGreedy><<<(unsigned)grid, sv::kItemThreads, sv::kItemSmemBytes, st>>>(P);
-                break;
+                return launch_dependent(sv::item_round_kernel<sv::kGreedy>, (unsigned)grid,
+                                        sv::kItemThreads, sv::kItemSmemBytes, P, st);
             case sv::kSample:
-                sv::item_round_kernel<sv::kSample><<<(unsigned)grid, sv::kItemThreads, sv::kItemSmemBytes, st>>>(P);
-                break;
+                return launch_dependent(sv::item_round_kernel<sv::kSample>, (unsigned)grid,
+                                        sv::kItemThreads, sv::kItemSmemBytes, P, st);
             default:
-                sv::item_round_kernel<sv::kPerSequence>
-                    <<<(unsigned)grid, sv::kItemThreads, sv::kItemSmemBytes, st>>>(P);
-                break;
+                return launch_dependent(sv::item_round_kernel<sv::kPerSequence>, (unsigned)grid,
+                                        sv::kItemThreads, sv::kItemSmemBytes, P, st);
         }
-        return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
     }
     const bool tma = aligned && tma_occ > 0;
     int64_t grid;

@@ -325,12 +325,17 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// One try: the thread may sleep in it for up to kTrySuspendNs and is woken
+// as soon as the phase completes, so a waiting warp issues a few instructions
+// per wait instead of spinning.
+constexpr uint32_t kTrySuspendNs = 1000000u;
+
 __device__ __forceinline__ bool mbar_try(unsigned long long *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kTrySuspendNs)
         : "memory");
     return done != 0;
 }
@@ -356,16 +361,16 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
-// Idle-wait bookkeeping: idle() returns false once no progress has been made
-// for kWaitLimitNs.
+// Idle-wait bookkeeping for polls of shared state: idle(ns) sleeps about ns
+// and returns false once no progress has been made for kWaitLimitNs.
 struct IdleClock {
     uint64_t since = 0;
     __device__ void progress() { since = 0; }
-    __device__ bool idle() {
+    __device__ bool idle(uint32_t ns = 128) {
         const uint64_t now = global_ns();
         if (since == 0) since = now;
         if (now - since > kWaitLimitNs) return false;
-        __nanosleep(128);
+        __nanosleep(ns);
         return true;
     }
 };
@@ -705,10 +710,15 @@ __device__ __forceinline__ dd split_uniform(double ur) {
 struct DrawInputs {
     dd u;                     // the uniform split into two fp32 parts, unless u_res is set
     const double *u_res;      // else: loaded here once the segment loads are out
-    const float2 *blk_sh;     // block sums staged in shared memory (else read from blk) ...
-    unsigned long long *bar;  // ... by a bulk copy completing on this mbarrier phase
-    uint32_t parity;
+    bool seg_local;           // seg points to shared memory written by this CTA
+    const float2 *blk_sh;     // block sums in shared memory (else read from blk) ...
+    unsigned long long *bar;  // ... staged by a bulk copy completing on this mbarrier phase
+    uint32_t parity;          //     (no wait when bar is null)
 };
+
+__device__ __forceinline__ float2 load_sum(const float2 *p, bool local) {
+    return local ? *p : ld_l2(p);
+}
 
 // Inverse-CDF draw for sequence b over the segment sums seg[0..nseg) and
 // block sums blk of the row pair (pr, qr) (one warp): the token, -1 if the
@@ -726,7 +736,7 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
     for (int r = 0; r < kSegRegs; ++r) {
         v[r] = dd{0.f, 0.f};
         if (r0 + r < r1) {
-            const float2 x = ld_l2(seg + r0 + r);
+            const float2 x = load_sum(seg + r0 + r, in.seg_local);
             v[r] = dd{x.x, x.y};
         }
     }
@@ -735,13 +745,13 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
 #pragma unroll
     for (int r = 0; r < kSegRegs; ++r) own = dd_add(own, v[r]);
     for (int s = r0 + kSegRegs; s < r1; ++s) {  // rows longer than 32 * kSegRegs segments
-        const float2 x = ld_l2(seg + s);
+        const float2 x = load_sum(seg + s, in.seg_local);
         own = dd_add(own, dd{x.x, x.y});
     }
     const dd inc = warp_incl_scan(own, lane);
     const dd total = shfl_dd(inc, 31);
     // the staged copy has to land before this warp returns, whatever the outcome
-    if (in.blk_sh && !__all_sync(0xffffffffu, mbar_wait(in.bar, in.parity))) return -2;
+    if (in.bar && !__all_sync(0xffffffffu, mbar_wait(in.bar, in.parity))) return -2;
     if (total.hi == 0.f) return -1;
     const dd T = threshold(u, total);
     const dd zero = {0.f, 0.f};
@@ -762,7 +772,7 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
                     for (int i = 0; i < kSegRegs; ++i)
                         if (i == r) x = v[i];
                 } else {
-                    const float2 y = ld_l2(seg + s);
+                    const float2 y = load_sum(seg + s, in.seg_local);
                     x = dd{y.x, y.y};
                 }
                 const dd nx = dd_add(acc, x);
@@ -791,7 +801,7 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
         // searched with an infinite threshold (its last element with mass)
         int lastnz = -1;
         for (int s = r0; s < r1; ++s)
-            if (ld_l2(seg + s).x != 0.f) lastnz = s;
+            if (load_sum(seg + s, in.seg_local).x != 0.f) lastnz = s;
 #pragma unroll
         for (int mm = 16; mm > 0; mm >>= 1) lastnz = max(lastnz, __shfl_xor_sync(0xffffffffu, lastnz, mm));
         sg = lastnz;

@@ -63,6 +63,11 @@ constexpr int kItemRetireWarp = 9;
 #endif
 static_assert(kItemThreads == 12 * 32, "role map assumes twelve warps");
 constexpr int kDecideQueue = 16;  // sequences a CTA has completed but not yet decided
+// Poll intervals of the retire and decide warps: they wait on shared state,
+// not on a barrier, and a few hundred ns of delay costs them nothing, while
+// every poll takes issue slots from the producer.
+constexpr uint32_t kRetirePollNs = 256;
+constexpr uint32_t kDecidePollNs = 1024;
 
 struct ItemSlot {
     int state;     // 0 free, 1 streaming, 2 every stage issued (`issued` final)
@@ -72,7 +77,7 @@ struct ItemSlot {
     int issued;
     int consumed;
     int miss;      // greedy: kFlagBase - first missed row seen in this item
-    int pad;
+    int sbuf;      // shared-memory sum buffer holding this item's sums, or -1
     unsigned long long keys[kMaxK + 1];  // greedy: packed (value, index) maximum per row
 };
 
@@ -102,14 +107,22 @@ struct ItemShared {
     int dq_claim;             // entries claimed by the decide warps
     int4 dq[kDecideQueue];    // (b, rule, ns, h + 1 while entry h waits; 0 once read)
     unsigned long long dbar[kItemDecideWarps];  // each decide warp's staging copy
+    int sbuf_busy[kItemDecideWarps];            // sum buffers taken by whole-row items
 };
 
-// Dynamic shared memory: the header, each decide warp's block-sum buffer (rows
-// of up to kDecideSegs segments), the stage ring.
+// Dynamic shared memory: the header, two sum buffers (segment sums, then block
+// sums, of rows of up to kDecideSegs segments), the stage ring.  When an item
+// is a whole row (one item per sequence) its consumers write its sums into a
+// buffer the producer took for it, and the decide reads them there; otherwise
+// buffer d is decide warp d's landing area for the block sums it stages.
 constexpr int kItemHeaderBytes = 4096;
 constexpr int kDecideSegs = 128;
-constexpr int kDecideBytes = kDecideSegs * kBlocks * 8;
-constexpr int kItemBufOffset = kItemHeaderBytes + kItemDecideWarps * kDecideBytes;
+constexpr int kSumSegOffset = 0;
+constexpr int kSumBlkOffset = kDecideSegs * 8;
+constexpr int kSumUOffset = kSumBlkOffset + kDecideSegs * kBlocks * 8;  // the item's u_resample
+constexpr int kSumBufBytes = kSumUOffset + 16;
+
+constexpr int kItemBufOffset = kItemHeaderBytes + kItemDecideWarps * kSumBufBytes;
 static_assert(sizeof(ItemShared) <= kItemHeaderBytes, "shared header too large");
 constexpr int kItemSmemBytes = kItemBufOffset + kStages * kStageBytes;
 
@@ -133,6 +146,12 @@ __device__ __forceinline__ float ld_early(const float *p) {
     return v;
 }
 
+__device__ __forceinline__ double ld_early(const double *p) {
+    double v;
+    asm volatile("ld.global.nc.f64 %0, [%1];" : "=d"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint8_t ld_early(const uint8_t *p) {
     uint16_t v;
     asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
@@ -149,6 +168,7 @@ struct ItemPre {
     int rule;
     int32_t t0, t1;
     float u0, u1, pt0, pt1, qt0, qt1;
+    double ur;  // sampling: u_resample (lane 0)
     bool bad;
 };
 
@@ -228,6 +248,7 @@ struct ItemProducer {
             if (lane < P.K) x.u0 = ld_early(P.u_acc + tb + lane);
             if (lane + 32 < P.K) x.u1 = ld_early(P.u_acc + tb + lane + 32);
         }
+        if (kRule != kGreedy && lane == 0) x.ur = ld_early(P.u_res + b);
         return x;
     }
 
@@ -350,7 +371,8 @@ struct ItemProducer {
 };
 
 template <int kRule>
-__device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf, int lane) {
+__device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf,
+                             unsigned char *sumbufs, int lane) {
     ItemProducer pr(P, sh, buf, lane);
     IdleClock clk;
     // Items in flight: cur (gathered, streams now), nxt (gathered), nxt2
@@ -380,6 +402,21 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
         if (x < 0) break;
         const ItemPre c = cur;
         const int ns = pr.finish(c);
+        // a whole-row sampling item keeps its sums in a shared-memory buffer
+        int sb = -1;
+        if (c.rule == kSample && ns != kNBad && ns != 0 && P.ichunks == 1 && P.nseg <= kDecideSegs) {
+            while (pr.ok) {
+#pragma unroll
+                for (int i = 0; i < kItemDecideWarps && sb < 0; ++i)
+                    if (*(volatile int *)&sh.sbuf_busy[i] == 0) sb = i;
+                if (sb >= 0) {
+                    clk.progress();
+                    break;
+                }
+                if (!clk.idle()) pr.ok = false;
+            }
+            if (sb < 0) break;
+        }
         ItemSlot &sl = sh.slot[x];
         for (int i = lane; i <= P.K; i += 32) sl.keys[i] = 0ull;
         if (lane == 0) {
@@ -389,6 +426,11 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
             sl.issued = 0;
             sl.consumed = 0;
             sl.miss = 0;
+            sl.sbuf = sb;
+            if (sb >= 0) {
+                sh.sbuf_busy[sb] = 1;
+                *reinterpret_cast<double *>(sumbufs + sb * kSumBufBytes + kSumUOffset) = c.ur;
+            }
             __threadfence_block();
             *(volatile int *)&sl.state = 1;
         }
@@ -410,6 +452,9 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
         }
         __syncwarp();
     }
+    // this CTA reads no more rows into its ring: the next grid may start taking
+    // SM slots as they free up (it waits for this grid to end before it reads)
+    grid_dependents_may_launch();
     // stop the consumers, then the retire warp
     if (lane == 0 && pr.ok) {
         ItemMeta m = {};
@@ -442,7 +487,8 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
 // ---------------------------------------------------------------------------
 // consumers
 
-__device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf, int lane) {
+__device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf,
+                             unsigned char *sumbufs, int lane) {
     while (true) {
         int t = 0;
         if (lane == 0) t = atomicAdd(&sh.ticket, 1);
@@ -461,8 +507,11 @@ __device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf
         const int n0 = seg_len(P.V, m.s), c0 = n0 & ~3;
         const int n1 = m.nparts == 2 ? seg_len(P.V, m.s + 1) : 0, c1 = n1 & ~3;
         if (m.kind == kPair || m.kind == kMass) {
-            float2 *seg = P.seg + (int64_t)b * P.nseg;
-            float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
+            const int sb = sl.sbuf;
+            float2 *seg = sb >= 0 ? reinterpret_cast<float2 *>(sumbufs + sb * kSumBufBytes + kSumSegOffset)
+                                  : P.seg + (int64_t)b * P.nseg;
+            float2 *blk = sb >= 0 ? reinterpret_cast<float2 *>(sumbufs + sb * kSumBufBytes + kSumBlkOffset)
+                                  : P.blk + (int64_t)b * P.nseg * kBlocks;
             dd v[kBlocks];
             if (m.kind == kPair) {
                 const int n = sl.ns - 1;
@@ -515,8 +564,9 @@ __device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf
 // its state cleared for the next round.  A sampling draw stages the row's
 // block sums into `blk_sh` (when they fit) while it loads the segment sums;
 // `dphase` is the parity of the decide warp's staging barrier.
-__device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, float2 *blk_sh,
-                                     uint32_t &dphase, int b, int rule, int ns, int lane) {
+__device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, float2 *stage_sh,
+                                     const unsigned char *sums, uint32_t &dphase, int b, int rule,
+                                     int ns, int lane) {
     int n = 0, next = -1;
     uint32_t st = 0;
     unsigned long long *best = P.best + (int64_t)b * (P.K + 1);
@@ -543,15 +593,22 @@ __device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, 
             const float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
             DrawInputs in = {};
             in.u_res = P.u_res + b;
-            if (P.nseg <= kDecideSegs) {
+            if (sums) {
+                // this CTA streamed the whole row: its sums (and u) are in shared memory
+                seg = reinterpret_cast<const float2 *>(sums + kSumSegOffset);
+                in.seg_local = true;
+                in.blk_sh = reinterpret_cast<const float2 *>(sums + kSumBlkOffset);
+                in.u_res = nullptr;
+                in.u = split_uniform(*reinterpret_cast<const double *>(sums + kSumUOffset));
+            } else if (P.nseg <= kDecideSegs) {
                 const uint32_t bytes = (uint32_t)P.nseg * kBlocks * 8u;
                 if (lane == 0) {
                     // other CTAs wrote these sums through the generic proxy
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     mbar_arrive_expect_tx(dbar, bytes);
-                    bulk_copy_g2s(blk_sh, blk, bytes, dbar);
+                    bulk_copy_g2s(stage_sh, blk, bytes, dbar);
                 }
-                in.blk_sh = blk_sh;
+                in.blk_sh = stage_sh;
                 in.bar = dbar;
                 in.parity = dphase;
                 dphase ^= 1u;
@@ -564,8 +621,11 @@ __device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, 
                     for (int s = 0; s < P.nseg; ++s) segment_sum_store<false>(P, b, pr, nullptr, s, lane);
                     __threadfence_block();
                     __syncwarp();
+                    in.seg_local = false;
                     in.blk_sh = nullptr;
-                    next = draw_from_sums<false>(P, seg, blk, pr, nullptr, in, lane);
+                    in.bar = nullptr;
+                    next = draw_from_sums<false>(P, P.seg + (int64_t)b * P.nseg, blk, pr, nullptr, in,
+                                                 lane);
                 }
             } else {
                 next = draw_from_sums<false>(P, seg, blk, pr, nullptr, in, lane);
@@ -624,7 +684,7 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
             __threadfence_block();
             if (*(volatile int *)&sl.consumed < *(volatile int *)&sl.issued) continue;
             __threadfence_block();
-            const int b = sl.b, rule = sl.rule, ns = sl.ns, miss = sl.miss;
+            const int b = sl.b, rule = sl.rule, ns = sl.ns, miss = sl.miss, sb = sl.sbuf;
             const unsigned long long k0 = lane <= P.K ? sl.keys[lane] : 0ull;
             const unsigned long long k1 = lane + 32 <= P.K ? sl.keys[lane + 32] : 0ull;
             const unsigned long long k2 = lane + 64 <= P.K ? sl.keys[lane + 64] : 0ull;
@@ -632,7 +692,8 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
             if (lane == 0) *(volatile int *)&sl.state = 0;  // the producer may refill it now
             __syncwarp();
             did = true;
-            if (!item_retire(P, b, rule, ns, miss, k0, k1, k2, lane)) continue;
+            // a whole-row item with its sums in shared memory is its sequence
+            if (sb < 0 && !item_retire(P, b, rule, ns, miss, k0, k1, k2, lane)) continue;
             // queue the sequence for the decide warps (once its entry's previous
             // occupant has been read)
             const int h = sh.dq_head;
@@ -648,7 +709,7 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
             __syncwarp();
             if (lane == 0) {
                 e->x = b;
-                e->y = rule;
+                e->y = rule | ((sb + 1) << 8);
                 e->z = ns;
                 __threadfence_block();
                 *(volatile int *)&e->w = h + 1;
@@ -673,7 +734,7 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
             }
             return;
         }
-        if (!clk.idle()) ok = false;
+        if (!clk.idle(kRetirePollNs)) ok = false;
     }
     if (lane == 0) {
         atomicOr(P.status, kStatusTimeout);
@@ -684,7 +745,7 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
 // A decide warp claims queue entries in turn and decides their sequences; it
 // leaves once the retire warp has left and its claim is past the last entry.
 __device__ void item_decide_loop(const Params &P, ItemShared &sh, unsigned long long *dbar,
-                                 float2 *blk_sh, int lane) {
+                                 unsigned char *sumbufs, int d, int lane) {
     uint32_t dphase = 0;
     while (true) {
         int c = 0;
@@ -705,18 +766,28 @@ __device__ void item_decide_loop(const Params &P, ItemShared &sh, unsigned long 
                 if (c >= *(volatile int *)&sh.dq_head) return;
                 continue;
             }
-            if (!clk.idle()) {
+            if (!clk.idle(kDecidePollNs)) {
                 if (lane == 0) atomicOr(P.status, kStatusTimeout);
                 return;
             }
         }
         if (!have) return;
         __threadfence_block();
-        const int b = e->x, rule = e->y, ns = e->z;
+        const int b = e->x, rule = e->y & 0xff, sb = (e->y >> 8) - 1, ns = e->z;
         __syncwarp();
         if (lane == 0) *(volatile int *)&e->w = 0;  // the entry may be reused
-        __threadfence();  // the other items' results after their counts
-        item_decide_sequence(P, dbar, blk_sh, dphase, b, rule, ns, lane);
+        if (sb < 0) __threadfence();  // the other items' results after their counts
+        item_decide_sequence(P, dbar,
+                             reinterpret_cast<float2 *>(sumbufs + d * kSumBufBytes + kSumBlkOffset),
+                             sb >= 0 ? sumbufs + sb * kSumBufBytes : nullptr, dphase, b, rule, ns,
+                             lane);
+        if (sb >= 0) {
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                *(volatile int *)&sh.sbuf_busy[sb] = 0;  // the producer may reuse the buffer
+            }
+        }
     }
 }
 
@@ -731,7 +802,10 @@ __global__ void __launch_bounds__(kItemThreads, 2) item_round_kernel(const Param
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.empty[i], 1);
         }
-        for (int i = 0; i < kItemDecideWarps; ++i) mbar_init(&sh.dbar[i], 1);
+        for (int i = 0; i < kItemDecideWarps; ++i) {
+            mbar_init(&sh.dbar[i], 1);
+            sh.sbuf_busy[i] = 0;
+        }
         for (int i = 0; i < kDecideQueue; ++i) sh.dq[i] = make_int4(0, 0, 0, 0);
         for (int i = 0; i < kItemSlots; ++i) sh.slot[i].state = 0;
         sh.producer_done = 0;
@@ -742,14 +816,16 @@ __global__ void __launch_bounds__(kItemThreads, 2) item_round_kernel(const Param
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (warp == kItemProducerWarp) item_produce<kRule>(P, sh, buf, lane);
+    // launched as a programmatic dependent: the set-up above may overlap the
+    // previous grid; nothing in global memory is touched before it is done
+    wait_for_primary_grid();
+    if (warp == kItemProducerWarp) item_produce<kRule>(P, sh, buf, smem + kItemHeaderBytes, lane);
     else if (warp == kItemRetireWarp) item_retire_loop(P, sh, lane);
     else if (warp == kItemDecideWarpA || warp == kItemDecideWarpB) {
         const int d = warp == kItemDecideWarpA ? 0 : 1;
-        item_decide_loop(P, sh, &sh.dbar[d],
-                         reinterpret_cast<float2 *>(smem + kItemHeaderBytes + d * kDecideBytes), lane);
+        item_decide_loop(P, sh, &sh.dbar[d], smem + kItemHeaderBytes, d, lane);
     }
-    else item_consume(P, sh, buf, lane);
+    else item_consume(P, sh, buf, smem + kItemHeaderBytes, lane);
 }
 
 }  // namespace sv
