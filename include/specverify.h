@@ -17,10 +17,15 @@
  * These entry points batch that operation over B independent sequences.
  *
  * Common conventions
- *   Memory.  Every pointer argument is DEVICE memory on the current device,
- *     owned by the caller, and must stay valid until the stream reaches the
- *     end of the call.  Inputs are read-only; outputs must not alias inputs.
- *     The library allocates no memory.
+ *   Memory.  Every array argument is device memory of the current device or
+ *     page-locked host memory (cudaHostAlloc / cudaHostRegister), owned by
+ *     the caller, and must stay valid until the stream reaches the end of the
+ *     call; pageable host memory is rejected with SV_EINVAL.  When p or q is
+ *     in host memory the kernels read it where it is, over the host link, and
+ *     only the rows the rule needs cross it (the plain-load path is used).
+ *     The workspace must be device memory (else SV_EWORKSPACE).  Inputs are
+ *     read-only; outputs must not alias inputs.  The library allocates no
+ *     memory.
  *   Layout.  p holds B*(K+1) rows of V f32 target probabilities; row (b, i),
  *     i in [0, K], starts at p + (b*(K+1) + i) * p_row_stride.  q holds B*K
  *     rows of draft probabilities; row (b, i), i in [0, K), starts at
@@ -39,7 +44,8 @@
  *     call leaves it ready for the next one.  One workspace serves one call at
  *     a time: calls that share a workspace must be ordered on one stream.
  *   Return codes.  SV_OK, or a negative SV_E* code for errors detected on the
- *     host before anything is enqueued (SV_EINVAL: a null pointer, B < 0,
+ *     host before anything is enqueued (SV_EINVAL: a null pointer or an array
+ *     in pageable host memory, B < 0,
  *     K < 0 or K > SV_MAX_K, V < 1 or V > 2^31-1, a stride < V, max_len < 1;
  *     SV_EWORKSPACE: workspace null, misaligned or too small; SV_ECUDA: the
  *     launch failed).  B = 0 is a no-op.
@@ -175,14 +181,17 @@ int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride,
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags);
 
 /* Launch shape used by the calls above.  The kernels are persistent: their
- * grid holds ctas_per_sm CTAs of 256 threads per SM (0, the default, uses the
- * largest count the SMs can hold at once), and each warp works through
- * 1024-element segments of the batch.  The setting is process-wide and meant
+ * grid holds ctas_per_sm CTAs per SM (0, the default, uses the largest count
+ * the SMs can hold at once).  The setting is process-wide and meant
  * for tuning sweeps. */
 int sv_set_ctas_per_sm(int32_t ctas_per_sm);
 
 /* Number of CTAs the last call on this thread launched (its grid size). */
 int64_t sv_last_grid_size(void);
+
+/* Number of kernels the last verification call on this thread enqueued: 1 for
+ * the single-launch path, 3 for the scan / stream / decide chain. */
+int32_t sv_last_kernel_count(void);
 
 /* Text for an SV_* return code or SV_STATUS_* bit. */
 const char *sv_status_string(int code);

@@ -40,6 +40,7 @@ MAX_K = 64
 EXPORTED = (
     "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
     "sv_verify_round", "sv_get_status", "sv_set_ctas_per_sm", "sv_last_grid_size",
+    "sv_last_kernel_count",
     "sv_status_string", "sv_version", "sv_verify_sample_noalloc",
 )
 
@@ -86,6 +87,8 @@ def load():
         lib.sv_set_ctas_per_sm.restype = ctypes.c_int
         lib.sv_last_grid_size.argtypes = []
         lib.sv_last_grid_size.restype = i64
+        lib.sv_last_kernel_count.argtypes = []
+        lib.sv_last_kernel_count.restype = i32
         lib.sv_status_string.argtypes = [ctypes.c_int]
         lib.sv_status_string.restype = ctypes.c_char_p
         lib.sv_version.argtypes = []
@@ -116,6 +119,11 @@ def set_ctas_per_sm(n: int):
 
 def last_grid_size() -> int:
     return int(load().sv_last_grid_size())
+
+
+def last_kernel_count() -> int:
+    """Kernels the last verification call on this thread enqueued."""
+    return int(load().sv_last_kernel_count())
 
 
 def _torch():
@@ -174,11 +182,23 @@ def _workspace(ws, B, K, V, device):
     return w
 
 
+def _device_of(x):
+    """The CUDA device a call on x runs on: x's own, or the current one for a
+    pinned CPU tensor."""
+    torch = _torch()
+    return x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
+def _usable(x) -> bool:
+    """A CUDA tensor, or a CPU tensor in page-locked memory (read in place)."""
+    return x.is_cuda or x.is_pinned()
+
+
 def _rows3(x, rows, name, dtype):
     """(tensor viewed as [B][rows][V], B, V, row stride) with the library's layout."""
     torch = _torch()
-    if not isinstance(x, torch.Tensor) or not x.is_cuda:
-        raise SpecVerifyError(f"{name} must be a CUDA tensor")
+    if not isinstance(x, torch.Tensor) or not _usable(x):
+        raise SpecVerifyError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
     if x.dtype != dtype:
         raise SpecVerifyError(f"{name} must be {dtype}, got {x.dtype}")
     if x.dim() == 2:
@@ -200,8 +220,8 @@ def _vec(x, n, name, dtype, device):
     torch = _torch()
     if x is None:
         return None
-    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.device != device:
-        raise SpecVerifyError(f"{name} must be a CUDA tensor on {device}")
+    if not isinstance(x, torch.Tensor) or not (x.is_pinned() or (x.is_cuda and x.device == device)):
+        raise SpecVerifyError(f"{name} must be a CUDA tensor on {device} or a pinned CPU tensor")
     if x.dtype != dtype:
         raise SpecVerifyError(f"{name} must be {dtype}, got {x.dtype}")
     if not x.is_contiguous() or x.numel() != n:
@@ -230,7 +250,7 @@ def verify_greedy(p, t, *, ws=None, n_out=None, next_out=None, stream=None):
     torch = _torch()
     K = t.shape[-1]
     p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
-    dev = p.device
+    dev = _device_of(p)
     t = _vec(t, B * K, "t", torch.int32, dev)
     n_out, next_out = _outputs(B, dev, n_out, next_out)
     w = _workspace(ws, B, K, V, dev)
@@ -246,7 +266,7 @@ def verify_sample(p, q, t, u_acc, u_res, *, ws=None, n_out=None, next_out=None, 
     torch = _torch()
     K = t.shape[-1]
     p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
-    dev = p.device
+    dev = _device_of(p)
     q, Bq, Vq, qs = _rows3(q, K, "q", torch.float32) if K > 0 else (None, B, V, V)
     if (Bq, Vq) != (B, V):
         raise SpecVerifyError("q does not match p")
@@ -273,7 +293,7 @@ def verify_sample_noalloc(p, q, t, u_acc, u_res, *, n_out=None, next_out=None, s
     torch = _torch()
     K = t.shape[-1]
     p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
-    dev = p.device
+    dev = _device_of(p)
     q, Bq, Vq, qs = _rows3(q, K, "q", torch.float32) if K > 0 else (None, B, V, V)
     if (Bq, Vq) != (B, V):
         raise SpecVerifyError("q does not match p")
@@ -296,7 +316,7 @@ def verify_round(mode, p, q, t, u_acc, u_res, *, tokens=None, lengths=None, ws=N
     torch = _torch()
     K = t.shape[-1]
     p, B, V, ps = _rows3(p, K + 1, "p", torch.float32)
-    dev = p.device
+    dev = _device_of(p)
     q, Bq, Vq, qs = _rows3(q, K, "q", torch.float32) if K > 0 else (None, B, V, V)
     if (Bq, Vq) != (B, V):
         raise SpecVerifyError("q does not match p")
@@ -321,48 +341,79 @@ def verify_round(mode, p, q, t, u_acc, u_res, *, tokens=None, lengths=None, ws=N
 
 
 class HostVerifier:
-    """Verification of host-resident inputs: each call copies the inputs from
-    (pinned) host tensors into device buffers, runs the kernels and copies
-    (n_accepted, next_token) back, on one stream, and waits for the result."""
+    """Verification of host-resident inputs through the public calls.  Inputs
+    are pinned CPU tensors; (n_accepted, next_token) come back in pinned
+    memory and each call waits for them.
 
-    def __init__(self, B: int, K: int, V: int, device=None, sampling: bool = True):
+    mapped=True (default): the inputs are handed to the library where they
+    are; the kernels read them over the host link, and only the rows the rule
+    needs (the residual pair or bonus row of a sampling sequence, the rows up
+    to the first miss of a greedy one) cross it.  mapped=False: every call
+    first copies all inputs into device buffers."""
+
+    def __init__(self, B: int, K: int, V: int, device=None, sampling: bool = True,
+                 mapped: bool = True):
         torch = _torch()
         dev = torch.device("cuda") if device is None else torch.device(device)
-        self.B, self.K, self.V, self.device = B, K, V, dev
-        self.p = torch.empty(B, K + 1, V, dtype=torch.float32, device=dev)
-        self.q = torch.empty(B, K, V, dtype=torch.float32, device=dev) if sampling else None
-        self.t = torch.empty(B, K, dtype=torch.int32, device=dev)
-        self.u_acc = torch.empty(B, K, dtype=torch.float32, device=dev)
-        self.u_res = torch.empty(B, dtype=torch.float64, device=dev)
+        self.B, self.K, self.V, self.device, self.mapped = B, K, V, dev, mapped
+        self.sampling = sampling
+        if not mapped:
+            self.p = torch.empty(B, K + 1, V, dtype=torch.float32, device=dev)
+            self.q = torch.empty(B, K, V, dtype=torch.float32, device=dev) if sampling else None
+            self.t = torch.empty(B, K, dtype=torch.int32, device=dev)
+            self.u_acc = torch.empty(B, K, dtype=torch.float32, device=dev)
+            self.u_res = torch.empty(B, dtype=torch.float64, device=dev)
         self.n = torch.empty(B, dtype=torch.int32, device=dev)
         self.next = torch.empty(B, dtype=torch.int32, device=dev)
         self.n_host = torch.empty(B, dtype=torch.int32, pin_memory=True)
         self.next_host = torch.empty(B, dtype=torch.int32, pin_memory=True)
         self.ws = Workspace(B, K, V, dev)
 
-    def h2d_bytes(self, sampling=True) -> int:
-        n = self.p.numel() * 4 + self.t.numel() * 4
-        if sampling:
-            n += self.q.numel() * 4 + self.u_acc.numel() * 4 + self.u_res.numel() * 8
-        return n
+    def h2d_bytes(self) -> int:
+        """Bytes of input that crossed the host link in the last call: all of
+        them when copying, else what the rule read (from its n_accepted)."""
+        B, K, V = self.B, self.K, self.V
+        if not self.mapped:
+            n = (K + 1) * V * 4 * B + K * 4 * B
+            if self.sampling:
+                n += K * V * 4 * B + K * 4 * B + 8 * B
+            return n
+        total = 0
+        for n in self.n_host.tolist():
+            if self.sampling:
+                rows = 8 * V if n < K else 4 * V
+                total += rows + 64 * min(n + 1, K) + 8 * K + 8
+            else:
+                total += (n + 1) * 4 * V + 4 * K + 4 * min(n + 1, K)
+        return total
 
     def d2h_bytes(self) -> int:
         return self.B * 8
 
+    def _pinned(self, *xs):
+        for x in xs:
+            if x is not None and not x.is_pinned():
+                raise SpecVerifyError("HostVerifier inputs must be pinned CPU tensors")
+
     def sample(self, p, q, t, u_acc, u_res):
-        self.p.copy_(p, non_blocking=True)
-        self.q.copy_(q, non_blocking=True)
-        self.t.copy_(t, non_blocking=True)
-        self.u_acc.copy_(u_acc, non_blocking=True)
-        self.u_res.copy_(u_res, non_blocking=True)
-        verify_sample(self.p, self.q, self.t, self.u_acc, self.u_res, ws=self.ws,
-                      n_out=self.n, next_out=self.next)
+        self._pinned(p, q, t, u_acc, u_res)
+        if not self.mapped:
+            self.p.copy_(p, non_blocking=True)
+            self.q.copy_(q, non_blocking=True)
+            self.t.copy_(t, non_blocking=True)
+            self.u_acc.copy_(u_acc, non_blocking=True)
+            self.u_res.copy_(u_res, non_blocking=True)
+            p, q, t, u_acc, u_res = self.p, self.q, self.t, self.u_acc, self.u_res
+        verify_sample(p, q, t, u_acc, u_res, ws=self.ws, n_out=self.n, next_out=self.next)
         return self._finish()
 
     def greedy(self, p, t):
-        self.p.copy_(p, non_blocking=True)
-        self.t.copy_(t, non_blocking=True)
-        verify_greedy(self.p, self.t, ws=self.ws, n_out=self.n, next_out=self.next)
+        self._pinned(p, t)
+        if not self.mapped:
+            self.p.copy_(p, non_blocking=True)
+            self.t.copy_(t, non_blocking=True)
+            p, t = self.p, self.t
+        verify_greedy(p, t, ws=self.ws, n_out=self.n, next_out=self.next)
         return self._finish()
 
     def _finish(self):

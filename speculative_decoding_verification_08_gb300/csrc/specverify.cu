@@ -82,6 +82,7 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
 
 std::atomic<int32_t> g_ctas_per_sm{0};
 thread_local int64_t g_last_grid = 0;
+thread_local int32_t g_last_kernels = 0;
 
 struct DeviceInfo {
     int sms = 0;
@@ -215,7 +216,8 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
     P.ichunks = (int32_t)((nseg + P.isegs - 1) / P.isegs);
     int sms = 0, occ = 0, tma_occ = 0, item_occ = 0;
     if (!device_info(rule, &sms, &occ, &tma_occ, &item_occ)) return SV_ECUDA;
-    const bool aligned = aligned_rows(P.p, P.ps) &&
+    // bulk copies read device memory only: rows on the host take the plain loads
+    const bool aligned = !P.rows_on_host && aligned_rows(P.p, P.ps) &&
                          (rule == sv::kGreedy || P.K == 0 || aligned_rows(P.q, P.qs));
     const int32_t forced = g_ctas_per_sm.load();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -224,6 +226,7 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
         grid = std::min<int64_t>(grid, (int64_t)P.B * P.ichunks);
         P.warps = (int32_t)(grid * sv::kWarps);
         g_last_grid = grid;
+        g_last_kernels = 1;
         // a programmatic dependent of whatever precedes it on the stream: its
         // CTAs may be placed while that grid drains, and wait for it to end
         // before they touch global memory
@@ -251,6 +254,7 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
     }
     P.warps = (int32_t)(grid * sv::kWarps);
     g_last_grid = grid;
+    g_last_kernels = 3;
     switch (rule) {
         case sv::kGreedy: return launch_round<sv::kGreedy>(P, tma, (unsigned)grid, st);
         case sv::kSample: return launch_round<sv::kSample>(P, tma, (unsigned)grid, st);
@@ -293,8 +297,45 @@ int prepare_state(const sv::Params &P, void *ws, cudaStream_t st) {
     return SV_OK;
 }
 
+// Where a pointer lives, as the runtime knows it: device (or managed) memory,
+// page-locked host memory the GPU reads over the host link, or neither
+// (pageable host memory, which the kernels must not be given).
+enum Residence { kOnDevice = 0, kOnHost = 1, kUnusable = 2 };
+
+template <class T>
+Residence place(T *&ptr) {
+    if (!ptr) return kOnDevice;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return kUnusable;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return kOnDevice;
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return kUnusable;
+    // the address the device uses for this page-locked block
+    const char *base = static_cast<const char *>(a.hostPointer);
+    const ptrdiff_t off = reinterpret_cast<const char *>(ptr) - base;
+    ptr = reinterpret_cast<T *>(static_cast<char *>(a.devicePointer) + off);
+    return kOnHost;
+}
+
+// Checks where every caller array lives and rewrites host addresses to their
+// device-side aliases.  Rows in page-locked host memory select the plain-load
+// path (the kernels then read only the rows the rule needs over the link).
+int place_arrays(sv::Params &P) {
+    Residence r[10] = {place(P.p),       place(P.q),        place(P.t),      place(P.u_acc),
+                       place(P.u_res),   place(P.mode),     place(P.n_out),  place(P.next_out),
+                       place(P.tokens),  place(P.lengths)};
+    for (Residence x : r)
+        if (x == kUnusable) return SV_EINVAL;
+    P.rows_on_host = (r[0] == kOnHost || r[1] == kOnHost) ? 1 : 0;
+    return SV_OK;
+}
+
 int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return SV_EWORKSPACE;
+    void *w = ws;
+    if (place(w) != kOnDevice) return SV_EWORKSPACE;  // atomics and counters live here
     const Layout L = layout(P.B, P.K, P.V);
     if (bytes < L.total) return SV_EWORKSPACE;
     char *base = static_cast<char *>(ws);
@@ -366,6 +407,7 @@ int sv_verify_greedy(const float *p, int64_t p_row_stride, const int32_t *t, int
     sv::Params P = make_params(p, p_row_stride, nullptr, 0, t, nullptr, nullptr, nullptr, B, K, V,
                                n_accepted, next_token);
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kGreedy, P, stream);
 }
@@ -381,6 +423,7 @@ int sv_verify_sample(const float *p, int64_t p_row_stride, const float *q, int64
     sv::Params P = make_params(p, p_row_stride, q, q_row_stride, t, u_accept, u_resample, nullptr,
                                B, K, V, n_accepted, next_token);
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kSample, P, stream);
 }
@@ -401,6 +444,7 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride, c
     P.lengths = lengths;
     P.max_len = max_len;
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kPerSequence, P, stream);
 }
@@ -424,6 +468,8 @@ int sv_set_ctas_per_sm(int32_t ctas_per_sm) {
 }
 
 int64_t sv_last_grid_size(void) { return g_last_grid; }
+
+int32_t sv_last_kernel_count(void) { return g_last_kernels; }
 
 const char *sv_status_string(int code) {
     switch (code) {
@@ -499,5 +545,6 @@ extern "C" int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride, co
     sv::Params P = make_params(p, p_row_stride, q, q_row_stride, t, u_accept, u_resample,
                                nullptr, B, K, V, n_accepted, next_token);
     if ((rc = bind_workspace(P, scratch, SV_NOALLOC_SCRATCH_BYTES)) != SV_OK) return rc;
+    if ((rc = place_arrays(P)) != SV_OK) return rc;
     return launch(sv::kSample, P, stream);
 }

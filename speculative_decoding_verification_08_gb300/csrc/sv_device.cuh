@@ -98,6 +98,7 @@ struct Params {
     int32_t *lengths;
     int32_t max_len;
     int32_t nchunks;            // bulk-copy path: chunks of the batch
+    int32_t rows_on_host;       // host side: p or q is page-locked host memory
     int32_t ichunks;            // item kernel: items (chunks) per sequence
     int32_t isegs;              // item kernel: segments per item
     // workspace

@@ -1,6 +1,8 @@
 """CUDA path against the CPU oracle, element by element, on the same seeded
 inputs: greedy outputs and accept decisions bit-exact, drawn tokens exact up
 to counted boundary cases (oracle/compare.py).  Needs a GPU (-m gpu)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -334,6 +336,48 @@ def test_workspace_reused_across_sizes():
                           ws.status())
             if bnd:
                 BOUNDARY_REPORT.append((f"reused workspace {B}x{V}", bnd))
+
+
+@pytest.mark.parametrize("mapped", [True, False])
+def test_host_resident_inputs(mapped):
+    """Inputs in pinned host memory, read in place (mapped) or copied first:
+    the same outputs as the oracle, through the public HostVerifier."""
+    B, V, K = 160, 20000, 5
+    bt = make_inputs(3, "cuda", seed=1700, B=B, V=V, K=K)
+    p, q, t, ua, ur, md = bt.numpy()
+    hp, hq = bt.p.cpu().pin_memory(), bt.q.cpu().pin_memory()
+    ht, hua, hur = bt.t.cpu().pin_memory(), bt.u_acc.cpu().pin_memory(), bt.u_res.cpu().pin_memory()
+    hv = sv.HostVerifier(B, K, V, sampling=True, mapped=mapped)
+    n1, x1 = hv.sample(hp, hq, ht, hua, hur)
+    n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
+    bnd = compare(p, q, ur, 1, K, n0, x0, n1.numpy().copy(), x1.numpy().copy(), s0,
+                  hv.ws.status())
+    if bnd:
+        BOUNDARY_REPORT.append((f"host inputs mapped={mapped}", bnd))
+    assert hv.h2d_bytes() > 0
+    hg = sv.HostVerifier(B, K, V, sampling=False, mapped=mapped)
+    n1, x1 = hg.greedy(hp, ht)
+    n0, x0, s0 = oracle.verify_greedy(p, t, nthreads=8)
+    compare(p, q, ur, 0, K, n0, x0, n1.numpy().copy(), x1.numpy().copy(), s0, hg.ws.status())
+    if mapped:
+        assert sv.last_kernel_count() == 3  # host rows take the plain-load chain
+
+
+def test_pageable_host_memory_rejected():
+    """A pageable CPU array is refused on the host, before anything runs."""
+    B, V, K = 4, 1000, 2
+    lib = sv.load()
+    p = torch.rand(B, K + 1, V)            # pageable
+    t = torch.zeros(B, K, dtype=torch.int32, device="cuda")
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    nx = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = sv.Workspace(B, K, V)
+    rc = lib.sv_verify_greedy(ctypes.c_void_p(p.data_ptr()), V, ctypes.c_void_p(t.data_ptr()),
+                              B, K, V, ctypes.c_void_p(n.data_ptr()),
+                              ctypes.c_void_p(nx.data_ptr()), ws.ptr, ws.nbytes, None)
+    assert rc == sv.SV_EINVAL
+    with pytest.raises(sv.SpecVerifyError):
+        sv.verify_greedy(p, t)
 
 
 def test_mixed_round_full():
