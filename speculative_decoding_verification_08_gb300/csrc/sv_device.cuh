@@ -1,46 +1,45 @@
 // sv_device.cuh -- device code of the batched speculative-decoding
-// verification kernels (sm_103a).
+// verification kernels (sm_103a): the arithmetic and helpers every path
+// shares, and the plain-load path.
 //
-// One round is two launches on one stream.
+// A row of V probabilities is cut into 1024-element segments, each made of
+// eight 128-element blocks.  Three launch paths give identical outputs:
+//  * sv_item.cuh: one persistent launch over (sequence, chunk) items, rows
+//    moved into shared memory by bulk copies (16-byte aligned device rows and
+//    at least one sequence per SM);
+//  * sv_tma.cuh with this file: scan -> bulk-copy stream over chunks of
+//    segments -> decide (aligned device rows, smaller batches);
+//  * this file: scan -> plain-load stream -> decide (any alignment, and rows
+//    in page-locked host memory).
+// In the three-launch chain the scan kernel caches per-sequence data (the
+// first rejection n of a sampling sequence; the draft tokens and p_i(t_i) of
+// a greedy one), the stream kernel's warps take the batch's segments in turn
+// and leave partials in the workspace, and the decide kernel, a programmatic
+// dependent, turns them into (n_accepted, next_token).
 //
-// 1. The stream kernel.  A row of V probabilities is cut into 1024-element
-//    segments; the unit of work ("item") is one segment of one sequence,
-//    items are numbered sequence-major, and the launch is persistent: its
-//    grid is sized to what the SMs hold at once and warp w of W takes items
-//    w, w + W, w + 2W, ...  Warps work independently, stream their segment
-//    with 16-byte non-coherent loads and leave a partial result in the
-//    workspace.  Nothing on this path waits or fences: partials are plain
-//    stores or relaxed atomics.
-// 2. The decide kernel, one warp per sequence, launched as a programmatic
-//    dependent of the first (it starts when the stream kernel's CTAs retire
-//    and waits in griddepcontrol.wait until all their writes are visible).
-//    It reads the partials and writes (n_accepted, next_token).
-//
-//  * Greedy rule ("spec-verify" page, section "Method", greedy bullet): the
-//    warp owning segment s of sequence b walks rows 0, 1, ... of that segment,
-//    keeping the largest value and its lowest index.  When a lane has seen an
+//  * Greedy rule ("spec-verify" page, section "Method", greedy bullet): a
+//    segment of row i is reduced to its largest value and lowest index.  An
 //    element that beats the draft token t_i (larger, or equal at a lower
-//    index) the warp records "row i missed" in a per-sequence flag (atomicMax
-//    of an encoding that favours smaller rows).  Every row's loads are issued
-//    together with a read of that flag, and the walk stops after the first row
-//    known to have missed, so rows past the first miss are not streamed.  Each
-//    row's segment maximum goes into a per-row 64-bit key with atomicMax.
-//    Only comparisons are involved, so the result is exact in any order.
-//  * Sampling rule (same section, sampling bullet): the first rejection n is
-//    found by a lane-parallel gather of p_i(t_i), q_i(t_i) and the exact fp64
-//    test u*q < p, then cached per sequence.  The warp streams its segment of
-//    the residual max(0, p_n - q_n), or of p_K when all K were accepted, and
-//    stores its double-fp32 sum.  The decide kernel scans the segment sums,
-//    finds the segment where the running mass first exceeds
-//    T = u_resample * total, and re-reads only that segment to locate the token.
+//    index) records "row i missed" in a per-sequence flag (atomicMax of an
+//    encoding that favours smaller rows); streaming stops after the first row
+//    known to have missed.  Row maxima go into per-row 64-bit keys with
+//    atomicMax.  Only comparisons are involved, so the result is exact in any
+//    order.
+//  * Sampling rule (same section, sampling bullet): the first rejection n
+//    comes from a lane-parallel gather of p_i(t_i), q_i(t_i) and the exact
+//    fp64 test u*q < p.  The residual max(0, p_n - q_n), or p_K when all K
+//    were accepted, is streamed once and leaves a double-fp32 sum per segment
+//    and per block.  The draw finds the segment where the running mass first
+//    exceeds T = u_resample * total, then the block within it, then re-reads
+//    that one block to locate the token.
 //
 // Mass sums use error-free transformations in fp32 instead of fp64 (fp64
-// throughput on this part is a small fraction of fp32): each element
-// p - q with p > q >= 0 is split exactly into hi + lo (Dekker's FastTwoSum on
-// p and -q), each lane accumulates its 32 elements per segment with the
-// Ogita-Rump-Oishi "Sum2" cascade (Knuth's TwoSum), and partials are combined
-// with double-fp32 addition (Dekker).  The relative error of every prefix is
-// below about 1e-11 for these non-negative terms.
+// throughput on this part is a small fraction of fp32).  Each residual
+// max(0, p - q) is exact as hi + lo: FastTwoSum(max(p, q), -q) (Dekker), with
+// max(p, q) >= q >= 0.  Four consecutive masses are added with a packed
+// fp32x2 TwoSum tree that keeps every rounding error; lanes' block partials
+// are combined with double-fp32 addition.  The relative error of any prefix
+// is below about 1e-11 for these non-negative terms.
 #pragma once
 
 #include <cuda_runtime.h>

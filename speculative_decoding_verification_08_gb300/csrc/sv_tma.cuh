@@ -1,5 +1,7 @@
 // sv_tma.cuh -- the streaming stage of a verification round as a bulk-copy
-// pipeline (sm_103a), used whenever every row starts on a 16-byte boundary.
+// pipeline (sm_103a), used for 16-byte-aligned device rows when the batch has
+// fewer sequences than SMs (larger batches run sv_item.cuh's single launch);
+// the ring primitives here serve both.
 //
 // A persistent CTA has one producer warp and eight consumer warps.  The
 // producer takes chunks (kChunkSegs consecutive 1024-element segments of one
