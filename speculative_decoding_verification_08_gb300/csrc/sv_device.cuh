@@ -156,9 +156,10 @@ __device__ __forceinline__ dd shfl_up_dd(dd x, int d) {
 }
 
 // Inclusive warp scan in lane order.
+template <int kWidth = 32>  // scans lanes [0, kWidth) (lanes past it get partial sums)
 __device__ __forceinline__ dd warp_incl_scan(dd v, int lane) {
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
+    for (int d = 1; d < kWidth; d <<= 1) {
         dd o = shfl_up_dd(v, d);
         if (lane >= d) v = dd_add(o, v);
     }
@@ -701,6 +702,18 @@ __device__ __forceinline__ int first_crossing(dd v, dd prefix, dd T, int lane, d
     return crossing_of_scan(v, warp_incl_scan(v, lane), prefix, T, lane, before);
 }
 
+// The same over the eight block sums of a segment, held by lanes 0..7.
+__device__ __forceinline__ int first_crossing8(dd v, dd prefix, dd T, int lane, dd &before) {
+    return crossing_of_scan(v, warp_incl_scan<kBlocks>(v, lane), prefix, T, lane, before);
+}
+
+// Asks the memory system to bring [p, p + bytes) into L2 (no destination, no
+// completion): a later load of it then waits on L2, not on DRAM.  p and bytes
+// are multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ dd split_uniform(double ur) {
     const float uh = __double2float_rn(ur);
     return {uh, __double2float_rn(__dsub_rn(ur, (double)uh))};
@@ -714,6 +727,8 @@ struct DrawInputs {
     const float2 *blk_sh;     // block sums in shared memory (else read from blk) ...
     unsigned long long *bar;  // ... staged by a bulk copy completing on this mbarrier phase
     uint32_t parity;          //     (no wait when bar is null)
+    bool prefetch;            // rows are 16-byte-aligned device memory: once the segment
+                              // is known, ask L2 for it while the block is searched
 };
 
 __device__ __forceinline__ float2 load_sum(const float2 *p, bool local) {
@@ -741,9 +756,9 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
         }
     }
     const dd u = in.u_res ? split_uniform(__ldg(in.u_res)) : in.u;
-    dd own = {0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < kSegRegs; ++r) own = dd_add(own, v[r]);
+    static_assert(kSegRegs == 8, "the lane total below is a tree over eight sums");
+    dd own = dd_add(dd_add(dd_add(v[0], v[1]), dd_add(v[2], v[3])),
+                    dd_add(dd_add(v[4], v[5]), dd_add(v[6], v[7])));
     for (int s = r0 + kSegRegs; s < r1; ++s) {  // rows longer than 32 * kSegRegs segments
         const float2 x = load_sum(seg + s, in.seg_local);
         own = dd_add(own, dd{x.x, x.y});
@@ -807,6 +822,11 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
         sg = lastnz;
         Tt = dd{__int_as_float(0x7f800000), 0.f};
     }
+    if (in.prefetch && lane < 2) {
+        const int c = min(kSeg, (int)(P.V - (int64_t)sg * kSeg)) & ~3;
+        const float *row = lane == 0 ? pr : qr;
+        if (c && row) prefetch_l2(row + (int64_t)sg * kSeg, 4u * (uint32_t)c);
+    }
     // block within the segment
     dd bv = zero;
     if (lane < kBlocks) {
@@ -815,7 +835,7 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
         bv = dd{x.x, x.y};
     }
     dd bbefore;
-    int bk = first_crossing(bv, sbefore, Tt, lane, bbefore);
+    int bk = first_crossing8(bv, sbefore, Tt, lane, bbefore);
     if (bk < 0) {
         // block sums and the segment sum disagree in the last bits: the last
         // block with mass, with an infinite threshold

@@ -67,7 +67,7 @@ constexpr int kDecideQueue = 16;  // sequences a CTA has completed but not yet d
 // not on a barrier, and a few hundred ns of delay costs them nothing, while
 // every poll takes issue slots from the producer.
 constexpr uint32_t kRetirePollNs = 256;
-constexpr uint32_t kDecidePollNs = 1024;
+constexpr uint32_t kDecidePollNs = 256;
 
 struct ItemSlot {
     int state;     // 0 free, 1 streaming, 2 every stage issued (`issued` final)
@@ -593,6 +593,7 @@ __device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, 
             const float2 *blk = P.blk + (int64_t)b * P.nseg * kBlocks;
             DrawInputs in = {};
             in.u_res = P.u_res + b;
+            in.prefetch = true;  // this kernel runs on aligned device rows only
             if (sums) {
                 // this CTA streamed the whole row: its sums (and u) are in shared memory
                 seg = reinterpret_cast<const float2 *>(sums + kSumSegOffset);
