@@ -27,7 +27,7 @@
 //    order.
 //  * Sampling rule (same section, sampling bullet): the first rejection n
 //    comes from a lane-parallel gather of p_i(t_i), q_i(t_i) and the exact
-//    fp64 test u*q < p.  The residual max(0, p_n - q_n), or p_K when all K
+//    test u*q < p (`accepts`).  The residual max(0, p_n - q_n), or p_K when all K
 //    were accepted, is streamed once and leaves a double-fp32 sum per segment
 //    and per block.  The draw finds the segment where the running mass first
 //    exceeds T = u_resample * total, then the block within it, then re-reads
@@ -526,7 +526,19 @@ __device__ void greedy_item(const Params &P, int b, int s, int lane) {
 
 // First rejection of sequence b as n + 1 (n = K when all K are accepted), or
 // kNBad when a draft id is outside [0, V): a lane-parallel gather of
-// p_i(t_i), q_i(t_i) and the exact fp64 accept test for every position.
+// p_i(t_i), q_i(t_i) and the exact accept test for every position.
+// The accept test u * q < p, decided exactly (the product of two fp32 values
+// is exact in fp64, which is how the test is defined).  fmaf(-u, q, p) rounds
+// p - u*q once, and a rounding never changes the sign of a nonzero value, so
+// a nonzero result decides alone; only a zero result -- p equal to the exact
+// product, or a difference below half the smallest subnormal -- needs the
+// fp64 comparison, whose pipe is slow on this part.
+__device__ __forceinline__ bool accepts(float u, float q, float p) {
+    const float r = __fmaf_rn(-u, q, p);
+    if (r != 0.f) return r > 0.f;
+    return __dmul_rn((double)u, (double)q) < (double)p;
+}
+
 __device__ int32_t first_rejection(const Params &P, int b, int lane) {
     int n = P.K;
     bool bad = false;
@@ -541,8 +553,7 @@ __device__ int32_t first_rejection(const Params &P, int b, int lane) {
                 const float pt = __ldg(prow(P, b, i) + x);
                 const float qt = __ldg(qrow(P, b, i) + x);
                 const float u = __ldg(P.u_acc + (int64_t)b * P.K + i);
-                // exact: the fp64 product of two fp32 values is exact
-                rej = !(__dmul_rn((double)u, (double)qt) < (double)pt);
+                rej = !accepts(u, qt, pt);
             }
         }
         const unsigned m = __ballot_sync(0xffffffffu, rej);

@@ -9,7 +9,7 @@
 // Each CTA runs three roles:
 //  * a producer warp takes the next item, finds what the item needs one item
 //    ahead of use (sampling: the first rejection n from gathered p_i(t_i),
-//    q_i(t_i) and the exact fp64 accept test; greedy: the draft tokens and
+//    q_i(t_i) and the exact accept test; greedy: the draft tokens and
 //    p_i(t_i)), and streams the item's row segments into a ring of
 //    shared-memory stages with cp.async.bulk;
 //  * eight consumer warps reduce the stages -- the double-fp32 segment and
@@ -266,14 +266,14 @@ struct ItemProducer {
         }
     }
 
-    // n + 1 for sampling (exact fp64 accept test), 1 for greedy, kNBad for
+    // n + 1 for sampling (exact accept test), 1 for greedy, kNBad for
     // invalid draft ids, 0 for an invalid mode.
     __device__ int finish(const ItemPre &x) {
         if (x.rule != kSample && x.rule != kGreedy) return 0;
         if (x.bad) return kNBad;
         if (x.rule == kGreedy) return 1;
-        const bool r0 = lane < P.K && !(__dmul_rn((double)x.u0, (double)x.qt0) < (double)x.pt0);
-        const bool r1 = lane + 32 < P.K && !(__dmul_rn((double)x.u1, (double)x.qt1) < (double)x.pt1);
+        const bool r0 = lane < P.K && !accepts(x.u0, x.qt0, x.pt0);
+        const bool r1 = lane + 32 < P.K && !accepts(x.u1, x.qt1, x.pt1);
         const unsigned m0 = __ballot_sync(0xffffffffu, r0);
         const unsigned m1 = __ballot_sync(0xffffffffu, r1);
         const int n = m0 ? __ffs(m0) - 1 : (m1 ? 32 + __ffs(m1) - 1 : P.K);

@@ -230,6 +230,39 @@ def test_commit_matches_oracle():
         assert np.array_equal(lens.cpu().numpy(), len_ref)
 
 
+def test_accept_test_edges_are_exact():
+    """u*q against p at the edges of fp32: exact equality of the product, one
+    ulp either side, and magnitudes whose difference underflows.  n must match
+    the oracle's exact fp64 test bit for bit."""
+    rng = np.random.default_rng(17)
+    cases = []
+    for _ in range(200):   # p exactly equal to the fp32 product u*q, and one ulp either side
+        u = np.float32(rng.integers(1, 1 << 24) / (1 << 24))
+        q = np.float32(rng.uniform(1e-6, 1e-2))
+        prod = np.float32(u * q)
+        for p in (prod, np.nextafter(prod, np.float32(1)), np.nextafter(prod, np.float32(0))):
+            cases.append((u, q, p))
+    for e in (-100, -120, -126, -130, -140, -149):   # tiny magnitudes, products far below p's ulp
+        tiny = np.float32(2.0 ** e)
+        for u in (np.float32(0.5), np.float32(0.75), np.float32(1 - 2 ** -24)):
+            for q in (tiny, np.float32(2 * tiny), np.float32(2.0 ** -60)):
+                for p in (tiny, np.float32(0.0), np.nextafter(np.float32(u * q), np.float32(1))):
+                    cases.append((u, q, p))
+    B, K, V = len(cases), 1, 8
+    p = np.full((B, K + 1, V), 1e-3, dtype=np.float32)
+    q = np.full((B, K, V), 1e-3, dtype=np.float32)
+    t = np.zeros((B, K), dtype=np.int32)
+    ua = np.zeros((B, K), dtype=np.float32)
+    for b, (u, qt, pt) in enumerate(cases):
+        p[b, 0, 0], q[b, 0, 0], ua[b, 0] = pt, qt, u
+    ur = np.full(B, 0.5)
+    n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    n1, x1 = sv.verify_sample(dev(p), dev(q), dev(t), dev(ua), dev(torch.from_numpy(ur).numpy()))
+    assert np.array_equal(n0, n1.cpu().numpy())
+    assert (n0 == 0).any() and (n0 == 1).any()
+
+
 def test_boundary_thresholds_are_counted_not_wrong():
     """Uniforms placed exactly on the oracle's CDF boundaries: the GPU may pick
     either neighbour, and every difference must be boundary-explained."""
