@@ -93,6 +93,8 @@ class Oracle:
                                          P, P, P, i32]
         lib.orc_verify_round.restype = i32
         lib.orc_commit.argtypes = [P, i32, i32, P, P, P, P, i32, P]
+        lib.orc_alpha.argtypes = [P, i64, P, i64, i32, i32, i64, P, P]
+        lib.orc_alpha.restype = None
         lib.orc_commit.restype = None
         self.lib = lib
         self.path = path
@@ -172,6 +174,22 @@ class Oracle:
             raise MemoryError("oracle: out of host memory")
         return n, nxt, int(st[0])
 
+    def alpha(self, p, q, K=None):
+        """p [B][K+1][V], q [B][K][V] -> (alpha [B][K] f64, expected accepted
+        length [B] f64)."""
+        q = _f32(q)
+        if q.ndim == 2:
+            q = q[None]
+        K = q.shape[1] if K is None else K
+        p, B, V, ps = _rows(p, K + 1, "p")
+        q, Bq, Vq, qs = _rows(q, K, "q")
+        if (Bq, Vq) != (B, V):
+            raise ValueError("q shape does not match p")
+        a = np.empty((B, K), dtype=np.float64)
+        e = np.empty(B, dtype=np.float64)
+        self.lib.orc_alpha(_ptr(p), ps, _ptr(q), qs, B, K, V, _ptr(a), _ptr(e))
+        return a, e
+
     def commit(self, t, n, nxt, tokens, lengths):
         """Appends t[b][:n[b]] and next[b] to tokens[b] in place; returns status bits."""
         t = np.ascontiguousarray(t, dtype=np.int32)
@@ -227,3 +245,7 @@ def verify_round(mode, p, q, t, u_acc, u_res, nthreads=1):
 
 def commit(t, n, nxt, tokens, lengths):
     return get().commit(t, n, nxt, tokens, lengths)
+
+
+def alpha(p, q, K=None):
+    return get().alpha(p, q, K)

@@ -358,3 +358,44 @@ void orc_commit(const int32_t *t, int B, int K, const int32_t *n_acc,
         lengths[b] = len + n + 1;
     }
 }
+
+/* Per-position acceptance rate of the sampling rule, the quantity behind the
+ * page's analytic accepted-length law ("spec-verify" page, section
+ * "Measured"; the law itself is the rejection-sampling theorem of Leviathan
+ * et al. / Chen et al.).  For each sequence b and draft position i < K:
+ *     alpha[b][i] = sum_v min(p_i(v) / P_i, q_i(v) / Q_i),
+ * P_i and Q_i the fp64 row totals (rows need not be normalised; a row with
+ * zero total gives alpha = 0), and, when expected != NULL,
+ *     expected[b] = sum_{m=1..K} prod_{j<m} alpha[b][j],
+ * the mean number of accepted draft tokens of a round.  Sums run in fp64 in
+ * ascending v. */
+void orc_alpha(const float *p, int64_t p_stride, const float *q,
+               int64_t q_stride, int B, int K, int64_t V, double *alpha,
+               double *expected)
+{
+    for (int b = 0; b < B; ++b) {
+        double mean = 0.0, reach = 1.0;
+        for (int i = 0; i < K; ++i) {
+            const float *pr = p + ((int64_t)b * (K + 1) + i) * p_stride;
+            const float *qr = q + ((int64_t)b * K + i) * q_stride;
+            double P = 0.0, Q = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                P += (double)pr[v];
+                Q += (double)qr[v];
+            }
+            double a = 0.0;
+            if (P > 0.0 && Q > 0.0) {
+                for (int64_t v = 0; v < V; ++v) {
+                    const double x = (double)pr[v] / P;
+                    const double y = (double)qr[v] / Q;
+                    a += x < y ? x : y;
+                }
+            }
+            alpha[(int64_t)b * K + i] = a;
+            reach *= a;    /* P(n > i) = prod_{j <= i} alpha_j */
+            mean += reach;
+        }
+        if (expected)
+            expected[b] = mean;
+    }
+}

@@ -363,6 +363,79 @@ def pin_analytic_length_law(orc, rounds=1200, V=2048):
     return float(n.mean()), float(mean.mean()), float(alpha.mean())
 
 
+def pin_alpha(orc):
+    """Per-position acceptance rate alpha = sum min(p_hat, q_hat) and the
+    expected accepted length sum_m prod_{j<m} alpha_j, pinned to:
+    the identity alpha = 1 - TV(p_hat, q_hat) (a different formula, with
+    |.| instead of min); exact rationals on small integer rows; closed forms
+    (identical rows, disjoint supports, one-hot p, zero rows, power-of-two
+    scaling); and the mean accepted length of the oracle's own sampler over
+    many rounds (the law, not the formula)."""
+    rng = np.random.default_rng(8080)
+    # identity with total variation, unnormalised rows of assorted scales
+    B, K, V = 6, 3, 700
+    p = (rng.random((B, K + 1, V)) ** 3 * rng.uniform(0.2, 5, (B, K + 1, 1))).astype(np.float32)
+    q = (rng.random((B, K, V)) ** 3 * rng.uniform(0.2, 5, (B, K, 1))).astype(np.float32)
+    a, e = orc.alpha(p, q)
+    ph = p[:, :K].astype(np.float64) / p[:, :K].astype(np.float64).sum(-1, keepdims=True)
+    qh = q.astype(np.float64) / q.astype(np.float64).sum(-1, keepdims=True)
+    tv = 0.5 * np.abs(ph - qh).sum(-1)
+    assert np.allclose(a, 1.0 - tv, atol=1e-12, rtol=0), (a, 1 - tv)
+    assert ((0 <= a) & (a <= 1 + 1e-12)).all()
+    # exact rationals
+    pi = rng.integers(0, 9, (2, 3, 5))
+    qi = rng.integers(0, 9, (2, 2, 5))
+    pi[:, :, 0] += 1
+    qi[:, :, 0] += 1
+    a, e = orc.alpha(pi.astype(np.float32), qi.astype(np.float32))
+    for b in range(2):
+        exp_len, reach = Fr(0), Fr(1)
+        for i in range(2):
+            P, Q = int(pi[b, i].sum()), int(qi[b, i].sum())
+            ex = sum(min(Fr(int(x), P), Fr(int(y), Q)) for x, y in zip(pi[b, i], qi[b, i]))
+            assert abs(a[b, i] - float(ex)) < 1e-15, (a[b, i], ex)
+            reach *= ex
+            exp_len += reach
+        assert abs(e[b] - float(exp_len)) < 1e-14, (e[b], exp_len)
+    # closed forms: position 0 identical after scaling, 1 disjoint supports,
+    # 2 one-hot p, 3 an all-zero p row; row 4 is the (unused) bonus row
+    V = 64
+    base = rng.random(V).astype(np.float32) + 0.01
+    low = (np.arange(V) < 32).astype(np.float32)
+    p = np.stack([base * 4, base * (1 - low), np.eye(V, dtype=np.float32)[7] * 3,
+                  np.zeros(V, np.float32), base])
+    q = np.stack([base * 0.25, base * low, base, base])
+    a, e = orc.alpha(p[None], q[None])
+    assert abs(a[0, 0] - 1.0) < V * 2.0 ** -52, a
+    assert a[0, 1] == 0.0 and a[0, 3] == 0.0, a
+    assert abs(a[0, 2] - float(base[7]) / float(base.astype(np.float64).sum())) < 1e-15, a
+    assert e[0] == a[0, 0], e                                    # 1 + 0 + 0 + 0 terms after a_0
+    s1, e1 = orc.alpha(p[None] * np.float32(2.0 ** 5), q[None] * np.float32(2.0 ** -7))
+    assert np.array_equal(s1, a) and np.array_equal(e1, e)       # scaling invariance, exact
+    # the law, through the sampler: rows fixed, drafts and uniforms fresh each round
+    R, K, V = 4000, 3, 40
+    prow = _softmax(rng.normal(0, 1.5, (K + 1, V))).astype(np.float32)
+    qrow = _softmax(rng.normal(0, 1.5, (K, V)) + 0.4 * rng.normal(0, 1, (K, V))).astype(np.float32)
+    a, e = orc.alpha(prow[None], qrow[None])
+    pp = np.broadcast_to(prow, (R, K + 1, V)).copy()
+    qq = np.broadcast_to(qrow, (R, K, V)).copy()
+    qn = qrow.astype(np.float64) / qrow.astype(np.float64).sum(-1, keepdims=True)
+    t = np.stack([rng.choice(V, size=R, p=qn[i]) for i in range(K)], 1).astype(np.int32)
+    ua = rng.random((R, K)).astype(np.float32)
+    ur = rng.random(R)
+    n, _, st = orc.verify_sample(pp, qq, t, ua, ur, nthreads=4)
+    assert st == 0
+    probs, pre = [], 1.0
+    for m in range(K):
+        probs.append(pre * (1 - a[0, m]))
+        pre *= a[0, m]
+    probs.append(pre)
+    probs = np.array(probs)
+    var = (probs * np.arange(K + 1) ** 2).sum() - e[0] ** 2
+    z = (n.mean() - e[0]) / math.sqrt(var / R)
+    assert abs(z) < 4.0, f"sampler mean {n.mean():.4f} vs expected length {e[0]:.4f} (z={z:.2f})"
+
+
 def pin_special_cases(orc):
     """q == p accepts everything; one-hot targets and single-token residuals are
     deterministic; power-of-two scaling changes nothing."""
@@ -511,4 +584,5 @@ PINS = [
     pin_round_and_commit,
     pin_threads_agree,
     pin_analytic_length_law,
+    pin_alpha,
 ]

@@ -52,6 +52,10 @@ MUTANTS = [
     ("token_range_off_by_one", "(int64_t)t[i] >= V", "(int64_t)t[i] > V", 1),
     ("round_modes_swapped", "if (m == 0) {", "if (m == 1 && 0) {", 1),
     ("commit_next_misplaced", "row[len + n] = next[b];", "row[len + n - 1] = next[b];", 1),
+    ("alpha_max_not_min", "a += x < y ? x : y;", "a += x > y ? x : y;", 1),
+    ("alpha_unnormalised_q", "const double y = (double)qr[v] / Q;", "const double y = (double)qr[v];", 1),
+    ("alpha_expected_off_by_one", "reach *= a;    /* P(n > i) = prod_{j <= i} alpha_j */\n            mean += reach;",
+     "mean += reach;\n            reach *= a;", 1),
     ("threads_drop_tail", "j->b1 = (int)((int64_t)B * (k + 1) / nthreads);",
      "j->b1 = (int)((int64_t)B * (k + 1) / nthreads) - (k == nthreads - 1 && k > 0);", 1),
 ]
