@@ -46,7 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--mode", choices=["sample", "greedy", "round"], default=None)
+    ap.add_argument("--mode", choices=["sample", "greedy", "round", "alpha"], default=None,
+                    help="alpha: the acceptance-rate diagnostic instead of a verification round")
     ap.add_argument("--sets", type=int, default=4, help="input sets rotated through")
     ap.add_argument("--graph", action="store_true", help="replay the steps from a CUDA graph")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="persistent grid residency (0 = max)")
@@ -118,6 +119,13 @@ def required_bytes(mode_arr, n_arr, K: int, V: int) -> int:
             rows = 8 * V if n < K else 4 * V
             total += 64 * tested + rows + 4 * K + 4 * K + 8 + 8
     return total
+
+
+def alpha_bytes(B: int, K: int, V: int) -> int:
+    """The acceptance-rate diagnostic reads rows p_0..p_{K-1} and q_0..q_{K-1}
+    of every sequence in full, twice (totals, then the min-sum), and writes
+    B*K + B doubles."""
+    return 2 * 8 * V * B * K + 8 * (B * K + B)
 
 
 def dense_bytes(mode_arr, K: int, V: int) -> int:
@@ -262,6 +270,8 @@ def time_oracle(host, mode: str, K: int, seconds: float, nthreads: int, max_roun
             oracle.verify_greedy(p, t, nthreads=nthreads)
         elif mode == "sample":
             oracle.verify_sample(p, q, t, ua, ur, nthreads=nthreads)
+        elif mode == "alpha":
+            oracle.alpha(p, q)   # single-threaded
         else:
             oracle.verify_round(md, p, q, t, ua, ur, nthreads=nthreads)
         rounds += 1
@@ -354,8 +364,16 @@ def main(argv=None):
 
     # precomputed C-ABI argument lists: the timed loop is one C call per step
     calls = []
+    keep = []
     for bt, (n, nx) in zip(sets, outs):
-        if args.mode == "greedy":
+        if args.mode == "alpha":
+            a_out = torch.empty(B, K, dtype=torch.float64, device=dev)
+            e_out = torch.empty(B, dtype=torch.float64, device=dev)
+            keep.append((a_out, e_out))
+            calls.append((lib.sv_alpha,
+                          (P(bt.p), V, P(bt.q), V, B, K, V, P(a_out), P(e_out), ws.ptr, ws.nbytes,
+                           sh)))
+        elif args.mode == "greedy":
             calls.append((lib.sv_verify_greedy,
                           (P(bt.p), V, P(bt.t), B, K, V, P(n), P(nx), ws.ptr, ws.nbytes, sh)))
         elif args.mode == "sample":
@@ -382,13 +400,15 @@ def main(argv=None):
 
     # algorithmic bytes per launch, from each set's n_accepted
     req, dense, nhist = [], [], np.zeros(K + 1, dtype=np.int64)
-    for bt, (n, _) in zip(sets, outs):
+    for bt, (n, _) in zip(sets if args.mode != "alpha" else [], outs):
         md = bt.mode.cpu().numpy() if args.mode == "round" else np.full(
             B, 0 if args.mode == "greedy" else 1)
         nn = n.cpu().numpy()
         nhist += np.bincount(nn, minlength=K + 1)[:K + 1]
         req.append(required_bytes(md, nn, K, V))
         dense.append(dense_bytes(md, K, V))
+    if args.mode == "alpha":
+        req = dense = [alpha_bytes(B, K, V)]
     req_per_launch = float(np.mean(req))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
@@ -468,9 +488,10 @@ def main(argv=None):
         host = sets[0].numpy()
         ncpu = os.cpu_count() or 1
         rps, nb, rounds, el = time_oracle(host, args.mode, K, args.cpu_seconds, ncpu)
-        cpu = {"value": rps, "unit": UNIT, "cores": ncpu, "kind": "oracle",
+        used = 1 if args.mode == "alpha" else ncpu   # the alpha oracle is single-threaded
+        cpu = {"value": rps, "unit": UNIT, "cores": used, "kind": "oracle",
                "sample": f"{rounds} full rounds ({nb} sequences each) of input set 0, "
-                         f"{el:.1f} s on {ncpu} threads"}
+                         f"{el:.1f} s on {used} thread{'s' if used > 1 else ''}"}
 
     if rank == 0:
         clk = clocks.summary(t_wall0, t_wall1) if clocks else None

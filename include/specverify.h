@@ -186,11 +186,29 @@ int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags);
  * for tuning sweeps. */
 int sv_set_ctas_per_sm(int32_t ctas_per_sm);
 
+/* Acceptance-rate diagnostic: for each sequence b and draft position i < K,
+ *   alpha[b][i] = sum_v min(p_i(v) / P_i, q_i(v) / Q_i),
+ * P_i, Q_i the totals of rows p (b, i) and q (b, i) (a row with zero total
+ * gives alpha = 0), and, when expected_length is not NULL,
+ *   expected_length[b] = sum_{m=1..K} prod_{j<m} alpha[b][j],
+ * the mean number of accepted draft tokens of a sampling round: the
+ * rejection-sampling theorem behind the "spec-verify" page's analytic
+ * accepted-length law (section "Measured").  Not part of a verification
+ * round: it reads every row p_0..p_{K-1} and q_0..q_{K-1} in full, twice.
+ * Layout and memory rules as above; alpha is [B][K] f64, expected_length [B]
+ * f64.  |alpha - exact| <= 2 * 2^-24 * alpha (fp32 scaling of each term,
+ * double-fp32 sums).  Uses the workspace of sv_workspace_size(B, K, V); any
+ * call may use a workspace between verification calls. */
+int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row_stride,
+             int32_t B, int32_t K, int64_t V, double *alpha, double *expected_length,
+             void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
 /* Number of CTAs the last call on this thread launched (its grid size). */
 int64_t sv_last_grid_size(void);
 
-/* Number of kernels the last verification call on this thread enqueued: 1 for
- * the single-launch path, 3 for the scan / stream / decide chain. */
+/* Number of kernels the last call on this thread enqueued: 1 for the
+ * single-launch verification path, 3 for the scan / stream / decide chain,
+ * up to 3 for sv_alpha. */
 int32_t sv_last_kernel_count(void);
 
 /* Text for an SV_* return code or SV_STATUS_* bit. */

@@ -40,7 +40,7 @@ MAX_K = 64
 EXPORTED = (
     "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
     "sv_verify_round", "sv_get_status", "sv_set_ctas_per_sm", "sv_last_grid_size",
-    "sv_last_kernel_count",
+    "sv_last_kernel_count", "sv_alpha",
     "sv_status_string", "sv_version", "sv_verify_sample_noalloc",
 )
 
@@ -89,6 +89,8 @@ def load():
         lib.sv_last_grid_size.restype = i64
         lib.sv_last_kernel_count.argtypes = []
         lib.sv_last_kernel_count.restype = i32
+        lib.sv_alpha.argtypes = [P, i64, P, i64, i32, i32, i64, P, P, P, sz, P]
+        lib.sv_alpha.restype = ctypes.c_int
         lib.sv_status_string.argtypes = [ctypes.c_int]
         lib.sv_status_string.restype = ctypes.c_char_p
         lib.sv_version.argtypes = []
@@ -306,6 +308,30 @@ def verify_sample_noalloc(p, q, t, u_acc, u_res, *, n_out=None, next_out=None, s
                                          _stream_handle(stream))
     _check(rc, "sv_verify_sample_noalloc")
     return n_out, next_out
+
+
+def alpha(p, q, *, ws=None, alpha_out=None, expected_out=None, stream=None):
+    """Acceptance-rate diagnostic: p [B][K+1][V], q [B][K][V] f32 ->
+    (alpha [B][K] f64, expected accepted length [B] f64), with
+    alpha[b][i] = sum_v min(p_i / P_i, q_i / Q_i) over row totals P_i, Q_i."""
+    torch = _torch()
+    q3, B, V, qs = _rows3(q, q.shape[-2] if q.dim() >= 2 else 1, "q", torch.float32)
+    K = q3.shape[1]
+    p, Bp, Vp, ps = _rows3(p, K + 1, "p", torch.float32)
+    if (Bp, Vp) != (B, V):
+        raise SpecVerifyError("q shape does not match p")
+    dev = _device_of(p)
+    if alpha_out is None:
+        alpha_out = torch.empty(B, K, dtype=torch.float64, device=dev)
+    if expected_out is None:
+        expected_out = torch.empty(B, dtype=torch.float64, device=dev)
+    _vec(alpha_out.reshape(-1), B * K, "alpha_out", torch.float64, dev)
+    _vec(expected_out, B, "expected_out", torch.float64, dev)
+    w = _workspace(ws, B, K, V, dev)
+    _check(load().sv_alpha(_ptr(p), ps, _ptr(q3), qs, B, K, V, _ptr(alpha_out),
+                           _ptr(expected_out), w.ptr, w.nbytes, _stream_handle(stream)),
+           "sv_alpha")
+    return alpha_out, expected_out
 
 
 def verify_round(mode, p, q, t, u_acc, u_res, *, tokens=None, lengths=None, ws=None,

@@ -12,6 +12,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "sv_alpha.cuh"
 #include "sv_device.cuh"
 #include "sv_item.cuh"
 #include "specverify.h"
@@ -48,10 +49,11 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
 
 // Workspace layout:
 // [status, queue, exit | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] |
-//  seg[B][nseg] | blk[B][nseg][8] | udd[B]], every region 256-byte aligned;
-// everything before seg must start at zero (and every call leaves it so).
+//  seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2]], every region
+// 256-byte aligned; everything before seg must start at zero (and every call
+// leaves it so).
 struct Layout {
-    size_t status, queue, miss, nstate, done, ptok, best, seg, blk, udd, total;
+    size_t status, queue, miss, nstate, done, ptok, best, seg, blk, udd, norm, total;
 };
 
 Layout layout(int32_t B, int32_t K, int64_t V) {
@@ -76,6 +78,8 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     off += round_up((size_t)B * (size_t)num_segments(V) * sv::kBlocks * sizeof(float2));
     L.udd = off;
     off += round_up((size_t)B * sizeof(float2));
+    L.norm = off;
+    off += round_up((size_t)B * (size_t)K * 2 * sizeof(float2));
     L.total = off;
     return L;
 }
@@ -162,9 +166,9 @@ bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *item_occ) {
 // Launches kernel on stream st as a programmatic dependent of the previous
 // launch: it may be scheduled while that grid's CTAs retire and waits on the
 // device (griddepcontrol.wait) before it reads their results.
-template <class Kernel>
+template <class Kernel, class Args>
 int launch_dependent(Kernel kernel, unsigned grid, unsigned threads, size_t smem,
-                     const sv::Params &P, cudaStream_t st) {
+                     const Args &P, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(threads);
@@ -447,6 +451,58 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride, c
     if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kPerSequence, P, stream);
+}
+
+int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row_stride,
+             int32_t B, int32_t K, int64_t V, double *alpha, double *expected_length,
+             void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+    if (!sizes_ok(B, K, V)) return SV_EINVAL;
+    if (B == 0) return SV_OK;
+    if (!p || p_row_stride < V) return SV_EINVAL;
+    if (K > 0 && (!q || q_row_stride < V || !alpha)) return SV_EINVAL;
+    if ((int64_t)B * K > INT32_MAX) return SV_EINVAL;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return SV_EWORKSPACE;
+    const Layout L = layout(B, K, V);
+    if (workspace_bytes < L.total) return SV_EWORKSPACE;
+    void *w = workspace;
+    if (place(w) != kOnDevice) return SV_EWORKSPACE;
+    sv::AlphaParams A{};
+    A.p = p;
+    A.ps = p_row_stride;
+    A.q = q;
+    A.qs = q_row_stride;
+    A.B = B;
+    A.K = K;
+    A.V = V;
+    A.nseg = (int32_t)num_segments(V);
+    A.alpha = alpha;
+    A.expected = expected_length;
+    if (place(A.p) == kUnusable || place(A.q) == kUnusable || place(A.alpha) == kUnusable ||
+        place(A.expected) == kUnusable)
+        return SV_EINVAL;
+    A.norm = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + L.norm);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    g_last_grid = (int64_t)B * K;
+    g_last_kernels = 0;
+    if (K > 0) {
+        sv::alpha_norm_kernel<<<(unsigned)(B * K), sv::kAlphaThreads, 0, st>>>(A);
+        if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
+        int rc = launch_dependent(sv::alpha_min_kernel, (unsigned)(B * K), sv::kAlphaThreads, 0, A, st);
+        if (rc != SV_OK) return rc;
+        g_last_kernels = 2;
+    }
+    if (A.expected) {
+        if (K == 0) {
+            if (cudaMemsetAsync(A.expected, 0, (size_t)B * sizeof(double), st) != cudaSuccess)
+                return SV_ECUDA;
+        } else {
+            int rc = launch_dependent(sv::alpha_length_kernel, (unsigned)((B + 255) / 256), 256u, 0,
+                                      A, st);
+            if (rc != SV_OK) return rc;
+            g_last_kernels = 3;
+        }
+    }
+    return SV_OK;
 }
 
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags) {
