@@ -95,6 +95,11 @@ class Oracle:
         lib.orc_commit.argtypes = [P, i32, i32, P, P, P, P, i32, P]
         lib.orc_alpha.argtypes = [P, i64, P, i64, i32, i32, i64, P, P]
         lib.orc_alpha.restype = None
+        lib.orc_softmax.argtypes = [P, i64, ctypes.c_double, P]
+        lib.orc_softmax.restype = None
+        lib.orc_verify_sample_logits.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64,
+                                                 ctypes.c_double, P, P, P]
+        lib.orc_verify_sample_logits.restype = ctypes.c_int
         lib.orc_commit.restype = None
         self.lib = lib
         self.path = path
@@ -190,6 +195,35 @@ class Oracle:
         self.lib.orc_alpha(_ptr(p), ps, _ptr(q), qs, B, K, V, _ptr(a), _ptr(e))
         return a, e
 
+    def softmax(self, z, tau: float):
+        """fp64 temperature softmax of one f32 logit row."""
+        z = _f32(z).reshape(-1)
+        out = np.empty(z.shape[0], dtype=np.float64)
+        self.lib.orc_softmax(_ptr(z), z.shape[0], float(tau), _ptr(out))
+        return out
+
+    def verify_sample_logits(self, zp, zq, t, u_acc, u_res, tau: float):
+        """Sampling verification from logits zp [B][K+1][V], zq [B][K][V] with
+        temperature tau -> (n_accepted, next_token, status bits)."""
+        t = np.ascontiguousarray(t, dtype=np.int32)
+        K = t.shape[-1]
+        zp, B, V, ps = _rows(zp, K + 1, "zp")
+        zq, Bq, Vq, qs = _rows(zq, K, "zq")
+        if (Bq, Vq) != (B, V):
+            raise ValueError("zq shape does not match zp")
+        t = t.reshape(B, K)
+        ua = np.ascontiguousarray(u_acc, dtype=np.float32).reshape(B, K)
+        ur = np.ascontiguousarray(u_res, dtype=np.float64).reshape(B)
+        n, nxt, st = self._outputs(B)
+        rc = self.lib.orc_verify_sample_logits(_ptr(zp), ps, _ptr(zq), qs, _ptr(t), _ptr(ua),
+                                               _ptr(ur), B, K, V, float(tau), _ptr(n),
+                                               _ptr(nxt), _ptr(st))
+        if rc == -1:
+            raise ValueError("temperature must be a positive finite number")
+        if rc != 0:
+            raise MemoryError("oracle: out of host memory")
+        return n, nxt, int(st[0])
+
     def commit(self, t, n, nxt, tokens, lengths):
         """Appends t[b][:n[b]] and next[b] to tokens[b] in place; returns status bits."""
         t = np.ascontiguousarray(t, dtype=np.int32)
@@ -249,3 +283,11 @@ def commit(t, n, nxt, tokens, lengths):
 
 def alpha(p, q, K=None):
     return get().alpha(p, q, K)
+
+
+def softmax(z, tau):
+    return get().softmax(z, tau)
+
+
+def verify_sample_logits(zp, zq, t, u_acc, u_res, tau):
+    return get().verify_sample_logits(zp, zq, t, u_acc, u_res, tau)

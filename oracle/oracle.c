@@ -399,3 +399,92 @@ void orc_alpha(const float *p, int64_t p_stride, const float *q,
             expected[b] = mean;
     }
 }
+
+/* Temperature softmax of one row of logits in fp64:
+ *     out_v = exp((z_v - max_w z_w) / tau) / sum_w exp((z_w - max_w z_w) / tau),
+ * the warp the "spec-verify" page requires both distributions to share
+ * (section "Requirements and limits").  Sums run in ascending v. */
+void orc_softmax(const float *z, int64_t V, double tau, double *out)
+{
+    double m = (double)z[0];
+    for (int64_t v = 1; v < V; ++v)
+        if ((double)z[v] > m)
+            m = (double)z[v];
+    double S = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        out[v] = exp(((double)z[v] - m) / tau);
+        S += out[v];
+    }
+    for (int64_t v = 0; v < V; ++v)
+        out[v] /= S;
+}
+
+/* Sampling verification of one sequence from logits: p_i = softmax(zp_i/tau),
+ * q_i = softmax(zq_i/tau) in fp64, then the rule of section "Method" on those
+ * rows -- accept t_i iff u_acc[i] * q_i(t_i) < p_i(t_i) (fp64), on a rejection
+ * draw from max(0, p_i - q_i) with u_res, after all K the bonus from p_K. */
+static void sample_logits_one(const float *zp, int64_t zp_stride, const float *zq,
+                              int64_t zq_stride, const int32_t *t,
+                              const float *u_acc, double u_res, int K,
+                              int64_t V, double tau, double *pr, double *qr,
+                              int32_t *n_out, int32_t *next_out,
+                              uint32_t *status)
+{
+    if (!tokens_in_range(t, K, V)) {
+        *n_out = 0;
+        *next_out = -1;
+        *status |= ORC_STATUS_BAD_TOKEN;
+        return;
+    }
+    for (int i = 0; i < K; ++i) {
+        orc_softmax(zp + (int64_t)i * zp_stride, V, tau, pr);
+        orc_softmax(zq + (int64_t)i * zq_stride, V, tau, qr);
+        int32_t x = t[i];
+        if (!((double)u_acc[i] * qr[x] < pr[x])) {
+            for (int64_t v = 0; v < V; ++v) {
+                const double d = pr[v] - qr[v];
+                pr[v] = (d > 0.0) ? d : 0.0;
+            }
+            int64_t j = orc_icdf(pr, V, u_res);
+            if (j < 0) { /* p_i == q_i: the residual has no mass; draw from p_i */
+                orc_softmax(zp + (int64_t)i * zp_stride, V, tau, pr);
+                j = orc_icdf(pr, V, u_res);
+            }
+            *next_out = (int32_t)j;
+            *n_out = i;
+            return;
+        }
+    }
+    orc_softmax(zp + (int64_t)K * zp_stride, V, tau, pr);
+    *n_out = K;
+    *next_out = (int32_t)orc_icdf(pr, V, u_res);
+}
+
+/* Batched form over B sequences (layout as the probability entry points,
+ * logits in place of probabilities).  Returns -1 for a temperature that is
+ * not a positive finite number, -2 when out of memory, 0 otherwise. */
+int orc_verify_sample_logits(const float *zp, int64_t zp_stride,
+                             const float *zq, int64_t zq_stride,
+                             const int32_t *t, const float *u_acc,
+                             const double *u_res, int B, int K, int64_t V,
+                             double tau, int32_t *n_out, int32_t *next_out,
+                             uint32_t *status)
+{
+    if (!(tau > 0.0) || !isfinite(tau))
+        return -1;
+    double *pr = malloc((size_t)V * sizeof(double));
+    double *qr = malloc((size_t)V * sizeof(double));
+    if (!pr || !qr) {
+        free(pr);
+        free(qr);
+        return -2;
+    }
+    for (int b = 0; b < B; ++b)
+        sample_logits_one(zp + (int64_t)b * (K + 1) * zp_stride, zp_stride,
+                          zq + (int64_t)b * K * zq_stride, zq_stride,
+                          t + (int64_t)b * K, u_acc + (int64_t)b * K, u_res[b],
+                          K, V, tau, pr, qr, n_out + b, next_out + b, status);
+    free(pr);
+    free(qr);
+    return 0;
+}

@@ -436,6 +436,76 @@ def pin_alpha(orc):
     assert abs(z) < 4.0, f"sampler mean {n.mean():.4f} vs expected length {e[0]:.4f} (z={z:.2f})"
 
 
+def pin_logits(orc):
+    """Sampling from logits (temperature softmax in fp64, then the rule),
+    pinned to: scipy's softmax (a library routine); exact shift and
+    temperature identities; huge logits (no overflow: the max is
+    subtracted); agreement with the probability oracle on the same
+    distributions, away from its decision boundaries; and distribution
+    preservation of the first emitted token (the rejection-sampling theorem),
+    by a chi-square test over many rounds."""
+    from scipy import special, stats
+
+    rng = np.random.default_rng(9191)
+    z = (rng.normal(0, 3, 1000)).astype(np.float32)
+    for tau in (0.5, 1.0, 1.7):
+        ref = special.softmax(z.astype(np.float64) / tau)
+        got = orc.softmax(z, tau)
+        assert np.allclose(got, ref, rtol=1e-13, atol=0), tau
+        assert abs(got.sum() - 1.0) < 1e-13
+    # exact identities: a shift by a representable constant, and tau = 2 on z
+    # equals tau = 1 on z / 2 (both exact in fp32 here)
+    zq16 = (np.round(z * 1024) / 1024).astype(np.float32)
+    assert np.array_equal(orc.softmax(zq16, 1.3), orc.softmax(zq16 + np.float32(8.0), 1.3))
+    assert np.array_equal(orc.softmax(zq16, 2.0), orc.softmax(zq16 / np.float32(2.0), 1.0))
+    big = np.array([3.0e38, 2.9e38, -3.0e38, 3.0e38], dtype=np.float32)
+    sb = orc.softmax(big, 1e36)
+    assert np.isfinite(sb).all() and abs(sb.sum() - 1) < 1e-12 and sb[0] == sb[3] > sb[1]
+    # the same draws as the probability oracle, except near its boundaries
+    B, K, V = 300, 3, 200
+    zp = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    zqq = (zp[:, :K] + rng.normal(0, 0.8, (B, K, V))).astype(np.float32)
+    tau = 0.9
+    P = np.stack([[orc.softmax(zp[b, i], tau) for i in range(K + 1)] for b in range(B)])
+    Q = np.stack([[orc.softmax(zqq[b, i], tau) for i in range(K)] for b in range(B)])
+    t = np.stack([[rng.choice(V, p=Q[b, i] / Q[b, i].sum()) for i in range(K)] for b in range(B)])
+    t = t.astype(np.int32)
+    ua = rng.random((B, K)).astype(np.float32)
+    ur = rng.random(B)
+    n1, x1, s1 = orc.verify_sample_logits(zp, zqq, t, ua, ur, tau)
+    n0, x0, s0 = orc.verify_sample(P.astype(np.float32), Q.astype(np.float32), t, ua, ur)
+    assert s1 == 0 and s0 == 0
+    agree = (n1 == n0) & (x1 == x0)
+    assert agree.mean() > 0.97, agree.mean()
+    for b in np.nonzero(~agree)[0]:   # a disagreement needs a near-tie somewhere
+        i = min(int(n0[b]), int(n1[b]))
+        if n0[b] != n1[b]:
+            pt, qt = P[b, i, t[b, i]], Q[b, i, t[b, i]]
+            assert abs(ua[b, i] * qt - pt) <= 1e-6 * max(pt, 1e-30), (b, i, ua[b, i] * qt, pt)
+        else:
+            r = np.maximum(P[b, i] - Q[b, i], 0) if i < K else P[b, K]
+            C = np.cumsum(r)
+            T = ur[b] * C[-1]
+            lo, hi = sorted((int(x0[b]), int(x1[b])))
+            assert np.abs(C[lo:hi + 1] - T).min() <= 1e-6 * C[-1], (b, lo, hi)
+    # distribution preservation: the first emitted token ~ p_0
+    R, K, V = 20000, 2, 12
+    zp1 = rng.normal(0, 1.2, (K + 1, V)).astype(np.float32)
+    zq1 = (zp1[:K] + rng.normal(0, 0.7, (K, V))).astype(np.float32)
+    tau = 1.3
+    q0 = np.stack([orc.softmax(zq1[i], tau) for i in range(K)])
+    zpb = np.broadcast_to(zp1, (R, K + 1, V)).copy()
+    zqb = np.broadcast_to(zq1, (R, K, V)).copy()
+    t = np.stack([rng.choice(V, size=R, p=q0[i] / q0[i].sum()) for i in range(K)], 1).astype(np.int32)
+    n, x, st = orc.verify_sample_logits(zpb, zqb, t, rng.random((R, K)).astype(np.float32),
+                                        rng.random(R), tau)
+    first = np.where(n > 0, t[:, 0], x)
+    p0 = orc.softmax(zp1[0], tau)
+    obs = np.bincount(first, minlength=V)
+    chi = ((obs - R * p0) ** 2 / (R * p0)).sum()
+    assert stats.chi2.sf(chi, V - 1) > 1e-3, (obs, R * p0)
+
+
 def pin_special_cases(orc):
     """q == p accepts everything; one-hot targets and single-token residuals are
     deterministic; power-of-two scaling changes nothing."""
@@ -585,4 +655,5 @@ PINS = [
     pin_threads_agree,
     pin_analytic_length_law,
     pin_alpha,
+    pin_logits,
 ]

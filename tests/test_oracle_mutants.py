@@ -56,6 +56,14 @@ MUTANTS = [
     ("alpha_unnormalised_q", "const double y = (double)qr[v] / Q;", "const double y = (double)qr[v];", 1),
     ("alpha_expected_off_by_one", "reach *= a;    /* P(n > i) = prod_{j <= i} alpha_j */\n            mean += reach;",
      "mean += reach;\n            reach *= a;", 1),
+    ("logits_no_temperature", "out[v] = exp(((double)z[v] - m) / tau);",
+     "out[v] = exp(((double)z[v] - m));", 1),
+    ("logits_no_max_shift", "out[v] = exp(((double)z[v] - m) / tau);",
+     "out[v] = exp((double)z[v] / tau);", 1),
+    ("logits_draft_unwarped", "orc_softmax(zq + (int64_t)i * zq_stride, V, tau, qr);",
+     "orc_softmax(zq + (int64_t)i * zq_stride, V, 1.0, qr);", 1),
+    ("logits_bonus_row_k_minus_1", "orc_softmax(zp + (int64_t)K * zp_stride, V, tau, pr);",
+     "orc_softmax(zp + (int64_t)(K - 1) * zp_stride, V, tau, pr);", 1),
     ("threads_drop_tail", "j->b1 = (int)((int64_t)B * (k + 1) / nthreads);",
      "j->b1 = (int)((int64_t)B * (k + 1) / nthreads) - (k == nthreads - 1 && k > 0);", 1),
 ]
