@@ -46,8 +46,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--mode", choices=["sample", "greedy", "round", "alpha"], default=None,
-                    help="alpha: the acceptance-rate diagnostic instead of a verification round")
+    ap.add_argument("--mode", choices=["sample", "greedy", "round", "alpha", "logits"],
+                    default=None,
+                    help="alpha: the acceptance-rate diagnostic; logits: sampling from logits "
+                         "(log of the workload's probabilities, temperature 1)")
     ap.add_argument("--sets", type=int, default=4, help="input sets rotated through")
     ap.add_argument("--graph", action="store_true", help="replay the steps from a CUDA graph")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="persistent grid residency (0 = max)")
@@ -118,6 +120,17 @@ def required_bytes(mode_arr, n_arr, K: int, V: int) -> int:
             tested = min(n + 1, K)
             rows = 8 * V if n < K else 4 * V
             total += 64 * tested + rows + 4 * K + 4 * K + 8 + 8
+    return total
+
+
+def logits_bytes(n_arr, K: int, V: int) -> int:
+    """Sampling from logits reads the row pair (zp_i, zq_i) of every tested
+    position once for its normalisers, then the rejected pair again (8V) or the
+    bonus row zp_K twice (8V), plus tokens, uniforms and outputs."""
+    total = 0
+    for n in n_arr:
+        tested = min(int(n) + 1, K)
+        total += (tested + 1) * 8 * V + 8 * K + 16
     return total
 
 
@@ -263,6 +276,8 @@ def time_oracle(host, mode: str, K: int, seconds: float, nthreads: int, max_roun
         p, t, ua, ur, md = p[sl], t[sl], ua[sl], ur[sl], md[sl]
         q = None if q is None else q[sl]
     nb = p.shape[0]
+    if mode == "logits":
+        p, q = np.log(p), np.log(q)
     rounds = 0
     t0 = time.perf_counter()
     while True:
@@ -272,6 +287,8 @@ def time_oracle(host, mode: str, K: int, seconds: float, nthreads: int, max_roun
             oracle.verify_sample(p, q, t, ua, ur, nthreads=nthreads)
         elif mode == "alpha":
             oracle.alpha(p, q)   # single-threaded
+        elif mode == "logits":
+            oracle.verify_sample_logits(p, q, t, ua, ur, 1.0)   # single-threaded
         else:
             oracle.verify_round(md, p, q, t, ua, ur, nthreads=nthreads)
         rounds += 1
@@ -366,7 +383,13 @@ def main(argv=None):
     calls = []
     keep = []
     for bt, (n, nx) in zip(sets, outs):
-        if args.mode == "alpha":
+        if args.mode == "logits":
+            zp, zq = torch.log(bt.p), torch.log(bt.q)
+            keep.append((zp, zq))
+            calls.append((lib.sv_verify_sample_logits,
+                          (P(zp), V, P(zq), V, P(bt.t), P(bt.u_acc), P(bt.u_res), B, K, V,
+                           ctypes.c_float(1.0), P(n), P(nx), ws.ptr, ws.nbytes, sh)))
+        elif args.mode == "alpha":
             a_out = torch.empty(B, K, dtype=torch.float64, device=dev)
             e_out = torch.empty(B, dtype=torch.float64, device=dev)
             keep.append((a_out, e_out))
@@ -402,10 +425,10 @@ def main(argv=None):
     req, dense, nhist = [], [], np.zeros(K + 1, dtype=np.int64)
     for bt, (n, _) in zip(sets if args.mode != "alpha" else [], outs):
         md = bt.mode.cpu().numpy() if args.mode == "round" else np.full(
-            B, 0 if args.mode == "greedy" else 1)
+            B, 0 if args.mode == "greedy" else 1)   # logits: sampling
         nn = n.cpu().numpy()
         nhist += np.bincount(nn, minlength=K + 1)[:K + 1]
-        req.append(required_bytes(md, nn, K, V))
+        req.append(logits_bytes(nn, K, V) if args.mode == "logits" else required_bytes(md, nn, K, V))
         dense.append(dense_bytes(md, K, V))
     if args.mode == "alpha":
         req = dense = [alpha_bytes(B, K, V)]
@@ -488,7 +511,7 @@ def main(argv=None):
         host = sets[0].numpy()
         ncpu = os.cpu_count() or 1
         rps, nb, rounds, el = time_oracle(host, args.mode, K, args.cpu_seconds, ncpu)
-        used = 1 if args.mode == "alpha" else ncpu   # the alpha oracle is single-threaded
+        used = 1 if args.mode in ("alpha", "logits") else ncpu   # single-threaded oracles
         cpu = {"value": rps, "unit": UNIT, "cores": used, "kind": "oracle",
                "sample": f"{rounds} full rounds ({nb} sequences each) of input set 0, "
                          f"{el:.1f} s on {used} thread{'s' if used > 1 else ''}"}

@@ -186,6 +186,27 @@ int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags);
  * for tuning sweeps. */
 int sv_set_ctas_per_sm(int32_t ctas_per_sm);
 
+/* Sampling verification straight from logits: p_i = softmax(zp_i / T),
+ * q_i = softmax(zq_i / T) with T = temperature (the identical warp the
+ * "spec-verify" page requires of both distributions, section "Requirements and
+ * limits"), then the sampling rule of sv_verify_sample on those rows; the
+ * warped rows are never written to memory.  zp holds B*(K+1) rows and zq B*K
+ * rows of V f32 logits, laid out like p and q above.  Rows are read in order:
+ * the pair (zp_i, zq_i) once for its normalisers and the accept test of
+ * position i, the rejected pair (or zp_K) a second time for the draw.
+ * Arithmetic is fp32 with exp2.approx and double-fp32 sums: an accept decision
+ * can differ from an exact (fp64) softmax only when |u*q - p| < ~1e-5 * p, and
+ * a drawn token only when u*R lies within ~2e-6 of normalised mass of a
+ * boundary.  temperature must be positive and finite (else SV_EINVAL); logits
+ * must be finite.  Greedy needs no warp: argmax softmax(z/T) = argmax z, so
+ * sv_verify_greedy takes logits directly.  Workspace and status as above. */
+int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride,
+                            const float *zq, int64_t zq_row_stride,
+                            const int32_t *t, const float *u_accept, const double *u_resample,
+                            int32_t B, int32_t K, int64_t V, float temperature,
+                            int32_t *n_accepted, int32_t *next_token,
+                            void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
 /* Acceptance-rate diagnostic: for each sequence b and draft position i < K,
  *   alpha[b][i] = sum_v min(p_i(v) / P_i, q_i(v) / Q_i),
  * P_i, Q_i the totals of rows p (b, i) and q (b, i) (a row with zero total

@@ -64,3 +64,47 @@ def compare(p, q, u_res, mode, K, n_ref, next_ref, n_gpu, next_gpu, st_ref=None,
                     f"boundary case (T={T!r}, R={R!r})")
         boundary.append((b, int(next_ref[b]), int(next_gpu[b])))
     return boundary
+
+
+# Sampling from logits: the kernels warp with fp32 exp2.approx, the oracle with
+# an fp64 softmax.  Each mass then carries ~1e-6 relative error at most
+# (exp2.approx ~2^-22, the fp32 argument (z - max)/T, the fp32 normaliser), so
+# an accept decision may differ only where |u*q - p| <= ACCEPT_TOL_LOGITS * p,
+# and a drawn token only where u*R lies within DRAW_TOL_LOGITS (normalised
+# mass) of a boundary between the two answers.
+ACCEPT_TOL_LOGITS = 1e-5
+DRAW_TOL_LOGITS = 2e-6
+
+
+def compare_logits(zp, zq, tau, t, u_acc, u_res, n_ref, next_ref, n_gpu, next_gpu):
+    """Checks GPU outputs of sampling-from-logits against the oracle's; returns
+    the explained differences [(b, kind)]: 'accept' near-threshold decisions and
+    'draw' near-boundary tokens.  Raises AssertionError on any other."""
+    import oracle
+    explained = []
+    K = t.shape[1]
+    for b in np.nonzero((n_ref != n_gpu) | (next_ref != next_gpu))[0]:
+        if n_ref[b] != n_gpu[b]:
+            i = int(min(n_ref[b], n_gpu[b]))
+            x = int(t[b, i])
+            p = oracle.softmax(zp[b, i], tau)[x]
+            q = oracle.softmax(zq[b, i], tau)[x]
+            margin = abs(float(u_acc[b, i]) * q - p)
+            assert margin <= ACCEPT_TOL_LOGITS * p, (
+                f"seq {b}: n oracle {n_ref[b]} gpu {n_gpu[b]}, accept margin {margin / p:.3e}")
+            explained.append((int(b), "accept"))
+            continue
+        n = int(n_ref[b])
+        if n < K:
+            r = np.maximum(oracle.softmax(zp[b, n], tau) - oracle.softmax(zq[b, n], tau), 0.0)
+        else:
+            r = oracle.softmax(zp[b, K], tau)
+        C = np.cumsum(r)
+        T = float(u_res[b]) * C[-1]
+        j = int(next_gpu[b])
+        assert 0 <= j < r.shape[0] and r[j] > 0, f"seq {b}: gpu token {j} has no mass"
+        lo, hi = sorted((int(next_ref[b]), j))
+        assert np.abs(C[lo:hi] - T).min() <= DRAW_TOL_LOGITS, (
+            f"seq {b}: token oracle {next_ref[b]} gpu {j} not at a boundary")
+        explained.append((int(b), "draw"))
+    return explained

@@ -40,7 +40,7 @@ MAX_K = 64
 EXPORTED = (
     "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
     "sv_verify_round", "sv_get_status", "sv_set_ctas_per_sm", "sv_last_grid_size",
-    "sv_last_kernel_count", "sv_alpha",
+    "sv_last_kernel_count", "sv_alpha", "sv_verify_sample_logits",
     "sv_status_string", "sv_version", "sv_verify_sample_noalloc",
 )
 
@@ -91,6 +91,9 @@ def load():
         lib.sv_last_kernel_count.restype = i32
         lib.sv_alpha.argtypes = [P, i64, P, i64, i32, i32, i64, P, P, P, sz, P]
         lib.sv_alpha.restype = ctypes.c_int
+        lib.sv_verify_sample_logits.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64,
+                                                ctypes.c_float, P, P, P, sz, P]
+        lib.sv_verify_sample_logits.restype = ctypes.c_int
         lib.sv_status_string.argtypes = [ctypes.c_int]
         lib.sv_status_string.restype = ctypes.c_char_p
         lib.sv_version.argtypes = []
@@ -307,6 +310,32 @@ def verify_sample_noalloc(p, q, t, u_acc, u_res, *, n_out=None, next_out=None, s
                                          _ptr(u_res), B, K, V, _ptr(n_out), _ptr(next_out),
                                          _stream_handle(stream))
     _check(rc, "sv_verify_sample_noalloc")
+    return n_out, next_out
+
+
+def verify_sample_logits(zp, zq, t, u_acc, u_res, temperature: float = 1.0, *, ws=None,
+                         n_out=None, next_out=None, stream=None):
+    """Sampling verification from logits: zp [B][K+1][V], zq [B][K][V] f32 (or
+    [K+1][V] / [K][V]), warped by softmax(z / temperature) on the fly ->
+    (n_accepted, next_token) int32 [B]."""
+    torch = _torch()
+    t_ = t if t.dim() == 2 else t.reshape(1, -1)
+    K = t_.shape[1]
+    zp, B, V, ps = _rows3(zp, K + 1, "zp", torch.float32)
+    dev = _device_of(zp)
+    zq, Bq, Vq, qs = _rows3(zq, K, "zq", torch.float32) if K > 0 else (None, B, V, V)
+    if K > 0 and (Bq, Vq) != (B, V):
+        raise SpecVerifyError("zq shape does not match zp")
+    t = _vec(t, B * K, "t", torch.int32, dev)
+    u_acc = _vec(u_acc, B * K, "u_acc", torch.float32, dev)
+    u_res = _vec(u_res, B, "u_res", torch.float64, dev)
+    n_out, next_out = _outputs(B, dev, n_out, next_out)
+    w = _workspace(ws, B, K, V, dev)
+    _check(load().sv_verify_sample_logits(_ptr(zp), ps, _ptr(zq), qs, _ptr(t), _ptr(u_acc),
+                                          _ptr(u_res), B, K, V, float(temperature), _ptr(n_out),
+                                          _ptr(next_out), w.ptr, w.nbytes,
+                                          _stream_handle(stream)),
+           "sv_verify_sample_logits")
     return n_out, next_out
 
 

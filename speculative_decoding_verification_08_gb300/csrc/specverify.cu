@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
@@ -15,6 +16,7 @@
 #include "sv_alpha.cuh"
 #include "sv_device.cuh"
 #include "sv_item.cuh"
+#include "sv_logits.cuh"
 #include "specverify.h"
 
 // 1: batches of 16-byte-aligned rows with at least one sequence per SM run as
@@ -503,6 +505,45 @@ int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row
         }
     }
     return SV_OK;
+}
+
+int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float *zq,
+                            int64_t zq_row_stride, const int32_t *t, const float *u_accept,
+                            const double *u_resample, int32_t B, int32_t K, int64_t V,
+                            float temperature, int32_t *n_accepted, int32_t *next_token,
+                            void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+    int rc = common_checks(zp, zp_row_stride, t, B, K, V, n_accepted, next_token);
+    if (rc != SV_OK || B == 0) return rc;
+    if (!u_resample || !(temperature > 0.f) || !std::isfinite(temperature)) return SV_EINVAL;
+    if (K > 0 && (!zq || !u_accept || zq_row_stride < V)) return SV_EINVAL;
+    sv::Params P = make_params(zp, zp_row_stride, zq, zq_row_stride, t, u_accept, u_resample,
+                               nullptr, B, K, V, n_accepted, next_token);
+    if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
+    if ((rc = place_arrays(P)) != SV_OK) return rc;
+    if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
+    sv::LogitsParams L{};
+    L.zp = P.p;
+    L.ps = P.ps;
+    L.zq = P.q;
+    L.qs = P.qs;
+    L.t = P.t;
+    L.u_acc = P.u_acc;
+    L.u_res = P.u_res;
+    L.B = B;
+    L.K = K;
+    L.V = V;
+    L.nseg = (int32_t)num_segments(V);
+    L.c = (float)(1.4426950408889634 / (double)temperature);
+    L.n_out = P.n_out;
+    L.next_out = P.next_out;
+    L.status = P.status;
+    L.seg = P.seg;
+    L.blk = P.blk;
+    g_last_grid = B;
+    g_last_kernels = 1;
+    sv::logits_sample_kernel<<<(unsigned)B, sv::kLgThreads, 0,
+                               reinterpret_cast<cudaStream_t>(stream)>>>(L);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags) {

@@ -746,17 +746,20 @@ __device__ __forceinline__ float2 load_sum(const float2 *p, bool local) {
     return local ? *p : ld_l2(p);
 }
 
-// Inverse-CDF draw for sequence b over the segment sums seg[0..nseg) and
-// block sums blk of the row pair (pr, qr) (one warp): the token, -1 if the
-// total mass is zero, -2 if the staged block sums never arrived.  The segment
-// (lane l owns segments [l * per, (l + 1) * per)), the block within it (lanes
-// 0..7), the element within the block: one load round trip each, or two in
-// all when the block sums were staged while the segment sums loaded.
-template <bool kResidual>
-__device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *blk,
-                              const float *pr, const float *qr, const DrawInputs &in, int lane) {
-    const int per = (P.nseg + 31) / 32;
-    const int r0 = min(P.nseg, lane * per), r1 = min(P.nseg, r0 + per);
+// Inverse-CDF draw over the segment sums seg[0..nseg) and block sums blk of a
+// row of V masses (one warp): the token, -1 if the total mass is zero, -2 if
+// the staged block sums never arrived.  The segment (lane l owns segments
+// [l * per, (l + 1) * per)), the block within it (lanes 0..7), then
+// in_block(base, prefix, T), which finds the element within the 128-element
+// block at `base`: one load round trip each, or two in all when the block
+// sums were staged while the segment sums loaded.  With in.prefetch, rows
+// pf0 and pf1 (either may be null) are asked into L2 at the chosen segment.
+template <class InBlock>
+__device__ int draw_core(int nseg, int64_t V, const float2 *seg, const float2 *blk,
+                         const float *pf0, const float *pf1, const DrawInputs &in, int lane,
+                         InBlock in_block) {
+    const int per = (nseg + 31) / 32;
+    const int r0 = min(nseg, lane * per), r1 = min(nseg, r0 + per);
     dd v[kSegRegs];
 #pragma unroll
     for (int r = 0; r < kSegRegs; ++r) {
@@ -834,8 +837,8 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
         Tt = dd{__int_as_float(0x7f800000), 0.f};
     }
     if (in.prefetch && lane < 2) {
-        const int c = min(kSeg, (int)(P.V - (int64_t)sg * kSeg)) & ~3;
-        const float *row = lane == 0 ? pr : qr;
+        const int c = min(kSeg, (int)(V - (int64_t)sg * kSeg)) & ~3;
+        const float *row = lane == 0 ? pf0 : pf1;
         if (c && row) prefetch_l2(row + (int64_t)sg * kSeg, 4u * (uint32_t)c);
     }
     // block within the segment
@@ -855,7 +858,16 @@ __device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *
         bbefore = zero;
         Tt = dd{__int_as_float(0x7f800000), 0.f};
     }
-    return search_block<kResidual>(pr, qr, (int64_t)sg * kSeg + 128 * bk, P.V, bbefore, Tt, lane);
+    return in_block((int64_t)sg * kSeg + 128 * bk, bbefore, Tt);
+}
+
+// The draw over a probability row pair (pr, qr), or over pr alone.
+template <bool kResidual>
+__device__ int draw_from_sums(const Params &P, const float2 *seg, const float2 *blk,
+                              const float *pr, const float *qr, const DrawInputs &in, int lane) {
+    return draw_core(P.nseg, P.V, seg, blk, pr, qr, in, lane, [&](int64_t base, dd prefix, dd T) {
+        return search_block<kResidual>(pr, qr, base, P.V, prefix, T, lane);
+    });
 }
 
 // Commit step of a round ("spec-verify", section "Usage": keep

@@ -1,0 +1,100 @@
+"""Sampling verification from logits on the GPU against the oracle's fp64
+softmax: n and next_token equal except near-threshold accept decisions and
+near-boundary draws within the tolerances the fp32 warp allows
+(oracle/compare.py), which are counted.  Greedy from logits is bit-exact."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.compare import compare_logits
+import speculative_decoding_verification_08_gb300 as sv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sv.build()
+    sv.load()
+
+
+def make_logits(B, V, K, tau, seed, target_std=2.0, noise=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    zp = torch.randn(B, K + 1, V, device="cuda", generator=g) * target_std
+    zq = zp[:, :K] + noise * torch.randn(B, K, V, device="cuda", generator=g)
+    if K > 0:
+        q = torch.softmax(zq.double() / tau, -1)
+        t = torch.multinomial(q.reshape(B * K, V).float(), 1, generator=g).reshape(B, K)
+    else:
+        t = torch.zeros(B, 0, dtype=torch.int64, device="cuda")
+    ua = torch.rand(B, K, device="cuda", generator=g)
+    ur = torch.rand(B, device="cuda", generator=g, dtype=torch.float64)
+    return zp.contiguous(), zq.contiguous(), t.to(torch.int32).contiguous(), ua, ur
+
+
+def run(zp, zq, t, ua, ur, tau):
+    n1, x1 = sv.verify_sample_logits(zp, zq, t, ua, ur, tau)
+    h = [x.cpu().numpy() for x in (zp, zq, t, ua, ur)]
+    n0, x0, s0 = oracle.verify_sample_logits(*h, tau)
+    assert s0 == 0
+    expl = compare_logits(h[0], h[1], tau, h[2], h[3], h[4], n0, x0, n1.cpu().numpy(),
+                          x1.cpu().numpy())
+    return n0, expl
+
+
+@pytest.mark.parametrize("B,V,K,tau", [(64, 4096, 4, 1.0), (33, 20011, 5, 0.7), (8, 1, 3, 1.0),
+                                       (16, 50000, 8, 1.6), (5, 3000, 0, 1.0), (9, 777, 16, 0.5)])
+def test_logits_match_oracle(B, V, K, tau):
+    zp, zq, t, ua, ur = make_logits(B, V, K, tau, seed=7000 + V + K)
+    n0, expl = run(zp, zq, t, ua, ur, tau)
+    assert len(expl) <= max(1, B // 20), expl
+    if K > 0 and V > 1:
+        assert len(set(n0.tolist())) > 1
+
+
+def test_logits_headline_shape():
+    """B=256, V=128256, K=5 logits, the warp at T=1."""
+    zp, zq, t, ua, ur = make_logits(256, 128256, 5, 1.0, seed=20261203)
+    n0, expl = run(zp, zq, t, ua, ur, 1.0)
+    assert len(expl) <= 6, expl
+    counts = np.bincount(n0, minlength=6)
+    assert counts[0] > 0 and counts[5] > 0
+
+
+def test_logits_unaligned_rows_and_equal_rows():
+    B, V, K, tau = 12, 3001, 3, 1.0
+    zp, zq, t, ua, ur = make_logits(B, V + 1, K, tau, seed=99)
+    zp = zp[..., 1:]          # rows start off a 16-byte boundary
+    zq = zq[..., 1:]
+    t = torch.clamp(t, max=V - 1)
+    zq[0] = zp[0, :K]         # identical rows: every draft accepted
+    n0, expl = run(zp, zq, t, ua, ur, tau)
+    assert n0[0] == K and len(expl) <= 1
+
+
+def test_greedy_from_logits_is_exact():
+    """argmax softmax(z/T) = argmax z: the greedy entry point on raw logits
+    (negative values, planted ties) equals the oracle's greedy on the same."""
+    B, V, K = 40, 5000, 4
+    g = torch.Generator(device="cuda").manual_seed(3)
+    zp = torch.randn(B, K + 1, V, device="cuda", generator=g) * 3 - 5
+    am = zp.argmax(-1)
+    t = am[:, :K].clone()
+    t[::3, 1] = (t[::3, 1] + 1) % V          # some misses
+    dup = torch.arange(0, B, 4, device="cuda")
+    zp[dup, 0, 17] = zp[dup, 0].max(-1).values   # exact ties, lowest index wins
+    n1, x1 = sv.verify_greedy(zp, t.to(torch.int32).contiguous())
+    n0, x0, s0 = oracle.verify_greedy(zp.cpu().numpy(), t.to(torch.int32).cpu().numpy())
+    assert np.array_equal(n1.cpu().numpy(), n0) and np.array_equal(x1.cpu().numpy(), x0)
+
+
+@pytest.mark.parametrize("tau", [0.0, -1.0, float("inf"), float("nan")])
+def test_bad_temperature_rejected(tau):
+    zp, zq, t, ua, ur = make_logits(2, 100, 2, 1.0, seed=1)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.verify_sample_logits(zp, zq, t, ua, ur, tau)
