@@ -1,0 +1,160 @@
+"""The round driver and the speculation governor.
+
+The governor is host logic (CPU tests).  The driver runs its verification on
+the GPU: greedy decoding through it must give exactly the stream plain greedy
+decoding of the target gives ("spec-verify", section "Method"), with or without
+the governor switching to one-token rounds; sampled rounds must agree with
+the oracle on the same rows and uniforms."""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_08_gb300 as sv
+from speculative_decoding_verification_08_gb300.decoder import SpeculationGovernor, SpeculativeDecoder
+
+V = 48
+
+
+def _logits(prefix, salt):
+    h = hashlib.sha256((salt + ",".join(map(str, prefix[-4:]))).encode()).digest()
+    rng = np.random.default_rng(int.from_bytes(h[:8], "little"))
+    z = rng.normal(0, 2.0, V)
+    z[rng.integers(0, V)] = z.max()          # frequent exact ties: lowest index must win
+    return z
+
+
+def _softmax(z):
+    e = np.exp(z - z.max())
+    return (e / e.sum()).astype(np.float32)
+
+
+def target_row(prefix):
+    return _softmax(_logits(prefix, "target"))
+
+
+def draft_row(prefix, noise):
+    z = _logits(prefix, "target") + noise * _logits(prefix, "draft")
+    return _softmax(z)
+
+
+def make_callbacks(noise=0.6, greedy_draft=True, seed=0):
+    rng = np.random.default_rng(seed)
+
+    def draft_step(prefix, k):
+        toks, probs = [], []
+        p = list(prefix)
+        for _ in range(k):
+            q = draft_row(p, noise)
+            x = int(np.argmax(q)) if greedy_draft else int(rng.choice(V, p=q / q.sum()))
+            toks.append(x)
+            probs.append(q)
+            p.append(x)
+        return toks, np.stack(probs)
+
+    def target_step(prefix, proposed):
+        p = list(prefix)
+        rows = [target_row(p)]
+        for x in proposed:
+            p.append(int(x))
+            rows.append(target_row(p))
+        return np.stack(rows)
+
+    return draft_step, target_step
+
+
+def plain_greedy(prompt, max_new):
+    p = list(prompt)
+    for _ in range(max_new):
+        p.append(int(oracle.argmax_lowest(target_row(p))))
+    return p[len(prompt):]
+
+
+# ---------------------------------------------------------------------------
+# governor (CPU)
+
+def test_governor_trips_on_zero_accept_and_never_resumes():
+    g = SpeculationGovernor(window=4, alpha_threshold=0.0)
+    assert g.record(3, 4) and g.record(1, 4)
+    assert not g.record(0, 4) and g.reason == "zero-accept round"
+    assert not g.record(4, 4) and not g.speculating
+
+
+def test_governor_threshold_over_a_full_window():
+    g = SpeculationGovernor(window=3, alpha_threshold=0.5, stop_on_zero_accept=False)
+    assert g.record(1, 4) and g.record(1, 4)          # window not yet full
+    assert not g.record(2, 4)                          # 4/12 < 0.5 once full
+    assert g.reason == "acceptance below threshold"
+    g2 = SpeculationGovernor(window=2, alpha_threshold=0.5)
+    for _ in range(10):
+        assert g2.record(3, 4)                         # rolling 0.75 stays above
+    assert g2.rate == 0.75
+
+
+def test_governor_rejects_bad_counts():
+    g = SpeculationGovernor()
+    with pytest.raises(ValueError):
+        g.record(5, 4)
+    with pytest.raises(ValueError):
+        SpeculationGovernor(window=0)
+
+
+# ---------------------------------------------------------------------------
+# driver (GPU)
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("k", [1, 3, 4, 7])
+def test_greedy_driver_equals_plain_greedy(k):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    draft_step, target_step = make_callbacks(noise=0.6)
+    dec = SpeculativeDecoder(draft_step, target_step, k=k, greedy=True)
+    prompt = [1, 2, 3]
+    out = dec.generate(prompt, max_new=60)
+    assert out == plain_greedy(prompt, 60)
+    assert any(n > 0 for _, n, _ in dec.trace) and any(n < k for _, n, _ in dec.trace)
+
+
+@pytest.mark.gpu
+def test_governor_switches_to_single_token_rounds():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    draft_step, target_step = make_callbacks(noise=8.0)     # a poor draft: zero-accept rounds
+    gov = SpeculationGovernor(window=4, alpha_threshold=0.4)
+    dec = SpeculativeDecoder(draft_step, target_step, k=4, greedy=True, governor=gov)
+    out = dec.generate([5, 6], max_new=40)
+    assert out == plain_greedy([5, 6], 40)
+    assert not gov.speculating
+    ks = [k for k, _, _ in dec.trace]
+    first_ar = ks.index(0)
+    assert all(k == 0 for k in ks[first_ar:]) and all(k == 4 for k in ks[:first_ar])
+
+
+@pytest.mark.gpu
+def test_sampling_rounds_match_the_oracle():
+    """Each sampled round equals the oracle's verification of the same rows
+    with the same uniforms (the decoder's generator is replayed here)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    k = 4
+    draft_step, target_step = make_callbacks(noise=0.8, greedy_draft=False, seed=5)
+    dec = SpeculativeDecoder(draft_step, target_step, k=k, greedy=False, seed=123)
+    prompt = [9, 9]
+    out = dec.generate(prompt, max_new=50)
+    assert len(out) == 50
+    # replay: same callbacks (fresh rng with the same seed), same generator
+    draft_step, target_step = make_callbacks(noise=0.8, greedy_draft=False, seed=5)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(123)
+    prefix = list(prompt)
+    for kk, n, nxt in dec.trace:
+        toks, q = draft_step(prefix, kk)
+        p = target_step(prefix, toks)
+        ua = torch.rand(1, kk, generator=gen, device="cuda").cpu().numpy()
+        ur = torch.rand(1, generator=gen, device="cuda", dtype=torch.float64).cpu().numpy()
+        n0, x0, _ = oracle.verify_sample(p[None], q[None], np.array([toks], dtype=np.int32), ua, ur)
+        assert (int(n0[0]), int(x0[0])) == (n, nxt)
+        prefix = prefix + list(toks[:n]) + [nxt]
+    assert prefix[len(prompt):len(prompt) + 50] == out
