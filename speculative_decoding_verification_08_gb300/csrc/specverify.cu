@@ -539,11 +539,24 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     L.status = P.status;
     L.seg = P.seg;
     L.blk = P.blk;
-    g_last_grid = B;
+    // one cluster of up to 8 CTAs per sequence, never more CTAs than segments
+    L.csize = (int32_t)std::min<int64_t>(sv::kLgMaxCluster, std::max<int64_t>(1, L.nseg));
+    if ((int64_t)B * L.csize > INT32_MAX) return SV_EINVAL;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * L.csize));
+    cfg.blockDim = dim3(sv::kLgThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)L.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    g_last_grid = (int64_t)B * L.csize;
     g_last_kernels = 1;
-    sv::logits_sample_kernel<<<(unsigned)B, sv::kLgThreads, 0,
-                               reinterpret_cast<cudaStream_t>(stream)>>>(L);
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+    return cudaLaunchKernelEx(&cfg, sv::logits_sample_kernel, L) == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags) {

@@ -8,30 +8,46 @@
 // argmax p_i = argmax zp_i, and the greedy entry point takes logits as they
 // are.)
 //
-// One CTA per sequence walks its rows in order.  For position i it streams the
-// row pair (zp_i, zq_i) once, keeping per lane an online maximum and a
-// double-fp32 sum of exp2((z - max) * c), c = log2(e) / tau; a CTA combine
-// gives the normalisers, and the accept test u * q_i(t_i) < p_i(t_i) is made
-// on the recomputed gathers.  After the first rejection it streams that row
-// pair a second time, forming r = max(0, p - q) per element in fp32 and the
-// double-fp32 block and segment sums of r; when all K are accepted it streams
-// zp_K twice (normaliser, then the masses of p_K).  The draw is the same
-// segment -> block -> element search as the probability path, its element step
+// One thread-block cluster of up to 8 CTAs per sequence walks its rows in
+// order; CTA r of the cluster streams segments r*8 + w, r*8 + w + 8*C, ... (w
+// its warp, C the cluster size).  For position i each CTA streams its share of
+// the row pair (zp_i, zq_i) once, keeping per lane an online maximum and a
+// compensated (Kahan) fp32 sum of exp2((z - max) * c), c = log2(e) / tau.  The CTA writes
+// its (max, sum) pair into a shared slot (two slots, alternating by row), one
+// cluster barrier follows, and every CTA combines all C slots in rank order
+// through distributed shared memory -- so every CTA holds bit-identical
+// normalisers and reaches the same accept decision u * q_i(t_i) < p_i(t_i)
+// (made on the recomputed gathers).  After the first rejection the cluster
+// streams that row pair a second time, forming r = max(0, p - q) per element
+// in fp32 and, from fp32 sums of four, the double-fp32 block and segment sums
+// of r in the workspace;
+// when all K are accepted it streams zp_K twice (normaliser, then the masses
+// of p_K).  After a last cluster barrier CTA 0 draws: the same segment ->
+// block -> element search as the probability path, its element step
 // recomputing the masses with the same instructions.
+//
+// Every CTA of a cluster makes the same sequence of barrier calls: the
+// decisions between them depend only on values every CTA computes identically,
+// and no CTA leaves while another may still read its shared memory (the last
+// reads of it precede the last barrier).
 //
 // Accuracy: each mass carries the error of exp2.approx (~2^-22), of the fp32
 // subtraction and scaling of its argument (about |z - max| * c * 2^-24 in the
 // exponent) and of the fp32 normalisation -- around 1e-6 relative at most for
-// the elements that carry mass.  Accept decisions can therefore differ from an
+// the elements that carry mass; sums of four add at most 3 * 2^-24 relative,
+// and the row totals are compensated.  Accept decisions can therefore differ from an
 // fp64 softmax only when |u*q - p| is within ~1e-5 of p, and drawn tokens only
 // when u*R lies within ~2e-6 (in units of normalised mass) of a boundary.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "sv_device.cuh"
 
 namespace sv {
 
 constexpr int kLgWarps = 8;
+constexpr int kLgMaxCluster = 8;  // portable cluster size
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr int kLgThreads = kLgWarps * 32;
 
@@ -52,6 +68,7 @@ struct LogitsParams {
     uint32_t *status;
     float2 *seg;        // workspace [B][nseg]
     float2 *blk;        // workspace [B][nseg][8]
+    int32_t csize;      // CTAs per sequence (the cluster size)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -66,23 +83,36 @@ __device__ __forceinline__ float warp_e(float z, float m, float c) {
     return ex2(__fmul_rn(__fsub_rn(z, m), c));
 }
 
-// Running (max, sum of exp) of one row, per lane.
+// Sum of four fp32 masses in one fixed order (the same everywhere in this
+// file, so the element step of the draw reproduces the block sums).
+__device__ __forceinline__ float sum4(float4 m) {
+    return __fadd_rn(__fadd_rn(m.x, m.y), __fadd_rn(m.z, m.w));
+}
+
+// Running (max, sum of exp) of one row, per lane: the sum is compensated
+// (Kahan), s.hi the running sum and s.lo the compensation.
 struct Online {
     float m = kNegInf;
     dd s = {0.f, 0.f};
     __device__ void add4(float4 x, float c) {
         const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+        if (mx == kNegInf) return;  // padding only
         if (mx > m) {
             if (s.hi != 0.f) {
                 const float f = warp_e(m, mx, c);
-                s = fast_two_sum(__fmul_rn(s.hi, f), __fmul_rn(s.lo, f));
+                s = dd{__fmul_rn(s.hi, f), __fmul_rn(s.lo, f)};
             }
             m = mx;
         }
-        const float4 e = make_float4(warp_e(x.x, m, c), warp_e(x.y, m, c), warp_e(x.z, m, c),
-                                     warp_e(x.w, m, c));
-        s = dd_add(s, quad_mass<false>(e, make_float4(0.f, 0.f, 0.f, 0.f)));
+        const float q = sum4(make_float4(warp_e(x.x, m, c), warp_e(x.y, m, c), warp_e(x.z, m, c),
+                                         warp_e(x.w, m, c)));
+        const float y = __fsub_rn(q, s.lo);
+        const float t = __fadd_rn(s.hi, y);
+        s.lo = __fsub_rn(__fsub_rn(t, s.hi), y);
+        s.hi = t;
     }
+    // the lane's sum as a double-fp32 value (s.hi - s.lo, exactly split)
+    __device__ dd total() const { return two_sum(s.hi, -s.lo); }
     // merges another (max, sum) into this one
     __device__ void merge(float m2, dd s2, float c) {
         if (m2 == kNegInf) return;
@@ -118,8 +148,11 @@ struct RowNorm {
     dd s;
 };
 
+// CTA-wide (max, sum) of two rows' lane states, combined in warp order.
 __device__ void cta_norms(Online a, Online b, RowNorm &na, RowNorm &nb, float c, int warp,
                           int lane, RowNorm (*sh)[kLgWarps]) {
+    a.s = a.total();
+    b.s = b.total();
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
         const float ma = __shfl_xor_sync(0xffffffffu, a.m, d);
@@ -148,22 +181,51 @@ __device__ __forceinline__ bool lg_vec(const LogitsParams &L) {
     return aligned16(L.zp) && aligned16(L.zq) && (L.ps & 3) == 0 && (L.qs & 3) == 0;
 }
 
-// Online normalisers of row pair (a, b) (b may be null).
-__device__ void row_norms(const float *a, const float *b, const LogitsParams &L, bool vec, int warp,
-                          int lane, RowNorm &na, RowNorm &nb, RowNorm (*sh)[kLgWarps]) {
+// This CTA's (max, sum) of its segments of row pair (a, b) (b may be null).
+__device__ void row_norms(const float *a, const float *b, const LogitsParams &L, bool vec, int rank,
+                          int warp, int lane, RowNorm &na, RowNorm &nb, RowNorm (*sh)[kLgWarps]) {
     Online oa, ob;
-    for (int s = warp; s < L.nseg; s += kLgWarps) {
+    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+    for (int s = rank * kLgWarps + warp; s < L.nseg; s += L.csize * kLgWarps) {
         const int64_t base = (int64_t)s * kSeg;
         const int64_t end = min(L.V, base + kSeg);
-#pragma unroll 4
+        float4 xa[kVecPerLane], xb[kVecPerLane];  // every load of the segment first
+#pragma unroll
         for (int k = 0; k < kVecPerLane; ++k) {
             const int64_t e = base + 4 * (lane + 32 * k);
-            if (e >= end) break;
-            oa.add4(load4(a, e, end, vec), L.c);
-            if (b) ob.add4(load4(b, e, end, vec), L.c);
+            xa[k] = e < end ? load4(a, e, end, vec) : none;
+            xb[k] = (b && e < end) ? load4(b, e, end, vec) : none;
+        }
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
+            oa.add4(xa[k], L.c);
+            if (b) ob.add4(xb[k], L.c);
         }
     }
     cta_norms(oa, ob, na, nb, L.c, warp, lane, sh);
+}
+
+// The cluster's normalisers: each CTA publishes its pair in slot[parity],
+// one cluster barrier, then every CTA combines all of them in rank order.
+__device__ void cluster_norms(RowNorm &na, RowNorm &nb, RowNorm (*slot)[2], int parity,
+                              float c) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    if (threadIdx.x == 0) {
+        slot[parity][0] = na;
+        slot[parity][1] = nb;
+    }
+    cl.sync();
+    Online x, y;
+    const int C = (int)cl.num_blocks();
+    for (int r = 0; r < C; ++r) {
+        const RowNorm *o = cl.map_shared_rank(&slot[parity][0], r);
+        const RowNorm pa = o[0], pb = o[1];
+        x.merge(pa.m, pa.s, c);
+        y.merge(pb.m, pb.s, c);
+    }
+    na = RowNorm{x.m, x.s};
+    nb = RowNorm{y.m, y.s};
 }
 
 // Mass of one element: the residual max(0, p - q) of the warped rows, or p
@@ -187,19 +249,25 @@ __device__ void mass_sums(const float *a, const float *b, const LogitsParams &L,
         const int64_t base = (int64_t)s * kSeg;
         const int64_t end = min(L.V, base + kSeg);
         dd v[kBlocks];
+        float4 xa[kBlocks], xb[kBlocks];  // every load of the segment first
+#pragma unroll
+        for (int k = 0; k < kBlocks; ++k) {
+            const int64_t e = base + 4 * (lane + 32 * k);
+            xa[k] = e < end ? load4(a, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xb[k] = (b && e < end) ? load4(b, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
         for (int k = 0; k < kBlocks; ++k) {
             const int64_t e = base + 4 * (lane + 32 * k);
             float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
             if (e < end) {
-                const float4 x = load4(a, e, end, vec);
-                const float4 y = b ? load4(b, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 x = xa[k], y = xb[k];
                 m.x = lg_mass(x.x, y.x, b, na, nb, ia, ib, L.c);
                 m.y = e + 1 < end ? lg_mass(x.y, y.y, b, na, nb, ia, ib, L.c) : 0.f;
                 m.z = e + 2 < end ? lg_mass(x.z, y.z, b, na, nb, ia, ib, L.c) : 0.f;
                 m.w = e + 3 < end ? lg_mass(x.w, y.w, b, na, nb, ia, ib, L.c) : 0.f;
             }
-            v[k] = quad_mass<false>(m, make_float4(0.f, 0.f, 0.f, 0.f));
+            v[k] = dd{sum4(m), 0.f};
         }
         store_sums(seg, blk, s, v, lane);
     }
@@ -221,8 +289,7 @@ __device__ int lg_search_block(const float *a, const float *b, int64_t base, int
             if (mh[j] != 0.f) last_nz = (int)(e0 - base) + j;
         }
     }
-    const dd mine = quad_mass<false>(make_float4(mh[0], mh[1], mh[2], mh[3]),
-                                     make_float4(0.f, 0.f, 0.f, 0.f));
+    const dd mine = {sum4(make_float4(mh[0], mh[1], mh[2], mh[3])), 0.f};
     const dd inc = warp_incl_scan(mine, lane);
     const unsigned msk = __ballot_sync(0xffffffffu, mine.hi != 0.f && dd_gt(dd_add(prefix, inc), T));
     if (msk) {
@@ -252,11 +319,15 @@ __device__ int lg_search_block(const float *a, const float *b, int64_t base, int
 }
 
 __global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const LogitsParams L) {
+    namespace cg = cooperative_groups;
     __shared__ RowNorm sh[2][kLgWarps];
+    __shared__ RowNorm slot[2][2];  // this CTA's (p, q) normaliser pair, by row parity
     __shared__ int sh_tok[kMaxK];
     __shared__ float sh_u[kMaxK];
     __shared__ int sh_bad;
-    const int b = blockIdx.x;
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int b = blockIdx.x / L.csize;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool vec = lg_vec(L);
     if (threadIdx.x == 0) sh_bad = 0;
@@ -268,20 +339,22 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const Logi
         if (x < 0 || (int64_t)x >= L.V) atomicOr(&sh_bad, 1);
     }
     __syncthreads();
-    if (sh_bad) {
-        if (threadIdx.x == 0) {
+    if (sh_bad) {  // the same verdict in every CTA of the cluster: nobody waits
+        if (rank == 0 && threadIdx.x == 0) {
             atomicOr(L.status, kStatusBadToken);
             L.n_out[b] = 0;
             L.next_out[b] = -1;
         }
         return;
     }
-    int n = L.K;
+    int n = L.K, parity = 0;
     RowNorm np, nq;
     for (int i = 0; i < L.K; ++i) {
         const float *a = L.zp + ((int64_t)b * (L.K + 1) + i) * L.ps;
         const float *c = L.zq + ((int64_t)b * L.K + i) * L.qs;
-        row_norms(a, c, L, vec, warp, lane, np, nq, sh);
+        row_norms(a, c, L, vec, rank, warp, lane, np, nq, sh);
+        cluster_norms(np, nq, slot, parity, L.c);
+        parity ^= 1;
         const int x = sh_tok[i];
         const float pt = __fmul_rn(warp_e(__ldg(a + x), np.m, L.c), __frcp_rn(np.s.hi));
         const float qt = __fmul_rn(warp_e(__ldg(c + x), nq.m, L.c), __frcp_rn(nq.s.hi));
@@ -292,13 +365,15 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const Logi
     }
     const float *a = L.zp + ((int64_t)b * (L.K + 1) + n) * L.ps;
     const float *c = n < L.K ? L.zq + ((int64_t)b * L.K + n) * L.qs : nullptr;
-    if (n == L.K) row_norms(a, nullptr, L, vec, warp, lane, np, nq, sh);
+    if (n == L.K) {
+        row_norms(a, nullptr, L, vec, rank, warp, lane, np, nq, sh);
+        cluster_norms(np, nq, slot, parity, L.c);
+    }
     const float ia = __frcp_rn(np.s.hi), ib = c ? __frcp_rn(nq.s.hi) : 0.f;
-    mass_sums(a, c, L, b, vec, np, nq, ia, ib, warp, kLgWarps, lane);
-    __threadfence_block();
-    __syncthreads();
-    if (warp != 0) return;
-    // the draw, by warp 0
+    mass_sums(a, c, L, b, vec, np, nq, ia, ib, rank * kLgWarps + warp, L.csize * kLgWarps, lane);
+    cl.sync();  // every segment's sums are in the workspace (release / acquire)
+    if (rank != 0 || warp != 0) return;
+    // the draw, by warp 0 of CTA 0
     DrawInputs in = {};
     in.u = split_uniform(L.u_res[b]);
     const float2 *seg = L.seg + (int64_t)b * L.nseg;
@@ -311,7 +386,7 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const Logi
     if (next < 0 && c) {
         // p_n == q_n: the residual has no mass; draw from p_n (the probability
         // path's fallback)
-        mass_sums(a, nullptr, L, b, vec, np, nq, ia, ib, 0, 1, lane);  // warp 0 alone
+        mass_sums(a, nullptr, L, b, vec, np, nq, ia, ib, 0, 1, lane);  // this warp alone
         __threadfence_block();
         __syncwarp();
         next = draw_core(L.nseg, L.V, seg, blk, nullptr, nullptr, in, lane,
