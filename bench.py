@@ -420,6 +420,7 @@ def main(argv=None):
     torch.cuda.synchronize(dev)
     status = ws.status(stream)
     kernels_per_step = sv.last_kernel_count()
+    grid_ctas = int(sv.last_grid_size())     # of the timed launches (the e2e leg may differ)
 
     # algorithmic bytes per launch, from each set's n_accepted
     req, dense, nhist = [], [], np.zeros(K + 1, dtype=np.int64)
@@ -528,7 +529,7 @@ def main(argv=None):
                        f" required bytes per rotation = {len(sets) * req_per_launch / l2:.1f}x "
                        f"L2 ({l2 / 1e6:.0f} MB)"),
                 "launch": "cuda graph" if graph is not None else "one C-ABI call per step",
-                "grid_ctas": int(sv.last_grid_size())}),
+                "grid_ctas": grid_ctas}),
             "seq_rounds_per_s": rounds_per_s * B,
             "achieved_gbs": achieved * world,
             "required_bytes_per_round": req_per_launch,
