@@ -50,13 +50,18 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
 }
 
 // Workspace layout:
-// [status, queue, exit | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] |
-//  seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2]], every region
-// 256-byte aligned; everything before seg must start at zero (and every call
-// leaves it so).
+// [header | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] | arrive[B] |
+//  groups[B][K+2] | seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2] |
+//  fnorm[B][2]], every region 256-byte aligned; everything before seg must start
+// at zero (and every call leaves it so).  Header: status (u32 at 0), the
+// chunk queue and its exit count (u32 at 4 and 8), the logits path's task
+// counter and appended groups (u64 at 16 and 24), finished sequences and
+// exited workers (u32 at 32 and 36).
 struct Layout {
-    size_t status, queue, miss, nstate, done, ptok, best, seg, blk, udd, norm, total;
+    size_t status, queue, miss, nstate, done, ptok, best, arrive, groups, seg, blk, udd, norm,
+        fnorm, total;
 };
+constexpr size_t kLgHead = 16, kLgTail = 24, kLgDone = 32, kLgExit = 36;
 
 Layout layout(int32_t B, int32_t K, int64_t V) {
     Layout L;
@@ -74,6 +79,10 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     off += round_up((size_t)B * (size_t)K * sizeof(float));
     L.best = off;
     off += round_up((size_t)B * (size_t)(K + 1) * sizeof(unsigned long long));
+    L.arrive = off;
+    off += round_up((size_t)B * sizeof(int32_t));
+    L.groups = off;
+    off += round_up((size_t)B * (size_t)(K + 2) * sizeof(unsigned long long));
     L.seg = off;
     off += round_up((size_t)B * (size_t)num_segments(V) * sizeof(float2));
     L.blk = off;
@@ -82,6 +91,8 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     off += round_up((size_t)B * sizeof(float2));
     L.norm = off;
     off += round_up((size_t)B * (size_t)K * 2 * sizeof(float2));
+    L.fnorm = off;
+    off += round_up((size_t)B * 2 * sizeof(float4));
     L.total = off;
     return L;
 }
@@ -162,6 +173,38 @@ bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *item_occ) {
     *occ = d.occupancy[rule] > 0 ? d.occupancy[rule] : 1;
     *tma_occ = d.tma_occupancy[rule];
     *item_occ = d.item_occupancy[rule];
+    return true;
+}
+
+// SM count and the residency of the two logits kernels on the current device.
+bool logits_info(int *sms, int *task_occ, int *ring_occ) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(g_info_mu);
+    static int cached_sms[64], cached_task[64], cached_ring[64];
+    if (cached_sms[dev] == 0) {
+        int n = 0, o = 0, r = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return false;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv::logits_task_kernel,
+                                                          sv::kLgThreads, 0) != cudaSuccess ||
+            o <= 0)
+            return false;
+        if (cudaFuncSetAttribute(sv::logits_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 sv::kLgRingSmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, sv::logits_ring_kernel,
+                                                          sv::kLgRingThreads,
+                                                          sv::kLgRingSmemBytes) != cudaSuccess) {
+            cudaGetLastError();
+            r = 0;
+        }
+        cached_task[dev] = o;
+        cached_ring[dev] = r;
+        cached_sms[dev] = n;
+    }
+    *sms = cached_sms[dev];
+    *task_occ = cached_task[dev];
+    *ring_occ = cached_ring[dev];
     return true;
 }
 
@@ -521,6 +564,8 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
     if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
+    const Layout W = layout(B, K, V);
+    char *ws = static_cast<char *>(workspace);
     sv::LogitsParams L{};
     L.zp = P.p;
     L.ps = P.ps;
@@ -539,24 +584,30 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     L.status = P.status;
     L.seg = P.seg;
     L.blk = P.blk;
-    // one cluster of up to 8 CTAs per sequence, never more CTAs than segments
-    L.csize = (int32_t)std::min<int64_t>(sv::kLgMaxCluster, std::max<int64_t>(1, L.nseg));
-    if ((int64_t)B * L.csize > INT32_MAX) return SV_EINVAL;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * L.csize));
-    cfg.blockDim = dim3(sv::kLgThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)L.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    g_last_grid = (int64_t)B * L.csize;
+    L.fnorm = reinterpret_cast<float4 *>(ws + W.fnorm);
+    L.grp = reinterpret_cast<unsigned long long *>(ws + W.groups);
+    L.arrive = reinterpret_cast<int32_t *>(ws + W.arrive);
+    L.head = reinterpret_cast<unsigned long long *>(ws + kLgHead);
+    L.tail = reinterpret_cast<unsigned long long *>(ws + kLgTail);
+    L.ndone = reinterpret_cast<uint32_t *>(ws + kLgDone);
+    L.nexit = reinterpret_cast<uint32_t *>(ws + kLgExit);
+    L.ngroups = (int64_t)B * (K + 2);
+    // one persistent grid of as many CTAs as the SMs hold: bulk-copy workers
+    // for 16-byte-aligned device rows, plain-load workers otherwise
+    int sms = 0, task_occ = 0, ring_occ = 0;
+    if (!logits_info(&sms, &task_occ, &ring_occ)) return SV_ECUDA;
+    const bool ring = ring_occ > 0 && !P.rows_on_host && aligned_rows(P.p, P.ps) &&
+                      (K == 0 || aligned_rows(P.q, P.qs));
+    const int occ = ring ? ring_occ : task_occ;
+    const int32_t forced = g_ctas_per_sm.load();
+    const unsigned grid = (unsigned)sms * (unsigned)(forced > 0 ? std::min(forced, occ) : occ);
+    g_last_grid = grid;
     g_last_kernels = 1;
-    return cudaLaunchKernelEx(&cfg, sv::logits_sample_kernel, L) == cudaSuccess ? SV_OK : SV_ECUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (ring)
+        return launch_dependent(sv::logits_ring_kernel, grid, sv::kLgRingThreads,
+                                sv::kLgRingSmemBytes, L, st);
+    return launch_dependent(sv::logits_task_kernel, grid, sv::kLgThreads, 0, L, st);
 }
 
 int sv_get_status(void *workspace, sv_stream_t stream, uint32_t *flags) {

@@ -8,48 +8,54 @@
 // argmax p_i = argmax zp_i, and the greedy entry point takes logits as they
 // are.)
 //
-// One thread-block cluster of up to 8 CTAs per sequence walks its rows in
-// order; CTA r of the cluster streams segments r*8 + w, r*8 + w + 8*C, ... (w
-// its warp, C the cluster size).  For position i each CTA streams its share of
-// the row pair (zp_i, zq_i) once, keeping per lane an online maximum and a
-// compensated (Kahan) fp32 sum of exp2((z - max) * c), c = log2(e) / tau.  The CTA writes
-// its (max, sum) pair into a shared slot (two slots, alternating by row), one
-// cluster barrier follows, and every CTA combines all C slots in rank order
-// through distributed shared memory -- so every CTA holds bit-identical
-// normalisers and reaches the same accept decision u * q_i(t_i) < p_i(t_i)
-// (made on the recomputed gathers).  After the first rejection the cluster
-// streams that row pair a second time, forming r = max(0, p - q) per element
-// in fp32 and, from fp32 sums of four, the double-fp32 block and segment sums
-// of r in the workspace;
-// when all K are accepted it streams zp_K twice (normaliser, then the masses
-// of p_K).  After a last cluster barrier CTA 0 draws: the same segment ->
-// block -> element search as the probability path, its element step
-// recomputing the masses with the same instructions.
-//
-// Every CTA of a cluster makes the same sequence of barrier calls: the
-// decisions between them depend only on values every CTA computes identically,
-// and no CTA leaves while another may still read its shared memory (the last
-// reads of it precede the last barrier).
+// One persistent launch in which every warp is a worker.  Work comes in
+// groups, one per (sequence b, position i, kind), each group one task per
+// 1024-element segment of the row:
+//   norm(b, i), i < K  the normalisers of the row pair (zp_i, zq_i): the task
+//                      streams its segment of both rows once and stores, per
+//                      row, the segment's maximum M and the double-fp32 sum of
+//                      exp2((z - M) * c), c = log2(e) / tau (fp32 sums of four,
+//                      then a fixed tree and a butterfly over the lanes);
+//   norm(b, K)         the same on the bonus row zp_K alone;
+//   mass(b, n)         the masses r = max(0, p_n - q_n) (or p_K) of the chosen
+//                      row (pair), formed in fp32 from the normalisers, summed
+//                      in fours and stored as double-fp32 block and segment
+//                      sums.
+// One queue counter hands tasks out in order.  The first B groups are
+// norm(b, 0); every later group is appended by the worker that finishes the
+// last task of the sequence's previous group (an arrival counter per
+// sequence).  That worker merges the segment pairs in segment order -- so the
+// normalisers do not depend on which worker ran which task -- and decides:
+// after norm(b, i) it makes the accept test u * q_i(t_i) < p_i(t_i) on the
+// gathered logits and appends norm(b, i + 1) on acceptance, else mass(b, i);
+// after norm(b, K) it appends mass(b, K); after mass(b, n) it draws with the
+// same segment -> block -> element search as the probability path, its
+// element step recomputing the masses with the same instructions.  A
+// sequence's groups run one after another while other sequences' groups fill
+// the machine.  The only wait is that of a worker whose next task belongs to
+// a group not yet appended; it is bounded (kStatusTimeout) and ends once every
+// sequence has its token.
 //
 // Accuracy: each mass carries the error of exp2.approx (~2^-22), of the fp32
 // subtraction and scaling of its argument (about |z - max| * c * 2^-24 in the
 // exponent) and of the fp32 normalisation -- around 1e-6 relative at most for
-// the elements that carry mass; sums of four add at most 3 * 2^-24 relative,
-// and the row totals are compensated.  Accept decisions can therefore differ from an
-// fp64 softmax only when |u*q - p| is within ~1e-5 of p, and drawn tokens only
-// when u*R lies within ~2e-6 (in units of normalised mass) of a boundary.
+// the elements that carry mass; the fp32 sums within a lane (four masses, or a
+// lane's 32 normaliser terms) add at most 3 * 2^-24 and 5 * 2^-24 relative,
+// and everything above them is summed in double-fp32.  Accept decisions can therefore differ
+// from an fp64 softmax only when |u*q - p| is within ~1e-5 of p, and drawn
+// tokens only when u*R lies within ~2e-6 (in units of normalised mass) of a
+// boundary.
 #pragma once
 
-#include <cooperative_groups.h>
-
 #include "sv_device.cuh"
+#include "sv_tma.cuh"
 
 namespace sv {
 
 constexpr int kLgWarps = 8;
-constexpr int kLgMaxCluster = 8;  // portable cluster size
-constexpr float kNegInf = -__builtin_huge_valf();
 constexpr int kLgThreads = kLgWarps * 32;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr uint32_t kLgNorm = 1u, kLgMass = 2u;  // group kinds
 
 struct LogitsParams {
     const float *zp;
@@ -66,9 +72,18 @@ struct LogitsParams {
     int32_t *n_out;
     int32_t *next_out;
     uint32_t *status;
-    float2 *seg;        // workspace [B][nseg]
-    float2 *blk;        // workspace [B][nseg][8]
-    int32_t csize;      // CTAs per sequence (the cluster size)
+    float2 *seg;        // workspace [B][nseg] segment sums of the mass pass
+    float2 *blk;        // workspace [B][nseg][8] block sums of the mass pass; before a
+                        // sequence's mass pass the first half of its rows holds the
+                        // norm tasks' (max, sum) pairs, two float4 per segment
+    float4 *fnorm;      // workspace [B][2] normalisers of the chosen row (pair)
+    unsigned long long *grp;    // workspace [B * (K + 2)] groups (0 = not appended)
+    int32_t *arrive;    // workspace [B] finished tasks of the sequence's current group
+    unsigned long long *head;   // next task to hand out
+    unsigned long long *tail;   // groups appended after the first B
+    uint32_t *ndone;    // sequences finished
+    uint32_t *nexit;    // workers that left
+    int64_t ngroups;    // B * (K + 2): a sequence appends at most K + 1 groups
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -89,30 +104,11 @@ __device__ __forceinline__ float sum4(float4 m) {
     return __fadd_rn(__fadd_rn(m.x, m.y), __fadd_rn(m.z, m.w));
 }
 
-// Running (max, sum of exp) of one row, per lane: the sum is compensated
-// (Kahan), s.hi the running sum and s.lo the compensation.
+// A running (max, sum of exp2((z - max) * c)) pair of a row, merged from
+// per-segment pairs.
 struct Online {
     float m = kNegInf;
     dd s = {0.f, 0.f};
-    __device__ void add4(float4 x, float c) {
-        const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-        if (mx == kNegInf) return;  // padding only
-        if (mx > m) {
-            if (s.hi != 0.f) {
-                const float f = warp_e(m, mx, c);
-                s = dd{__fmul_rn(s.hi, f), __fmul_rn(s.lo, f)};
-            }
-            m = mx;
-        }
-        const float q = sum4(make_float4(warp_e(x.x, m, c), warp_e(x.y, m, c), warp_e(x.z, m, c),
-                                         warp_e(x.w, m, c)));
-        const float y = __fsub_rn(q, s.lo);
-        const float t = __fadd_rn(s.hi, y);
-        s.lo = __fsub_rn(__fsub_rn(t, s.hi), y);
-        s.hi = t;
-    }
-    // the lane's sum as a double-fp32 value (s.hi - s.lo, exactly split)
-    __device__ dd total() const { return two_sum(s.hi, -s.lo); }
     // merges another (max, sum) into this one
     __device__ void merge(float m2, dd s2, float c) {
         if (m2 == kNegInf) return;
@@ -128,9 +124,21 @@ struct Online {
         m = M;
         s = dd_add(a, b);
     }
+    // merges the lanes' states in a fixed butterfly and gives every lane the
+    // result lane 0 holds
+    __device__ void warp_merge(float c) {
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
+            const dd s2 = shfl_xor_dd(s, d);
+            merge(m2, s2, c);
+        }
+        m = __shfl_sync(0xffffffffu, m, 0);
+        s = shfl_dd(s, 0);
+    }
 };
 
-// Loads element e of a row (or 0-padding past n), vectorised when possible.
+// Loads element e of a row (or -inf padding past end), vectorised when possible.
 __device__ __forceinline__ float4 load4(const float *row, int64_t e, int64_t end, bool vec) {
     if (vec && e + 3 < end) return ld_stream4(row + e);
     float4 x;
@@ -142,94 +150,46 @@ __device__ __forceinline__ float4 load4(const float *row, int64_t e, int64_t end
     return x;
 }
 
-// CTA-wide (max, sum) of one or two rows' lane states.
+// A row's normalisers: the maximum logit and the sum of exp2((z - m) * c).
 struct RowNorm {
     float m;
     dd s;
 };
 
-// CTA-wide (max, sum) of two rows' lane states, combined in warp order.
-__device__ void cta_norms(Online a, Online b, RowNorm &na, RowNorm &nb, float c, int warp,
-                          int lane, RowNorm (*sh)[kLgWarps]) {
-    a.s = a.total();
-    b.s = b.total();
+// Normalisers of one 1024-element segment of a row held as eight float4 per
+// lane (lane l: elements 4 * (l + 32k) .. + 3, -inf past the row's end): the
+// segment's maximum M (warp-wide first, so every term below is independent)
+// and S = sum exp2((z - M) * c) -- a fixed fp32 tree over the lane's 32 terms
+// (at most 5 * 2^-24 relative error), then a double-fp32 butterfly over the
+// lanes (dd_add is commutative, so every lane ends with the same bits).
+__device__ __forceinline__ RowNorm seg_norm(const float4 (&x)[kVecPerLane], float c) {
+    float mx = kNegInf;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-        const float ma = __shfl_xor_sync(0xffffffffu, a.m, d);
-        const dd sa = shfl_xor_dd(a.s, d);
-        a.merge(ma, sa, c);
-        const float mb = __shfl_xor_sync(0xffffffffu, b.m, d);
-        const dd sb = shfl_xor_dd(b.s, d);
-        b.merge(mb, sb, c);
-    }
-    if (lane == 0) {
-        sh[0][warp] = RowNorm{a.m, a.s};
-        sh[1][warp] = RowNorm{b.m, b.s};
-    }
-    __syncthreads();
-    Online x, y;
-    for (int w = 0; w < kLgWarps; ++w) {
-        x.merge(sh[0][w].m, sh[0][w].s, c);
-        y.merge(sh[1][w].m, sh[1][w].s, c);
-    }
-    na = RowNorm{x.m, x.s};
-    nb = RowNorm{y.m, y.s};
-    __syncthreads();  // sh is reused by the next row
+    for (int k = 0; k < kVecPerLane; ++k)
+        mx = fmaxf(mx, fmaxf(fmaxf(x[k].x, x[k].y), fmaxf(x[k].z, x[k].w)));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    if (mx == kNegInf) return RowNorm{kNegInf, {0.f, 0.f}};  // padding only (warp-uniform)
+    float g[kVecPerLane];
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k)
+        g[k] = sum4(make_float4(warp_e(x[k].x, mx, c), warp_e(x[k].y, mx, c),
+                                warp_e(x[k].z, mx, c), warp_e(x[k].w, mx, c)));
+    static_assert(kVecPerLane == 8, "the lane sum below is a tree over eight");
+    dd t = {__fadd_rn(__fadd_rn(__fadd_rn(g[0], g[1]), __fadd_rn(g[2], g[3])),
+                      __fadd_rn(__fadd_rn(g[4], g[5]), __fadd_rn(g[6], g[7]))),
+            0.f};
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) t = dd_add(t, shfl_xor_dd(t, d));
+    return RowNorm{mx, t};
 }
 
 __device__ __forceinline__ bool lg_vec(const LogitsParams &L) {
     return aligned16(L.zp) && aligned16(L.zq) && (L.ps & 3) == 0 && (L.qs & 3) == 0;
 }
 
-// This CTA's (max, sum) of its segments of row pair (a, b) (b may be null).
-__device__ void row_norms(const float *a, const float *b, const LogitsParams &L, bool vec, int rank,
-                          int warp, int lane, RowNorm &na, RowNorm &nb, RowNorm (*sh)[kLgWarps]) {
-    Online oa, ob;
-    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-    for (int s = rank * kLgWarps + warp; s < L.nseg; s += L.csize * kLgWarps) {
-        const int64_t base = (int64_t)s * kSeg;
-        const int64_t end = min(L.V, base + kSeg);
-        float4 xa[kVecPerLane], xb[kVecPerLane];  // every load of the segment first
-#pragma unroll
-        for (int k = 0; k < kVecPerLane; ++k) {
-            const int64_t e = base + 4 * (lane + 32 * k);
-            xa[k] = e < end ? load4(a, e, end, vec) : none;
-            xb[k] = (b && e < end) ? load4(b, e, end, vec) : none;
-        }
-#pragma unroll
-        for (int k = 0; k < kVecPerLane; ++k) {
-            oa.add4(xa[k], L.c);
-            if (b) ob.add4(xb[k], L.c);
-        }
-    }
-    cta_norms(oa, ob, na, nb, L.c, warp, lane, sh);
-}
-
-// The cluster's normalisers: each CTA publishes its pair in slot[parity],
-// one cluster barrier, then every CTA combines all of them in rank order.
-__device__ void cluster_norms(RowNorm &na, RowNorm &nb, RowNorm (*slot)[2], int parity,
-                              float c) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    if (threadIdx.x == 0) {
-        slot[parity][0] = na;
-        slot[parity][1] = nb;
-    }
-    cl.sync();
-    Online x, y;
-    const int C = (int)cl.num_blocks();
-    for (int r = 0; r < C; ++r) {
-        const RowNorm *o = cl.map_shared_rank(&slot[parity][0], r);
-        const RowNorm pa = o[0], pb = o[1];
-        x.merge(pa.m, pa.s, c);
-        y.merge(pb.m, pb.s, c);
-    }
-    na = RowNorm{x.m, x.s};
-    nb = RowNorm{y.m, y.s};
-}
-
 // Mass of one element: the residual max(0, p - q) of the warped rows, or p
-// alone (b == null), with 1/S rounded once to fp32.
+// alone (pair false), with 1/S rounded once to fp32.
 __device__ __forceinline__ float lg_mass(float za, float zb, bool pair, const RowNorm &na,
                                          const RowNorm &nb, float ia, float ib, float c) {
     const float pa = __fmul_rn(warp_e(za, na.m, c), ia);
@@ -238,39 +198,34 @@ __device__ __forceinline__ float lg_mass(float za, float zb, bool pair, const Ro
     return fmaxf(__fsub_rn(pa, qb), 0.f);
 }
 
-// Streams the masses of a row (pair) into segment and block sums of sequence
-// bseq; warp w of `warps` takes segments w, w + warps, ...
-__device__ void mass_sums(const float *a, const float *b, const LogitsParams &L, int bseq, bool vec,
-                          const RowNorm &na, const RowNorm &nb, float ia, float ib, int warp,
-                          int warps, int lane) {
-    float2 *seg = L.seg + (int64_t)bseq * L.nseg;
-    float2 *blk = L.blk + (int64_t)bseq * L.nseg * kBlocks;
-    for (int s = warp; s < L.nseg; s += warps) {
-        const int64_t base = (int64_t)s * kSeg;
-        const int64_t end = min(L.V, base + kSeg);
-        dd v[kBlocks];
-        float4 xa[kBlocks], xb[kBlocks];  // every load of the segment first
+// Masses of segment s of a row (pair) into its segment and block sums (one warp).
+__device__ void lg_mass_segment(const float *a, const float *b, const LogitsParams &L, float2 *seg,
+                                float2 *blk, int64_t s, bool vec, const RowNorm &na,
+                                const RowNorm &nb, float ia, float ib, int lane) {
+    const int64_t base = s * kSeg;
+    const int64_t end = min(L.V, base + kSeg);
+    dd v[kBlocks];
+    float4 xa[kBlocks], xb[kBlocks];  // every load of the segment first
 #pragma unroll
-        for (int k = 0; k < kBlocks; ++k) {
-            const int64_t e = base + 4 * (lane + 32 * k);
-            xa[k] = e < end ? load4(a, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
-            xb[k] = (b && e < end) ? load4(b, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < kBlocks; ++k) {
-            const int64_t e = base + 4 * (lane + 32 * k);
-            float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < end) {
-                const float4 x = xa[k], y = xb[k];
-                m.x = lg_mass(x.x, y.x, b, na, nb, ia, ib, L.c);
-                m.y = e + 1 < end ? lg_mass(x.y, y.y, b, na, nb, ia, ib, L.c) : 0.f;
-                m.z = e + 2 < end ? lg_mass(x.z, y.z, b, na, nb, ia, ib, L.c) : 0.f;
-                m.w = e + 3 < end ? lg_mass(x.w, y.w, b, na, nb, ia, ib, L.c) : 0.f;
-            }
-            v[k] = dd{sum4(m), 0.f};
-        }
-        store_sums(seg, blk, s, v, lane);
+    for (int k = 0; k < kBlocks; ++k) {
+        const int64_t e = base + 4 * (lane + 32 * k);
+        xa[k] = e < end ? load4(a, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xb[k] = (b && e < end) ? load4(b, e, end, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int k = 0; k < kBlocks; ++k) {
+        const int64_t e = base + 4 * (lane + 32 * k);
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < end) {
+            const float4 x = xa[k], y = xb[k];
+            m.x = lg_mass(x.x, y.x, b, na, nb, ia, ib, L.c);
+            m.y = e + 1 < end ? lg_mass(x.y, y.y, b, na, nb, ia, ib, L.c) : 0.f;
+            m.z = e + 2 < end ? lg_mass(x.z, y.z, b, na, nb, ia, ib, L.c) : 0.f;
+            m.w = e + 3 < end ? lg_mass(x.w, y.w, b, na, nb, ia, ib, L.c) : 0.f;
+        }
+        v[k] = dd{sum4(m), 0.f};
+    }
+    store_sums(seg, blk, s, v, lane);
 }
 
 // Element step of the draw on a logit row (pair): the same masses, recomputed.
@@ -318,66 +273,196 @@ __device__ int lg_search_block(const float *a, const float *b, int64_t base, int
     return last_nz < 0 ? -1 : (int)(base + last_nz);
 }
 
-__global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const LogitsParams L) {
-    namespace cg = cooperative_groups;
-    __shared__ RowNorm sh[2][kLgWarps];
-    __shared__ RowNorm slot[2][2];  // this CTA's (p, q) normaliser pair, by row parity
-    __shared__ int sh_tok[kMaxK];
-    __shared__ float sh_u[kMaxK];
-    __shared__ int sh_bad;
-    cg::cluster_group cl = cg::this_cluster();
-    const int rank = (int)cl.block_rank();
-    const int b = blockIdx.x / L.csize;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool vec = lg_vec(L);
-    if (threadIdx.x == 0) sh_bad = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < L.K; i += kLgThreads) {
-        const int32_t x = L.t[(int64_t)b * L.K + i];
-        sh_tok[i] = x;
-        sh_u[i] = L.u_acc[(int64_t)b * L.K + i];
-        if (x < 0 || (int64_t)x >= L.V) atomicOr(&sh_bad, 1);
-    }
-    __syncthreads();
-    if (sh_bad) {  // the same verdict in every CTA of the cluster: nobody waits
-        if (rank == 0 && threadIdx.x == 0) {
-            atomicOr(L.status, kStatusBadToken);
-            L.n_out[b] = 0;
-            L.next_out[b] = -1;
-        }
+// ---------------------------------------------------------------------------
+// the task queue
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Arrival of n tasks on a sequence's counter: release (the stores this thread
+// made or observed before it) and acquire (the earlier arrivals' stores) in
+// one atomic; returns the count before it.
+__device__ __forceinline__ int arrive_acq_rel(int32_t *p, int n) {
+    int v;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(v) : "l"(p), "r"(n) : "memory");
+    return v;
+}
+
+// A group: bit 63 marks it present, then kind (bits 40-41), position (32-39)
+// and sequence (0-31).
+__device__ __forceinline__ unsigned long long lg_group(int b, int i, uint32_t kind) {
+    return (1ull << 63) | ((unsigned long long)kind << 40) |
+           ((unsigned long long)(uint32_t)i << 32) | (unsigned long long)(uint32_t)b;
+}
+
+// Appends a group (one lane; its earlier stores are visible to every reader
+// of the group).
+__device__ __forceinline__ void lg_append(const LogitsParams &L, unsigned long long gdesc) {
+    const unsigned long long slot = (unsigned long long)L.B + atomicAdd(L.tail, 1ull);
+    if (slot >= (unsigned long long)L.ngroups) {  // cannot happen: at most K + 1 per sequence
+        atomicOr(L.status, kStatusOverflow);
         return;
     }
-    int n = L.K, parity = 0;
-    RowNorm np, nq;
-    for (int i = 0; i < L.K; ++i) {
-        const float *a = L.zp + ((int64_t)b * (L.K + 1) + i) * L.ps;
-        const float *c = L.zq + ((int64_t)b * L.K + i) * L.qs;
-        row_norms(a, c, L, vec, rank, warp, lane, np, nq, sh);
-        cluster_norms(np, nq, slot, parity, L.c);
-        parity ^= 1;
-        const int x = sh_tok[i];
-        const float pt = __fmul_rn(warp_e(__ldg(a + x), np.m, L.c), __frcp_rn(np.s.hi));
-        const float qt = __fmul_rn(warp_e(__ldg(c + x), nq.m, L.c), __frcp_rn(nq.s.hi));
-        if (!accepts(sh_u[i], qt, pt)) {
-            n = i;
-            break;
+    st_release(L.grp + slot, gdesc);
+}
+
+// Group g (one lane): the first B are implicit; a later one is waited for
+// until appended, or until every sequence is finished (0).
+__device__ unsigned long long lg_wait_group(const LogitsParams &L, uint64_t g) {
+    if (g < (uint64_t)L.B) return lg_group((int)g, 0, kLgNorm);
+    IdleClock clk;
+    while (true) {
+        const unsigned long long d = ld_acquire(L.grp + g);
+        if (d) return d;
+        if (ld_relaxed(L.ndone) >= (uint32_t)L.B) return 0ull;
+        if (!clk.idle(256)) {
+            atomicOr(L.status, kStatusTimeout);
+            return 0ull;
         }
     }
-    const float *a = L.zp + ((int64_t)b * (L.K + 1) + n) * L.ps;
-    const float *c = n < L.K ? L.zq + ((int64_t)b * L.K + n) * L.qs : nullptr;
-    if (n == L.K) {
-        row_norms(a, nullptr, L, vec, rank, warp, lane, np, nq, sh);
-        cluster_norms(np, nq, slot, parity, L.c);
+}
+
+// A sequence's result (one lane).
+__device__ __forceinline__ void lg_finish(const LogitsParams &L, int b, int n, int next,
+                                          uint32_t flags) {
+    if (flags) atomicOr(L.status, flags);
+    L.n_out[b] = n;
+    L.next_out[b] = next;
+    __threadfence();
+    atomicAdd(L.ndone, 1u);
+}
+
+__device__ __forceinline__ const float *lg_row_p(const LogitsParams &L, int b, int i) {
+    return L.zp + ((int64_t)b * (L.K + 1) + i) * L.ps;
+}
+
+__device__ __forceinline__ const float *lg_row_q(const LogitsParams &L, int b, int i) {
+    return i < L.K ? L.zq + ((int64_t)b * L.K + i) * L.qs : nullptr;
+}
+
+// The (max, sum) slot of segment s of sequence b: two float4, p then q.
+__device__ __forceinline__ float4 *lg_pair(const LogitsParams &L, int b, int64_t s) {
+    return reinterpret_cast<float4 *>(L.blk + (int64_t)b * L.nseg * kBlocks) + 2 * s;
+}
+
+// Stores a norm task's segment pairs (oa, ob), the same in every lane (lane 0).
+__device__ __forceinline__ void lg_store_pair(const LogitsParams &L, int b, int64_t s,
+                                              const RowNorm &oa, const RowNorm &ob) {
+    float4 *pr = lg_pair(L, b, s);
+    pr[0] = make_float4(oa.m, oa.s.hi, oa.s.lo, 0.f);
+    pr[1] = make_float4(ob.m, ob.s.hi, ob.s.lo, 0.f);
+}
+
+// `tasks` norm tasks of group g (sequence b, position i) have stored their
+// pairs: arrives for them; the group's last arrival merges every segment's
+// pair in segment order (lane l takes segments l, l + 32, ..., then a fixed
+// butterfly), makes the accept test on the gathered logits and appends the
+// sequence's next group (or finishes it on an invalid draft id).
+__device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i, uint64_t g, int tasks,
+                               int lane) {
+    const float *a = lg_row_p(L, b, i);
+    const float *c = lg_row_q(L, b, i);
+    int last = 0;
+    if (lane == 0) last = arrive_acq_rel(L.arrive + b, tasks) + tasks == L.nseg;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();  // lane 0's acquire, before every lane's reads below
+    int32_t x = -1;
+    float u = 0.f, gp = 0.f, gq = 0.f;
+    if (lane == 0) {
+        atomicExch(L.arrive + b, 0);  // the sequence's next group counts from zero
+        if (c) {
+            x = L.t[(int64_t)b * L.K + i];
+            u = L.u_acc[(int64_t)b * L.K + i];
+            if (x >= 0 && (int64_t)x < L.V) {
+                gp = __ldcg(a + x);
+                gq = __ldcg(c + x);
+            }
+        }
     }
-    const float ia = __frcp_rn(np.s.hi), ib = c ? __frcp_rn(nq.s.hi) : 0.f;
-    mass_sums(a, c, L, b, vec, np, nq, ia, ib, rank * kLgWarps + warp, L.csize * kLgWarps, lane);
-    cl.sync();  // every segment's sums are in the workspace (release / acquire)
-    if (rank != 0 || warp != 0) return;
-    // the draw, by warp 0 of CTA 0
+    Online na, nb;
+    for (int64_t k = lane; k < L.nseg; k += 32) {
+        const float4 *pr = lg_pair(L, b, k);
+        const float4 pa = __ldcg(pr);
+        na.merge(pa.x, dd{pa.y, pa.z}, L.c);
+        if (c) {
+            const float4 pb = __ldcg(pr + 1);
+            nb.merge(pb.x, dd{pb.y, pb.z}, L.c);
+        }
+    }
+    na.warp_merge(L.c);
+    if (c) nb.warp_merge(L.c);
+    bool bad = false;
+    if (c && i == 0) {  // every draft id is checked once, before the first decision
+        for (int j = lane; j < L.K; j += 32) {
+            const int32_t y = L.t[(int64_t)b * L.K + j];
+            bad |= y < 0 || (int64_t)y >= L.V;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+    }
+    if (lane != 0) return;
+    if (bad) {
+        lg_finish(L, b, 0, -1, kStatusBadToken);
+    } else if (c) {
+        const float pt = __fmul_rn(warp_e(gp, na.m, L.c), __frcp_rn(na.s.hi));
+        const float qt = __fmul_rn(warp_e(gq, nb.m, L.c), __frcp_rn(nb.s.hi));
+        if (accepts(u, qt, pt)) {
+            lg_append(L, lg_group(b, i + 1, kLgNorm));
+        } else {
+            L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
+            L.fnorm[2 * b + 1] = make_float4(nb.m, nb.s.hi, nb.s.lo, 0.f);
+            lg_append(L, lg_group(b, i, kLgMass));
+        }
+    } else {
+        L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
+        lg_append(L, lg_group(b, i, kLgMass));
+    }
+    if (g >= (uint64_t)L.B) L.grp[g] = 0ull;  // every task of the group has read it
+}
+
+// The chosen row (pair)'s normalisers, read by lane 0 (after the group's
+// publication) and given to every lane.
+__device__ __forceinline__ void lg_load_norms(const LogitsParams &L, int b, bool pair, int lane,
+                                              RowNorm &np, RowNorm &nq) {
+    float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+    if (lane == 0) {
+        f0 = __ldcg(L.fnorm + 2 * b);
+        if (pair) f1 = __ldcg(L.fnorm + 2 * b + 1);
+    }
+    np = {__shfl_sync(0xffffffffu, f0.x, 0),
+          {__shfl_sync(0xffffffffu, f0.y, 0), __shfl_sync(0xffffffffu, f0.z, 0)}};
+    nq = {__shfl_sync(0xffffffffu, f1.x, 0),
+          {__shfl_sync(0xffffffffu, f1.y, 0), __shfl_sync(0xffffffffu, f1.z, 0)}};
+}
+
+// `tasks` mass tasks of group g have stored their sums (and every lane's
+// stores are ordered before this call): arrives for them; the group's last
+// arrival draws and finishes the sequence.
+__device__ __noinline__ void lg_mass_arrive(const LogitsParams &L, int b, int n, uint64_t g, int tasks, bool vec,
+                               const RowNorm &np, const RowNorm &nq, float ia, float ib, int lane) {
+    const float *a = lg_row_p(L, b, n);
+    const float *c = lg_row_q(L, b, n);
+    float2 *seg = L.seg + (int64_t)b * L.nseg;
+    float2 *blk = L.blk + (int64_t)b * L.nseg * kBlocks;
+    int last = 0;
+    if (lane == 0) last = arrive_acq_rel(L.arrive + b, tasks) + tasks == L.nseg;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();  // lane 0's acquire, before every lane's reads below
+    if (lane == 0) atomicExch(L.arrive + b, 0);
     DrawInputs in = {};
     in.u = split_uniform(L.u_res[b]);
-    const float2 *seg = L.seg + (int64_t)b * L.nseg;
-    const float2 *blk = L.blk + (int64_t)b * L.nseg * kBlocks;
     int next = draw_core(L.nseg, L.V, seg, blk, nullptr, nullptr, in, lane,
                          [&](int64_t base, dd prefix, dd T) {
                              return lg_search_block(a, c, base, L.V, np, nq, ia, ib, L.c, prefix,
@@ -385,8 +470,9 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const Logi
                          });
     if (next < 0 && c) {
         // p_n == q_n: the residual has no mass; draw from p_n (the probability
-        // path's fallback)
-        mass_sums(a, nullptr, L, b, vec, np, nq, ia, ib, 0, 1, lane);  // this warp alone
+        // path's fallback), its sums formed by this warp alone
+        for (int64_t k = 0; k < L.nseg; ++k)
+            lg_mass_segment(a, nullptr, L, seg, blk, k, vec, np, nq, ia, ib, lane);
         __threadfence_block();
         __syncwarp();
         next = draw_core(L.nseg, L.V, seg, blk, nullptr, nullptr, in, lane,
@@ -396,9 +482,412 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_sample_kernel(const Logi
                          });
     }
     if (lane == 0) {
-        if (next < 0) atomicOr(L.status, kStatusZeroMass);
-        L.n_out[b] = n;
-        L.next_out[b] = next;
+        if (g >= (uint64_t)L.B) L.grp[g] = 0ull;
+        lg_finish(L, b, n, next, next < 0 ? kStatusZeroMass : 0u);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// plain-load workers (rows that are not 16-byte aligned, or in host memory):
+// every warp takes one segment task at a time and loads it itself
+
+__device__ void lg_norm_task(const LogitsParams &L, int b, int i, int64_t s, uint64_t g, bool vec,
+                             int lane) {
+    const float *a = lg_row_p(L, b, i);
+    const float *c = lg_row_q(L, b, i);
+    const int64_t base = s * kSeg;
+    const int64_t end = min(L.V, base + kSeg);
+    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+    float4 xa[kVecPerLane], xb[kVecPerLane];
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k) {
+        const int64_t e = base + 4 * (lane + 32 * k);
+        xa[k] = e < end ? load4(a, e, end, vec) : none;
+        xb[k] = (c && e < end) ? load4(c, e, end, vec) : none;
+    }
+    const RowNorm oa = seg_norm(xa, L.c);
+    const RowNorm ob = c ? seg_norm(xb, L.c) : RowNorm{kNegInf, {0.f, 0.f}};
+    if (lane == 0) lg_store_pair(L, b, s, oa, ob);
+    lg_norm_arrive(L, b, i, g, 1, lane);
+}
+
+__device__ void lg_mass_task(const LogitsParams &L, int b, int n, int64_t s, uint64_t g, bool vec,
+                             int lane) {
+    const float *a = lg_row_p(L, b, n);
+    const float *c = lg_row_q(L, b, n);
+    RowNorm np, nq;
+    lg_load_norms(L, b, c != nullptr, lane, np, nq);  // after lane 0's acquire of the group
+    const float ia = __frcp_rn(np.s.hi), ib = c ? __frcp_rn(nq.s.hi) : 0.f;
+    lg_mass_segment(a, c, L, L.seg + (int64_t)b * L.nseg, L.blk + (int64_t)b * L.nseg * kBlocks,
+                    s, vec, np, nq, ia, ib, lane);
+    __threadfence();  // this lane's sums, before the arrival
+    __syncwarp();
+    lg_mass_arrive(L, b, n, g, 1, vec, np, nq, ia, ib, lane);
+}
+
+__global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const LogitsParams L) {
+    const int lane = threadIdx.x & 31;
+    const bool vec = lg_vec(L);
+    const uint64_t nseg = (uint64_t)L.nseg;
+    wait_for_primary_grid();
+    unsigned long long h = 0;
+    if (lane == 0) h = atomicAdd(L.head, 1ull);
+    h = __shfl_sync(0xffffffffu, h, 0);
+    while (true) {
+        const uint64_t g = h / nseg;
+        if (g >= (uint64_t)L.ngroups) break;
+        unsigned long long d = 0;
+        if (lane == 0) d = lg_wait_group(L, g);
+        d = __shfl_sync(0xffffffffu, d, 0);
+        if (!d) break;
+        // the next task is claimed now: its number is needed only after this one
+        unsigned long long hn = 0;
+        if (lane == 0) hn = atomicAdd(L.head, 1ull);
+        const int b = (int)(uint32_t)d;
+        const int i = (int)((d >> 32) & 0xffu);
+        const int64_t s = (int64_t)(h % nseg);
+        if (((d >> 40) & 3u) == kLgNorm)
+            lg_norm_task(L, b, i, s, g, vec, lane);
+        else
+            lg_mass_task(L, b, i, s, g, vec, lane);
+        h = __shfl_sync(0xffffffffu, hn, 0);
+    }
+    // the last worker out returns the queue counters to zero for the next call
+    if (lane == 0) {
+        __threadfence();
+        if (atomicAdd(L.nexit, 1u) == gridDim.x * kLgWarps - 1) {
+            atomicExch(L.head, 0ull);
+            atomicExch(L.tail, 0ull);
+            atomicExch(L.ndone, 0u);
+            atomicExch(L.nexit, 0u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bulk-copy workers (16-byte-aligned device rows): per CTA one producer warp
+// takes chunks of kChunkSegs segment tasks of one group from the queue and
+// moves their row segments into a ring of shared-memory stages with
+// cp.async.bulk; eight consumer warps take the stages in order and run the
+// tasks on them.  The producer waits for the group of its next chunk (bounded,
+// as above); the copies already issued keep the consumers busy meanwhile.
+
+struct LgStage {
+    const float *g0;  // global start of the p segment and of the q segment (null: one row)
+    const float *g1;
+    unsigned long long g;  // group
+    int64_t s;        // segment
+    int kind;         // kLgNorm, kLgMass, 0 = stop
+    int b, i;
+    int n;            // elements of the segment
+    int c;            // elements delivered by the copies (a multiple of 4)
+    int slot;         // the chunk's counter in LgShared::left
+    int tasks;        // stages of the chunk
+    float4 np, nq;    // mass stages: the row (pair)'s normalisers (m, s.hi, s.lo)
+};
+
+// Chunks whose stages are counted in shared memory at once: a chunk's counter
+// is reused kLgSlots chunks later, and only once it is back at zero.
+constexpr int kLgSlots = 32;
+
+struct LgShared {
+    int ticket;  // next stage a consumer takes (ring position = ticket % kStages)
+    unsigned long long full[kStages];
+    unsigned long long empty[kStages];
+    LgStage meta[kStages];
+    int left[kLgSlots];  // stages of the chunk not yet done (0: free)
+};
+static_assert(sizeof(LgShared) <= kTmaBufOffset, "shared header too large");
+constexpr int kLgRingThreads = (kTmaConsumers + 1) * 32;
+constexpr int kLgRingSmemBytes = kTmaBufOffset + kStages * kStageBytes;
+
+struct LgProducer {
+    LgShared &sh;
+    unsigned char *buf;
+    uint32_t *status;
+    int lane;
+    int k = 0;           // next stage
+    uint32_t phase = 0;  // flips each time k wraps
+    uint32_t used = 0;   // bit i: stage i has been filled at least once
+    uint32_t parity = 0; // bit i: phase of the last fill of stage i
+    bool ok = true;
+
+    __device__ LgProducer(LgShared &sh_, unsigned char *buf_, uint32_t *status_, int lane_)
+        : sh(sh_), buf(buf_), status(status_), lane(lane_) {}
+
+    // Fills the next stage once its consumer released it (warp-uniform; lane 0 acts).
+    __device__ void issue(const LgStage &m) {
+        if (!ok) return;
+        bool good = true;
+        if (lane == 0) {
+            good = mbar_wait(&sh.empty[k], phase ^ 1u);
+            if (good) {
+                sh.meta[k] = m;
+                const uint32_t part = 4u * (uint32_t)m.c;
+                mbar_arrive_expect_tx(&sh.full[k], m.g1 ? 2u * part : part);
+                unsigned char *dst = buf + (size_t)k * kStageBytes;
+                if (part) {
+                    bulk_copy_g2s(dst, m.g0, part, &sh.full[k]);
+                    if (m.g1) bulk_copy_g2s(dst + kPartBytes, m.g1, part, &sh.full[k]);
+                }
+            } else {
+                atomicOr(status, kStatusTimeout);
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+            ok = false;
+            return;
+        }
+        used |= 1u << k;
+        parity = (parity & ~(1u << k)) | (phase << k);
+        if (++k == kStages) {
+            k = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+__device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *buf, int lane) {
+    LgProducer pr(sh, buf, L.status, lane);
+    const uint64_t nchunk = (uint64_t)((L.nseg + kChunkSegs - 1) / kChunkSegs);
+    // the claim after the current one is always in flight
+    unsigned long long h = 0, hn = 0;
+    if (lane == 0) {
+        h = atomicAdd(L.head, 1ull);
+        hn = atomicAdd(L.head, 1ull);
+    }
+    h = __shfl_sync(0xffffffffu, h, 0);
+    uint32_t nchunks_here = 0;
+    while (pr.ok) {
+        const uint64_t g = h / nchunk;
+        if (g >= (uint64_t)L.ngroups) break;
+        unsigned long long d = 0;
+        if (lane == 0) d = lg_wait_group(L, g);
+        d = __shfl_sync(0xffffffffu, d, 0);
+        if (!d) break;
+        const int64_t s0 = (int64_t)(h % nchunk) * kChunkSegs;
+        const int64_t s1 = min((int64_t)L.nseg, s0 + kChunkSegs);
+        h = __shfl_sync(0xffffffffu, hn, 0);
+        if (lane == 0) hn = atomicAdd(L.head, 1ull);
+        // the chunk's stage counter: free once the chunk kLgSlots before it is done
+        const int slot = (int)(nchunks_here++ % kLgSlots);
+        bool free = true;
+        if (lane == 0) {
+            IdleClock clk;
+            while (*(volatile int *)&sh.left[slot] != 0) {
+                if (!clk.idle(64)) {
+                    atomicOr(L.status, kStatusTimeout);
+                    free = false;
+                    break;
+                }
+            }
+            if (free) *(volatile int *)&sh.left[slot] = (int)(s1 - s0);
+        }
+        if (!__shfl_sync(0xffffffffu, free, 0)) {
+            pr.ok = false;
+            break;
+        }
+        LgStage m = {};
+        m.g = g;
+        m.b = (int)(uint32_t)d;
+        m.i = (int)((d >> 32) & 0xffu);
+        m.kind = (int)((d >> 40) & 3u);
+        m.slot = slot;
+        m.tasks = (int)(s1 - s0);
+        if (m.kind == (int)kLgMass) {  // read once per chunk, after the group's acquire
+            float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+            if (lane == 0) {
+                f0 = __ldcg(L.fnorm + 2 * m.b);
+                if (m.i < L.K) f1 = __ldcg(L.fnorm + 2 * m.b + 1);
+            }
+            m.np = make_float4(__shfl_sync(0xffffffffu, f0.x, 0), __shfl_sync(0xffffffffu, f0.y, 0),
+                               __shfl_sync(0xffffffffu, f0.z, 0), 0.f);
+            m.nq = make_float4(__shfl_sync(0xffffffffu, f1.x, 0), __shfl_sync(0xffffffffu, f1.y, 0),
+                               __shfl_sync(0xffffffffu, f1.z, 0), 0.f);
+        }
+        const float *a = lg_row_p(L, m.b, m.i);
+        const float *c = lg_row_q(L, m.b, m.i);
+        for (int64_t s = s0; s < s1; ++s) {
+            const int64_t base = s * kSeg;
+            m.s = s;
+            m.n = (int)min((int64_t)kSeg, L.V - base);
+            m.c = m.n & ~3;
+            m.g0 = a + base;
+            m.g1 = c ? c + base : nullptr;
+            pr.issue(m);
+        }
+    }
+    // tell every consumer to stop
+    for (int w = 0; w < kTmaConsumers; ++w) {
+        LgStage m = {};
+        pr.issue(m);
+    }
+    if (!pr.ok && lane == 0) {
+        // a wait gave up: let the copies still in flight land before returning
+        for (int i = 0; i < kStages; ++i)
+            if (pr.used & (1u << i)) mbar_wait(&sh.full[i], (pr.parity >> i) & 1u);
+    }
+}
+
+// Element e of a staged segment (the copy delivered the first c elements;
+// the last 1-3 of a ragged row come from global memory), pad past n.
+__device__ __forceinline__ float4 lg_stage4(const float *sm, const float *g, int n, int c, int e,
+                                            float pad) {
+    if (e + 3 < c) return *reinterpret_cast<const float4 *>(sm + e);
+    float4 x;
+    x.x = e < n ? part_elem(sm, g, c, e) : pad;
+    x.y = e + 1 < n ? part_elem(sm, g, c, e + 1) : pad;
+    x.z = e + 2 < n ? part_elem(sm, g, c, e + 2) : pad;
+    x.w = e + 3 < n ? part_elem(sm, g, c, e + 3) : pad;
+    return x;
+}
+
+// Normalisers of a staged segment that is not a full 1024 elements (the last
+// of a row; out of line, so the full-segment loop stays small).
+__device__ __noinline__ RowNorm lg_ragged_norm(const float *sm, const float *g, int n, int c,
+                                               float cc, int lane) {
+    float4 x[kVecPerLane];
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) x[j] = lg_stage4(sm, g, n, c, 4 * (lane + 32 * j), kNegInf);
+    return seg_norm(x, cc);
+}
+
+// Masses of a staged segment that is not a full 1024 elements, into the
+// segment's sums (out of line, as above).
+__device__ __noinline__ void lg_ragged_mass(const float *sp, const float *sq, const LgStage &m,
+                                            const RowNorm &np, const RowNorm &nq, float ia,
+                                            float ib, float2 *seg, float2 *blk, float cc,
+                                            int lane) {
+    const bool pair = m.g1 != nullptr;
+    dd v[kBlocks];
+#pragma unroll
+    for (int j = 0; j < kBlocks; ++j) {
+        const int e = 4 * (lane + 32 * j);
+        float4 ms = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < m.n) {
+            const float4 x = lg_stage4(sp, m.g0, m.n, m.c, e, 0.f);
+            const float4 y = pair ? lg_stage4(sq, m.g1, m.n, m.c, e, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ms.x = lg_mass(x.x, y.x, pair, np, nq, ia, ib, cc);
+            ms.y = e + 1 < m.n ? lg_mass(x.y, y.y, pair, np, nq, ia, ib, cc) : 0.f;
+            ms.z = e + 2 < m.n ? lg_mass(x.z, y.z, pair, np, nq, ia, ib, cc) : 0.f;
+            ms.w = e + 3 < m.n ? lg_mass(x.w, y.w, pair, np, nq, ia, ib, cc) : 0.f;
+        }
+        v[j] = dd{sum4(ms), 0.f};
+    }
+    store_sums(seg, blk, m.s, v, lane);
+}
+
+// Counts this warp's stage (its global stores made before the call) in its
+// chunk; true for the warp that completes the chunk, which then arrives for
+// all of the chunk's stages.  The CTA-scope fences make every counted stage's
+// stores part of what the completing warp's release at GPU scope publishes.
+__device__ __forceinline__ bool lg_chunk_done(LgShared &sh, int slot, int lane) {
+    __threadfence_block();
+    __syncwarp();
+    int done = 0;
+    if (lane == 0) done = atomicSub(&sh.left[slot], 1) == 1;
+    done = __shfl_sync(0xffffffffu, done, 0);
+    if (done) __threadfence_block();
+    return done;
+}
+
+__device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *buf, int lane) {
+    const RowNorm none = {kNegInf, {0.f, 0.f}};
+    while (true) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&sh.ticket, 1);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        const int k = t % kStages;
+        const float *sp = reinterpret_cast<const float *>(buf + (size_t)k * kStageBytes);
+        const float *sq = reinterpret_cast<const float *>(buf + (size_t)k * kStageBytes + kPartBytes);
+        if (!__all_sync(0xffffffffu, wait_ticket(sh.full, sh.empty, t))) {
+            if (lane == 0) atomicOr(L.status, kStatusTimeout);
+            return;
+        }
+        const LgStage m = sh.meta[k];
+        if (m.kind == 0) return;
+        const bool pair = m.g1 != nullptr;
+        const bool full = m.n == kSeg && m.c == kSeg;
+        const float4 *p4 = reinterpret_cast<const float4 *>(sp);
+        const float4 *q4 = reinterpret_cast<const float4 *>(sq);
+        if (m.kind == (int)kLgNorm) {
+            RowNorm oa, ob = none;
+            if (full) {
+                float4 xa[kVecPerLane], xb[kVecPerLane];
+#pragma unroll
+                for (int j = 0; j < kVecPerLane; ++j) {
+                    xa[j] = p4[lane + 32 * j];
+                    if (pair) xb[j] = q4[lane + 32 * j];
+                }
+                release_stage(sh.empty, k, lane);
+                oa = seg_norm(xa, L.c);
+                if (pair) ob = seg_norm(xb, L.c);
+            } else {
+                oa = lg_ragged_norm(sp, m.g0, m.n, m.c, L.c, lane);
+                if (pair) ob = lg_ragged_norm(sq, m.g1, m.n, m.c, L.c, lane);
+                release_stage(sh.empty, k, lane);
+            }
+            if (lane == 0) lg_store_pair(L, m.b, m.s, oa, ob);
+            if (lg_chunk_done(sh, m.slot, lane)) lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
+        } else {
+            const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};
+            const float ia = __frcp_rn(np.s.hi), ib = pair ? __frcp_rn(nq.s.hi) : 0.f;
+            float2 *seg = L.seg + (int64_t)m.b * L.nseg;
+            float2 *blk = L.blk + (int64_t)m.b * L.nseg * kBlocks;
+            if (full) {
+                dd v[kBlocks];
+#pragma unroll
+                for (int j = 0; j < kBlocks; ++j) {
+                    const float4 x = p4[lane + 32 * j];
+                    const float4 y = pair ? q4[lane + 32 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[j] = dd{sum4(make_float4(lg_mass(x.x, y.x, pair, np, nq, ia, ib, L.c),
+                                               lg_mass(x.y, y.y, pair, np, nq, ia, ib, L.c),
+                                               lg_mass(x.z, y.z, pair, np, nq, ia, ib, L.c),
+                                               lg_mass(x.w, y.w, pair, np, nq, ia, ib, L.c))),
+                              0.f};
+                }
+                release_stage(sh.empty, k, lane);
+                store_sums(seg, blk, m.s, v, lane);
+            } else {
+                lg_ragged_mass(sp, sq, m, np, nq, ia, ib, seg, blk, L.c, lane);
+                release_stage(sh.empty, k, lane);
+            }
+            if (lg_chunk_done(sh, m.slot, lane))
+                lg_mass_arrive(L, m.b, m.i, m.g, m.tasks, true, np, nq, ia, ib, lane);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kLgRingThreads, 2) logits_ring_kernel(const LogitsParams L) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    LgShared &sh = *reinterpret_cast<LgShared *>(smem);
+    unsigned char *buf = smem + kTmaBufOffset;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.empty[i], 1);
+        }
+        sh.ticket = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (threadIdx.x < kLgSlots) sh.left[threadIdx.x] = 0;
+    __syncthreads();
+    wait_for_primary_grid();
+    if (warp == kProducerWarp)
+        lg_produce(L, sh, buf, lane);
+    else
+        lg_consume(L, sh, buf, lane);
+    // the last CTA out returns the queue counters to zero for the next call
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(L.nexit, 1u) == gridDim.x - 1) {
+            atomicExch(L.head, 0ull);
+            atomicExch(L.tail, 0ull);
+            atomicExch(L.ndone, 0u);
+            atomicExch(L.nexit, 0u);
+        }
     }
 }
 
