@@ -10,7 +10,8 @@ INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "specverify.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "sv_tma.cuh"),
-                     os.path.join(CSRC, "sv_item.cuh"),
+                     os.path.join(CSRC, "sv_item.cuh"), os.path.join(CSRC, "sv_alpha.cuh"),
+                     os.path.join(CSRC, "sv_logits.cuh"),
                      os.path.join(INCLUDE, "specverify.h")]
 LIBRARY = os.path.join(PKG, "libspecverify.so")
 

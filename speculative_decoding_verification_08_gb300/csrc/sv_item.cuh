@@ -501,7 +501,10 @@ __device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf
             return;
         }
         const ItemMeta m = sh.meta[k];
-        if (m.kind == kStop) return;
+        if (m.kind == kStop) {  // released, so a stop may follow it round the ring
+            release_stage(sh.empty, k, lane);
+            return;
+        }
         ItemSlot &sl = sh.slot[m.slot];
         const int b = sl.b;
         const int n0 = seg_len(P.V, m.s), c0 = n0 & ~3;

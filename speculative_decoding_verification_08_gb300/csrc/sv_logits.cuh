@@ -78,8 +78,9 @@ struct LogitsParams {
                         // norm tasks' (max, sum) pairs, two float4 per segment
     float4 *fnorm;      // workspace [B][2] normalisers of the chosen row (pair)
     unsigned long long *grp;    // workspace [B * (K + 2)] groups (0 = not appended)
-    int32_t *arrive;    // workspace [B] finished tasks of the sequence's current group
-    unsigned long long *head;   // next task to hand out
+    int32_t *arrive;    // workspace [B] finished tasks of the sequence's groups so far (every
+                        // group has nseg tasks, so a group is complete at a multiple of nseg)
+    unsigned long long *head;   // next task (plain-load workers) or chunk (bulk-copy workers)
     unsigned long long *tail;   // groups appended after the first B
     uint32_t *ndone;    // sequences finished
     uint32_t *nexit;    // workers that left
@@ -376,23 +377,30 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
     const float *a = lg_row_p(L, b, i);
     const float *c = lg_row_q(L, b, i);
     int last = 0;
-    if (lane == 0) last = arrive_acq_rel(L.arrive + b, tasks) + tasks == L.nseg;
+    if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
-    int32_t x = -1;
+    // the group's last arrival: the draft token, its uniform and (position 0)
+    // every draft id are loaded together with the pairs, the token's logits
+    // as soon as its id is in
+    int32_t x = -1, y0 = 0, y1 = 0;
     float u = 0.f, gp = 0.f, gq = 0.f;
-    if (lane == 0) {
-        atomicExch(L.arrive + b, 0);  // the sequence's next group counts from zero
-        if (c) {
+    if (c) {
+        if (lane == 0) {
             x = L.t[(int64_t)b * L.K + i];
             u = L.u_acc[(int64_t)b * L.K + i];
-            if (x >= 0 && (int64_t)x < L.V) {
-                gp = __ldcg(a + x);
-                gq = __ldcg(c + x);
-            }
+        }
+        if (i == 0) {
+            if (lane < L.K) y0 = L.t[(int64_t)b * L.K + lane];
+            if (lane + 32 < L.K) y1 = L.t[(int64_t)b * L.K + lane + 32];
+        }
+        if (lane == 0 && x >= 0 && (int64_t)x < L.V) {
+            gp = __ldcg(a + x);
+            gq = __ldcg(c + x);
         }
     }
     Online na, nb;
+#pragma unroll 4
     for (int64_t k = lane; k < L.nseg; k += 32) {
         const float4 *pr = lg_pair(L, b, k);
         const float4 pa = __ldcg(pr);
@@ -406,14 +414,14 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
     if (c) nb.warp_merge(L.c);
     bool bad = false;
     if (c && i == 0) {  // every draft id is checked once, before the first decision
-        for (int j = lane; j < L.K; j += 32) {
-            const int32_t y = L.t[(int64_t)b * L.K + j];
-            bad |= y < 0 || (int64_t)y >= L.V;
-        }
+        static_assert(kMaxK <= 64, "two draft ids per lane");
+        bad = (lane < L.K && (y0 < 0 || (int64_t)y0 >= L.V)) ||
+              (lane + 32 < L.K && (y1 < 0 || (int64_t)y1 >= L.V));
         bad = __any_sync(0xffffffffu, bad);
     }
     if (lane != 0) return;
     if (bad) {
+        atomicExch(L.arrive + b, 0);  // no later group: the counter is back at zero
         lg_finish(L, b, 0, -1, kStatusBadToken);
     } else if (c) {
         const float pt = __fmul_rn(warp_e(gp, na.m, L.c), __frcp_rn(na.s.hi));
@@ -457,10 +465,10 @@ __device__ __noinline__ void lg_mass_arrive(const LogitsParams &L, int b, int n,
     float2 *seg = L.seg + (int64_t)b * L.nseg;
     float2 *blk = L.blk + (int64_t)b * L.nseg * kBlocks;
     int last = 0;
-    if (lane == 0) last = arrive_acq_rel(L.arrive + b, tasks) + tasks == L.nseg;
+    if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
-    if (lane == 0) atomicExch(L.arrive + b, 0);
+    if (lane == 0) atomicExch(L.arrive + b, 0);  // the sequence's last group: back to zero
     DrawInputs in = {};
     in.u = split_uniform(L.u_res[b]);
     int next = draw_core(L.nseg, L.V, seg, blk, nullptr, nullptr, in, lane,
@@ -566,7 +574,7 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const Logits
 
 // ---------------------------------------------------------------------------
 // bulk-copy workers (16-byte-aligned device rows): per CTA one producer warp
-// takes chunks of kChunkSegs segment tasks of one group from the queue and
+// takes chunks of kLgChunkSegs segment tasks of one group from the queue and
 // moves their row segments into a ring of shared-memory stages with
 // cp.async.bulk; eight consumer warps take the stages in order and run the
 // tasks on them.  The producer waits for the group of its next chunk (bounded,
@@ -576,30 +584,62 @@ struct LgStage {
     const float *g0;  // global start of the p segment and of the q segment (null: one row)
     const float *g1;
     unsigned long long g;  // group
-    int64_t s;        // segment
+    int64_t s;        // first segment
     int kind;         // kLgNorm, kLgMass, 0 = stop
     int b, i;
-    int n;            // elements of the segment
+    int ns;           // segments in the stage (1 .. kLgStageSegs)
+    int n;            // elements of the stage's part of a row
     int c;            // elements delivered by the copies (a multiple of 4)
     int slot;         // the chunk's counter in LgShared::left
     int tasks;        // stages of the chunk
     float4 np, nq;    // mass stages: the row (pair)'s normalisers (m, s.hi, s.lo)
 };
 
+// Segments per chunk (one queue claim, one group read, one global arrival).
+#ifndef SV_LG_CHUNK
+#define SV_LG_CHUNK 16
+#endif
+constexpr int kLgChunkSegs = SV_LG_CHUNK;
 // Chunks whose stages are counted in shared memory at once: a chunk's counter
 // is reused kLgSlots chunks later, and only once it is back at zero.
 constexpr int kLgSlots = 32;
 
+// The ring: kLgStages stages, each kLgStageSegs consecutive segments of the
+// row pair (or of one row), p's part first.
+#ifndef SV_LG_STAGE_SEGS
+#define SV_LG_STAGE_SEGS 2
+#endif
+#ifndef SV_LG_STAGES
+#define SV_LG_STAGES 6
+#endif
+constexpr int kLgStageSegs = SV_LG_STAGE_SEGS;
+constexpr int kLgStages = SV_LG_STAGES;
+constexpr int kLgPartBytes = kLgStageSegs * kSeg * 4;
+constexpr int kLgStageBytes = 2 * kLgPartBytes;
+static_assert(kLgChunkSegs % kLgStageSegs == 0, "a chunk is whole stages");
+static_assert(kLgStages <= 32, "stage bookkeeping is a 32-bit mask");
+// Consumer warps: eight, or fewer when the ring is short -- a ticket's parity
+// wait needs consumers <= stages + 1 (see wait_ticket).
+constexpr int kLgConsumers = kLgStages + 1 < kTmaConsumers ? kLgStages + 1 : kTmaConsumers;
+constexpr int kLgProducerWarp = kLgConsumers;
+
+// A chunk the producer has taken.
+struct LgChunk {
+    unsigned long long g, d;  // group and its record
+    uint64_t ci;              // chunk index within the group
+    float4 np, nq;            // mass chunks: the normalisers
+};
+
 struct LgShared {
-    int ticket;  // next stage a consumer takes (ring position = ticket % kStages)
-    unsigned long long full[kStages];
-    unsigned long long empty[kStages];
-    LgStage meta[kStages];
+    int ticket;  // next stage a consumer takes (ring position = ticket % kLgStages)
+    unsigned long long full[kLgStages];
+    unsigned long long empty[kLgStages];
+    LgStage meta[kLgStages];
     int left[kLgSlots];  // stages of the chunk not yet done (0: free)
 };
 static_assert(sizeof(LgShared) <= kTmaBufOffset, "shared header too large");
-constexpr int kLgRingThreads = (kTmaConsumers + 1) * 32;
-constexpr int kLgRingSmemBytes = kTmaBufOffset + kStages * kStageBytes;
+constexpr int kLgRingThreads = (kLgConsumers + 1) * 32;
+constexpr int kLgRingSmemBytes = kTmaBufOffset + kLgStages * kLgStageBytes;
 
 struct LgProducer {
     LgShared &sh;
@@ -625,10 +665,10 @@ struct LgProducer {
                 sh.meta[k] = m;
                 const uint32_t part = 4u * (uint32_t)m.c;
                 mbar_arrive_expect_tx(&sh.full[k], m.g1 ? 2u * part : part);
-                unsigned char *dst = buf + (size_t)k * kStageBytes;
+                unsigned char *dst = buf + (size_t)k * kLgStageBytes;
                 if (part) {
                     bulk_copy_g2s(dst, m.g0, part, &sh.full[k]);
-                    if (m.g1) bulk_copy_g2s(dst + kPartBytes, m.g1, part, &sh.full[k]);
+                    if (m.g1) bulk_copy_g2s(dst + kLgPartBytes, m.g1, part, &sh.full[k]);
                 }
             } else {
                 atomicOr(status, kStatusTimeout);
@@ -640,91 +680,106 @@ struct LgProducer {
         }
         used |= 1u << k;
         parity = (parity & ~(1u << k)) | (phase << k);
-        if (++k == kStages) {
+        if (++k == kLgStages) {
             k = 0;
             phase ^= 1u;
         }
     }
 };
 
+// Issues the stages of chunk ci (segments [ci * kLgChunkSegs, ...)) of group g.
+__device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &pr,
+                               const LgChunk &ch, uint32_t &nchunks_here, int lane) {
+    const uint64_t g = ch.g, ci = ch.ci;
+    const unsigned long long d = ch.d;
+    const int64_t s0 = (int64_t)ci * kLgChunkSegs;
+    const int64_t s1 = min((int64_t)L.nseg, s0 + kLgChunkSegs);
+    // the chunk's stage counter: free once the chunk kLgSlots before it is done
+    const int slot = (int)(nchunks_here++ % kLgSlots);
+    bool free = true;
+    if (lane == 0) {
+        IdleClock clk;
+        while (*(volatile int *)&sh.left[slot] != 0) {
+            if (!clk.idle(64)) {
+                atomicOr(L.status, kStatusTimeout);
+                free = false;
+                break;
+            }
+        }
+        if (free)
+            *(volatile int *)&sh.left[slot] = (int)((s1 - s0 + kLgStageSegs - 1) / kLgStageSegs);
+    }
+    if (!__shfl_sync(0xffffffffu, free, 0)) {
+        pr.ok = false;
+        return;
+    }
+    LgStage m = {};
+    m.g = g;
+    m.b = (int)(uint32_t)d;
+    m.i = (int)((d >> 32) & 0xffu);
+    m.kind = (int)((d >> 40) & 3u);
+    m.slot = slot;
+    m.tasks = (int)(s1 - s0);
+    m.np = ch.np;
+    m.nq = ch.nq;
+    const float *a = lg_row_p(L, m.b, m.i);
+    const float *c = lg_row_q(L, m.b, m.i);
+    for (int64_t s = s0; s < s1; s += kLgStageSegs) {
+        const int64_t base = s * kSeg;
+        m.s = s;
+        m.ns = (int)min((int64_t)kLgStageSegs, s1 - s);
+        m.n = (int)min((int64_t)m.ns * kSeg, L.V - base);
+        m.c = m.n & ~3;
+        m.g0 = a + base;
+        m.g1 = c ? c + base : nullptr;
+        pr.issue(m);
+    }
+}
+
+// Chunks are taken in queue order (the first B groups, then the appended
+// ones as they come); the claim after the current one is always in flight.
 __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *buf, int lane) {
     LgProducer pr(sh, buf, L.status, lane);
-    const uint64_t nchunk = (uint64_t)((L.nseg + kChunkSegs - 1) / kChunkSegs);
-    // the claim after the current one is always in flight
+    const uint64_t nchunk = (uint64_t)((L.nseg + kLgChunkSegs - 1) / kLgChunkSegs);
+    uint32_t nchunks_here = 0;
     unsigned long long h = 0, hn = 0;
     if (lane == 0) {
         h = atomicAdd(L.head, 1ull);
         hn = atomicAdd(L.head, 1ull);
     }
     h = __shfl_sync(0xffffffffu, h, 0);
-    uint32_t nchunks_here = 0;
     while (pr.ok) {
-        const uint64_t g = h / nchunk;
-        if (g >= (uint64_t)L.ngroups) break;
+        LgChunk ch = {};
+        ch.g = h / nchunk;
+        if (ch.g >= (uint64_t)L.ngroups) break;
         unsigned long long d = 0;
-        if (lane == 0) d = lg_wait_group(L, g);
-        d = __shfl_sync(0xffffffffu, d, 0);
-        if (!d) break;
-        const int64_t s0 = (int64_t)(h % nchunk) * kChunkSegs;
-        const int64_t s1 = min((int64_t)L.nseg, s0 + kChunkSegs);
+        if (lane == 0) {
+            d = lg_wait_group(L, ch.g);
+            if (d && ((d >> 40) & 3u) == kLgMass) {  // after the group's acquire
+                const int b = (int)(uint32_t)d;
+                ch.np = __ldcg(L.fnorm + 2 * b);
+                if ((int)((d >> 32) & 0xffu) < L.K) ch.nq = __ldcg(L.fnorm + 2 * b + 1);
+            }
+        }
+        ch.d = __shfl_sync(0xffffffffu, d, 0);
+        if (!ch.d) break;
+        ch.np = make_float4(__shfl_sync(0xffffffffu, ch.np.x, 0), __shfl_sync(0xffffffffu, ch.np.y, 0),
+                            __shfl_sync(0xffffffffu, ch.np.z, 0), 0.f);
+        ch.nq = make_float4(__shfl_sync(0xffffffffu, ch.nq.x, 0), __shfl_sync(0xffffffffu, ch.nq.y, 0),
+                            __shfl_sync(0xffffffffu, ch.nq.z, 0), 0.f);
+        ch.ci = h % nchunk;
         h = __shfl_sync(0xffffffffu, hn, 0);
         if (lane == 0) hn = atomicAdd(L.head, 1ull);
-        // the chunk's stage counter: free once the chunk kLgSlots before it is done
-        const int slot = (int)(nchunks_here++ % kLgSlots);
-        bool free = true;
-        if (lane == 0) {
-            IdleClock clk;
-            while (*(volatile int *)&sh.left[slot] != 0) {
-                if (!clk.idle(64)) {
-                    atomicOr(L.status, kStatusTimeout);
-                    free = false;
-                    break;
-                }
-            }
-            if (free) *(volatile int *)&sh.left[slot] = (int)(s1 - s0);
-        }
-        if (!__shfl_sync(0xffffffffu, free, 0)) {
-            pr.ok = false;
-            break;
-        }
-        LgStage m = {};
-        m.g = g;
-        m.b = (int)(uint32_t)d;
-        m.i = (int)((d >> 32) & 0xffu);
-        m.kind = (int)((d >> 40) & 3u);
-        m.slot = slot;
-        m.tasks = (int)(s1 - s0);
-        if (m.kind == (int)kLgMass) {  // read once per chunk, after the group's acquire
-            float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
-            if (lane == 0) {
-                f0 = __ldcg(L.fnorm + 2 * m.b);
-                if (m.i < L.K) f1 = __ldcg(L.fnorm + 2 * m.b + 1);
-            }
-            m.np = make_float4(__shfl_sync(0xffffffffu, f0.x, 0), __shfl_sync(0xffffffffu, f0.y, 0),
-                               __shfl_sync(0xffffffffu, f0.z, 0), 0.f);
-            m.nq = make_float4(__shfl_sync(0xffffffffu, f1.x, 0), __shfl_sync(0xffffffffu, f1.y, 0),
-                               __shfl_sync(0xffffffffu, f1.z, 0), 0.f);
-        }
-        const float *a = lg_row_p(L, m.b, m.i);
-        const float *c = lg_row_q(L, m.b, m.i);
-        for (int64_t s = s0; s < s1; ++s) {
-            const int64_t base = s * kSeg;
-            m.s = s;
-            m.n = (int)min((int64_t)kSeg, L.V - base);
-            m.c = m.n & ~3;
-            m.g0 = a + base;
-            m.g1 = c ? c + base : nullptr;
-            pr.issue(m);
-        }
+        lg_issue_chunk(L, sh, pr, ch, nchunks_here, lane);
     }
     // tell every consumer to stop
-    for (int w = 0; w < kTmaConsumers; ++w) {
+    for (int w = 0; w < kLgConsumers; ++w) {
         LgStage m = {};
         pr.issue(m);
     }
     if (!pr.ok && lane == 0) {
         // a wait gave up: let the copies still in flight land before returning
-        for (int i = 0; i < kStages; ++i)
+        for (int i = 0; i < kLgStages; ++i)
             if (pr.used & (1u << i)) mbar_wait(&sh.full[i], (pr.parity >> i) & 1u);
     }
 }
@@ -777,6 +832,16 @@ __device__ __noinline__ void lg_ragged_mass(const float *sp, const float *sq, co
     store_sums(seg, blk, m.s, v, lane);
 }
 
+// Waits (bounded) until ring position t % kLgStages holds the fill of ticket t
+// (the same two-step wait as wait_ticket, on this ring's size; kLgConsumers
+// keeps it unambiguous).
+__device__ __forceinline__ bool lg_wait_ticket(unsigned long long *full, unsigned long long *empty,
+                                               int t) {
+    const int k = t % kLgStages;
+    const uint32_t phase = (uint32_t)(t / kLgStages) & 1u;
+    return mbar_wait(&empty[k], phase ^ 1u) && mbar_wait(&full[k], phase);
+}
+
 // Counts this warp's stage (its global stores made before the call) in its
 // chunk; true for the warp that completes the chunk, which then arrives for
 // all of the chunk's stages.  The CTA-scope fences make every counted stage's
@@ -797,61 +862,76 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
         int t = 0;
         if (lane == 0) t = atomicAdd(&sh.ticket, 1);
         t = __shfl_sync(0xffffffffu, t, 0);
-        const int k = t % kStages;
-        const float *sp = reinterpret_cast<const float *>(buf + (size_t)k * kStageBytes);
-        const float *sq = reinterpret_cast<const float *>(buf + (size_t)k * kStageBytes + kPartBytes);
-        if (!__all_sync(0xffffffffu, wait_ticket(sh.full, sh.empty, t))) {
+        const int k = t % kLgStages;
+        const float *sp = reinterpret_cast<const float *>(buf + (size_t)k * kLgStageBytes);
+        const float *sq = reinterpret_cast<const float *>(buf + (size_t)k * kLgStageBytes + kLgPartBytes);
+        if (!__all_sync(0xffffffffu, lg_wait_ticket(sh.full, sh.empty, t))) {
             if (lane == 0) atomicOr(L.status, kStatusTimeout);
             return;
         }
         const LgStage m = sh.meta[k];
-        if (m.kind == 0) return;
+        if (m.kind == 0) {  // released, so a stop may follow it round the ring
+            release_stage(sh.empty, k, lane);
+            return;
+        }
         const bool pair = m.g1 != nullptr;
-        const bool full = m.n == kSeg && m.c == kSeg;
-        const float4 *p4 = reinterpret_cast<const float4 *>(sp);
-        const float4 *q4 = reinterpret_cast<const float4 *>(sq);
         if (m.kind == (int)kLgNorm) {
-            RowNorm oa, ob = none;
-            if (full) {
-                float4 xa[kVecPerLane], xb[kVecPerLane];
+            for (int j = 0; j < m.ns; ++j) {
+                const int o = j * kSeg;  // the segment's offset in the stage
+                RowNorm oa, ob = none;
+                if (o + kSeg <= m.c) {   // a full segment, straight from shared memory
+                    const float4 *p4 = reinterpret_cast<const float4 *>(sp + o);
+                    const float4 *q4 = reinterpret_cast<const float4 *>(sq + o);
+                    float4 xa[kVecPerLane], xb[kVecPerLane];
 #pragma unroll
-                for (int j = 0; j < kVecPerLane; ++j) {
-                    xa[j] = p4[lane + 32 * j];
-                    if (pair) xb[j] = q4[lane + 32 * j];
+                    for (int v = 0; v < kVecPerLane; ++v) {
+                        xa[v] = p4[lane + 32 * v];
+                        if (pair) xb[v] = q4[lane + 32 * v];
+                    }
+                    oa = seg_norm(xa, L.c);
+                    if (pair) ob = seg_norm(xb, L.c);
+                } else {
+                    const int n = min(kSeg, m.n - o), c = max(0, min(kSeg, m.c - o));
+                    oa = lg_ragged_norm(sp + o, m.g0 + o, n, c, L.c, lane);
+                    if (pair) ob = lg_ragged_norm(sq + o, m.g1 + o, n, c, L.c, lane);
                 }
-                release_stage(sh.empty, k, lane);
-                oa = seg_norm(xa, L.c);
-                if (pair) ob = seg_norm(xb, L.c);
-            } else {
-                oa = lg_ragged_norm(sp, m.g0, m.n, m.c, L.c, lane);
-                if (pair) ob = lg_ragged_norm(sq, m.g1, m.n, m.c, L.c, lane);
-                release_stage(sh.empty, k, lane);
+                if (lane == 0) lg_store_pair(L, m.b, m.s + j, oa, ob);
             }
-            if (lane == 0) lg_store_pair(L, m.b, m.s, oa, ob);
+            release_stage(sh.empty, k, lane);
             if (lg_chunk_done(sh, m.slot, lane)) lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
         } else {
             const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};
             const float ia = __frcp_rn(np.s.hi), ib = pair ? __frcp_rn(nq.s.hi) : 0.f;
             float2 *seg = L.seg + (int64_t)m.b * L.nseg;
             float2 *blk = L.blk + (int64_t)m.b * L.nseg * kBlocks;
-            if (full) {
-                dd v[kBlocks];
+            for (int j = 0; j < m.ns; ++j) {
+                const int o = j * kSeg;
+                if (o + kSeg <= m.c) {
+                    const float4 *p4 = reinterpret_cast<const float4 *>(sp + o);
+                    const float4 *q4 = reinterpret_cast<const float4 *>(sq + o);
+                    dd v[kBlocks];
 #pragma unroll
-                for (int j = 0; j < kBlocks; ++j) {
-                    const float4 x = p4[lane + 32 * j];
-                    const float4 y = pair ? q4[lane + 32 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[j] = dd{sum4(make_float4(lg_mass(x.x, y.x, pair, np, nq, ia, ib, L.c),
-                                               lg_mass(x.y, y.y, pair, np, nq, ia, ib, L.c),
-                                               lg_mass(x.z, y.z, pair, np, nq, ia, ib, L.c),
-                                               lg_mass(x.w, y.w, pair, np, nq, ia, ib, L.c))),
-                              0.f};
+                    for (int w = 0; w < kBlocks; ++w) {
+                        const float4 x = p4[lane + 32 * w];
+                        const float4 y = pair ? q4[lane + 32 * w] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[w] = dd{sum4(make_float4(lg_mass(x.x, y.x, pair, np, nq, ia, ib, L.c),
+                                                   lg_mass(x.y, y.y, pair, np, nq, ia, ib, L.c),
+                                                   lg_mass(x.z, y.z, pair, np, nq, ia, ib, L.c),
+                                                   lg_mass(x.w, y.w, pair, np, nq, ia, ib, L.c))),
+                                  0.f};
+                    }
+                    store_sums(seg, blk, m.s + j, v, lane);
+                } else {
+                    LgStage mj = m;
+                    mj.s = m.s + j;
+                    mj.n = min(kSeg, m.n - o);
+                    mj.c = max(0, min(kSeg, m.c - o));
+                    mj.g0 = m.g0 + o;
+                    mj.g1 = pair ? m.g1 + o : nullptr;
+                    lg_ragged_mass(sp + o, sq + o, mj, np, nq, ia, ib, seg, blk, L.c, lane);
                 }
-                release_stage(sh.empty, k, lane);
-                store_sums(seg, blk, m.s, v, lane);
-            } else {
-                lg_ragged_mass(sp, sq, m, np, nq, ia, ib, seg, blk, L.c, lane);
-                release_stage(sh.empty, k, lane);
             }
+            release_stage(sh.empty, k, lane);
             if (lg_chunk_done(sh, m.slot, lane))
                 lg_mass_arrive(L, m.b, m.i, m.g, m.tasks, true, np, nq, ia, ib, lane);
         }
@@ -864,7 +944,7 @@ __global__ void __launch_bounds__(kLgRingThreads, 2) logits_ring_kernel(const Lo
     unsigned char *buf = smem + kTmaBufOffset;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kLgStages; ++i) {
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.empty[i], 1);
         }
@@ -874,7 +954,7 @@ __global__ void __launch_bounds__(kLgRingThreads, 2) logits_ring_kernel(const Lo
     if (threadIdx.x < kLgSlots) sh.left[threadIdx.x] = 0;
     __syncthreads();
     wait_for_primary_grid();
-    if (warp == kProducerWarp)
+    if (warp == kLgProducerWarp)
         lg_produce(L, sh, buf, lane);
     else
         lg_consume(L, sh, buf, lane);

@@ -43,6 +43,11 @@ constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 #define SV_STAGES 11
 #endif
 constexpr int kStages = SV_STAGES;
+// wait_ticket tells a stage's fills apart by barrier parity, which is only
+// unambiguous while no consumer can take ticket t + 2 * kStages before ticket
+// t's stage is released.  The other consumers can hold at most kStages - 1
+// filled tickets beyond t, so that holds while consumers <= kStages + 1.
+static_assert(kTmaConsumers <= kStages + 1, "too few ring stages for the consumers");
 constexpr int kPartBytes = kSeg * 4;        // one segment of one row
 constexpr int kStageBytes = 2 * kPartBytes;
 constexpr int kChunkSegs = 8;               // segments per chunk
@@ -467,7 +472,10 @@ __device__ void tma_consume(const Params &P, TmaShared &sh, unsigned char *buf, 
             return;
         }
         const StageMeta m = sh.meta[k];
-        if (m.kind == kStop) return;
+        if (m.kind == kStop) {  // released, so a stop may follow it round the ring
+            release_stage(sh.empty, k, lane);
+            return;
+        }
         float2 *seg = P.seg + (int64_t)m.b * P.nseg;
         float2 *blk = P.blk + (int64_t)m.b * P.nseg * kBlocks;
         if (m.kind == kPair) {
