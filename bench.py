@@ -35,6 +35,7 @@ KERNEL_SOURCES = [
     "speculative_decoding_verification_08_gb300/csrc/sv_device.cuh",
     "speculative_decoding_verification_08_gb300/csrc/sv_tma.cuh",
     "speculative_decoding_verification_08_gb300/csrc/sv_item.cuh",
+    "speculative_decoding_verification_08_gb300/csrc/sv_logits.cuh",
     "speculative_decoding_verification_08_gb300/csrc/specverify.cu",
 ]
 
@@ -50,7 +51,9 @@ def parse_args(argv=None):
                     default=None,
                     help="alpha: the acceptance-rate diagnostic; logits: sampling from logits "
                          "(log of the workload's probabilities, temperature 1)")
-    ap.add_argument("--sets", type=int, default=4, help="input sets rotated through")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="input sets rotated through (0: at least 4, and enough that their "
+                         "required bytes exceed 4x L2)")
     ap.add_argument("--graph", action="store_true", help="replay the steps from a CUDA graph")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="persistent grid residency (0 = max)")
     ap.add_argument("--e2e-steps", type=int, default=60)
@@ -301,7 +304,7 @@ def time_oracle(host, mode: str, K: int, seconds: float, nthreads: int, max_roun
 def workload_config(args, B, K, V, extra=None):
     from speculative_decoding_verification_08_gb300.inputs import CONFIGS
     cfg = {"workload": CONFIGS[args.config]["name"], "B": B, "V": V, "K": K, "mode": args.mode,
-           "input_sets": args.sets}
+           "input_sets": args.sets if args.sets > 0 else 4}
     if extra:
         cfg.update(extra)
     return cfg
@@ -367,47 +370,47 @@ def main(argv=None):
 
     c = CONFIGS[args.config]
     B, K, V = c["B"], c["K"], c["V"]
-    sets = [make_inputs(args.config, dev, seed=rank_seed(args.config, s, rank))
-            for s in range(args.sets)]
-    torch.cuda.empty_cache()
     ws = sv.Workspace(B, K, V, dev)
-    outs = [(torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32,
-                                                                         device=dev))
-            for _ in sets]
-    torch.cuda.synchronize(dev)
     stream = torch.cuda.Stream(dev)          # every timed launch goes to this stream
     sh = ctypes.c_void_p(stream.cuda_stream)
     P = lambda x: ctypes.c_void_p(0 if x is None else x.data_ptr())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets, outs, calls, keep = [], [], [], []
 
-    # precomputed C-ABI argument lists: the timed loop is one C call per step
-    calls = []
-    keep = []
-    for bt, (n, nx) in zip(sets, outs):
-        if args.mode == "logits":
-            zp, zq = torch.log(bt.p), torch.log(bt.q)
-            keep.append((zp, zq))
-            calls.append((lib.sv_verify_sample_logits,
-                          (P(zp), V, P(zq), V, P(bt.t), P(bt.u_acc), P(bt.u_res), B, K, V,
-                           ctypes.c_float(1.0), P(n), P(nx), ws.ptr, ws.nbytes, sh)))
-        elif args.mode == "alpha":
-            a_out = torch.empty(B, K, dtype=torch.float64, device=dev)
-            e_out = torch.empty(B, dtype=torch.float64, device=dev)
-            keep.append((a_out, e_out))
-            calls.append((lib.sv_alpha,
-                          (P(bt.p), V, P(bt.q), V, B, K, V, P(a_out), P(e_out), ws.ptr, ws.nbytes,
-                           sh)))
-        elif args.mode == "greedy":
-            calls.append((lib.sv_verify_greedy,
-                          (P(bt.p), V, P(bt.t), B, K, V, P(n), P(nx), ws.ptr, ws.nbytes, sh)))
-        elif args.mode == "sample":
-            calls.append((lib.sv_verify_sample,
-                          (P(bt.p), V, P(bt.q), V, P(bt.t), P(bt.u_acc), P(bt.u_res), B, K, V,
-                           P(n), P(nx), ws.ptr, ws.nbytes, sh)))
-        else:
-            calls.append((lib.sv_verify_round,
-                          (P(bt.mode), P(bt.p), V, P(bt.q), V, P(bt.t), P(bt.u_acc),
-                           P(bt.u_res), B, K, V, P(n), P(nx), None, None, 0, ws.ptr,
-                           ws.nbytes, sh)))
+    def add_sets(count):
+        """Appends input sets and their precomputed C-ABI argument lists (the
+        timed loop is one C call per step)."""
+        for s_idx in range(len(sets), len(sets) + count):
+            bt = make_inputs(args.config, dev, seed=rank_seed(args.config, s_idx, rank))
+            n = torch.empty(B, dtype=torch.int32, device=dev)
+            nx = torch.empty(B, dtype=torch.int32, device=dev)
+            sets.append(bt)
+            outs.append((n, nx))
+            if args.mode == "logits":
+                zp, zq = torch.log(bt.p), torch.log(bt.q)
+                keep.append((zp, zq))
+                calls.append((lib.sv_verify_sample_logits,
+                              (P(zp), V, P(zq), V, P(bt.t), P(bt.u_acc), P(bt.u_res), B, K, V,
+                               ctypes.c_float(1.0), P(n), P(nx), ws.ptr, ws.nbytes, sh)))
+            elif args.mode == "alpha":
+                a_out = torch.empty(B, K, dtype=torch.float64, device=dev)
+                e_out = torch.empty(B, dtype=torch.float64, device=dev)
+                keep.append((a_out, e_out))
+                calls.append((lib.sv_alpha,
+                              (P(bt.p), V, P(bt.q), V, B, K, V, P(a_out), P(e_out), ws.ptr,
+                               ws.nbytes, sh)))
+            elif args.mode == "greedy":
+                calls.append((lib.sv_verify_greedy,
+                              (P(bt.p), V, P(bt.t), B, K, V, P(n), P(nx), ws.ptr, ws.nbytes, sh)))
+            elif args.mode == "sample":
+                calls.append((lib.sv_verify_sample,
+                              (P(bt.p), V, P(bt.q), V, P(bt.t), P(bt.u_acc), P(bt.u_res), B, K,
+                               V, P(n), P(nx), ws.ptr, ws.nbytes, sh)))
+            else:
+                calls.append((lib.sv_verify_round,
+                              (P(bt.mode), P(bt.p), V, P(bt.q), V, P(bt.t), P(bt.u_acc),
+                               P(bt.u_res), B, K, V, P(n), P(nx), None, None, 0, ws.ptr,
+                               ws.nbytes, sh)))
 
     def step(k):
         fn, a = calls[k % len(calls)]
@@ -415,26 +418,44 @@ def main(argv=None):
         if rc != 0:
             raise RuntimeError(f"verify call failed: {sv.status_string(rc)}")
 
-    for k in range(args.warmup):
-        step(k)
-    torch.cuda.synchronize(dev)
+    def warm_up():
+        for k in range(max(args.warmup, len(calls))):   # every set's outputs at least once
+            step(k)
+        torch.cuda.synchronize(dev)
+
+    def required_per_launch():
+        """Algorithmic bytes per launch, from each set's n_accepted; with the
+        per-set figures, the histogram of n and the dense bytes."""
+        req, dense, nhist = [], [], np.zeros(K + 1, dtype=np.int64)
+        for bt, (n, _) in zip(sets if args.mode != "alpha" else [], outs):
+            md = bt.mode.cpu().numpy() if args.mode == "round" else np.full(
+                B, 0 if args.mode == "greedy" else 1)   # logits: sampling
+            nn = n.cpu().numpy()
+            nhist += np.bincount(nn, minlength=K + 1)[:K + 1]
+            req.append(logits_bytes(nn, K, V) if args.mode == "logits"
+                       else required_bytes(md, nn, K, V))
+            dense.append(dense_bytes(md, K, V))
+        if args.mode == "alpha":
+            req = dense = [alpha_bytes(B, K, V)]
+        return float(np.mean(req)), req, dense, nhist
+
+    add_sets(args.sets if args.sets > 0 else 4)
+    warm_up()
+    req_per_launch, req, dense, nhist = required_per_launch()
+    if args.sets == 0 and len(sets) * req_per_launch < 4 * l2:
+        # more sets, so that consecutive launches never find their rows in L2
+        # (bounded by a memory budget; the line says so if that is not enough)
+        per_set = max(1.0, float(np.mean(dense)) * (3 if args.mode == "logits" else 1))
+        want = int(np.ceil(4.4 * l2 / max(req_per_launch, 1.0)))   # sets differ a little
+        want = min(want, 4096, max(len(sets), int(40e9 // per_set)))
+        add_sets(want - len(sets))
+        warm_up()
+        req_per_launch, req, dense, nhist = required_per_launch()
+    torch.cuda.empty_cache()
     status = ws.status(stream)
     kernels_per_step = sv.last_kernel_count()
     grid_ctas = int(sv.last_grid_size())     # of the timed launches (the e2e leg may differ)
-
-    # algorithmic bytes per launch, from each set's n_accepted
-    req, dense, nhist = [], [], np.zeros(K + 1, dtype=np.int64)
-    for bt, (n, _) in zip(sets if args.mode != "alpha" else [], outs):
-        md = bt.mode.cpu().numpy() if args.mode == "round" else np.full(
-            B, 0 if args.mode == "greedy" else 1)   # logits: sampling
-        nn = n.cpu().numpy()
-        nhist += np.bincount(nn, minlength=K + 1)[:K + 1]
-        req.append(logits_bytes(nn, K, V) if args.mode == "logits" else required_bytes(md, nn, K, V))
-        dense.append(dense_bytes(md, K, V))
-    if args.mode == "alpha":
-        req = dense = [alpha_bytes(B, K, V)]
-    req_per_launch = float(np.mean(req))
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    l2_resident = len(sets) * req_per_launch < 4 * l2
 
     graph = None
     if args.graph:
@@ -511,11 +532,17 @@ def main(argv=None):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         host = sets[0].numpy()
         ncpu = os.cpu_count() or 1
-        rps, nb, rounds, el = time_oracle(host, args.mode, K, args.cpu_seconds, ncpu)
-        used = 1 if args.mode in ("alpha", "logits") else ncpu   # single-threaded oracles
+        threaded = args.mode not in ("alpha", "logits")   # those oracles are single-threaded
+        secs = args.cpu_seconds / 2 if threaded else args.cpu_seconds
+        rps, nb, rounds, el = time_oracle(host, args.mode, K, secs, ncpu)
+        used = ncpu if threaded else 1
         cpu = {"value": rps, "unit": UNIT, "cores": used, "kind": "oracle",
                "sample": f"{rounds} full rounds ({nb} sequences each) of input set 0, "
                          f"{el:.1f} s on {used} thread{'s' if used > 1 else ''}"}
+        if threaded:   # the same oracle on one thread, for the per-core figure
+            rps1, _, rounds1, el1 = time_oracle(host, args.mode, K, secs, 1)
+            cpu["value_1thread"] = rps1
+            cpu["sample"] += f"; {rounds1} rounds in {el1:.1f} s on 1 thread"
 
     if rank == 0:
         clk = clocks.summary(t_wall0, t_wall1) if clocks else None
@@ -525,6 +552,7 @@ def main(argv=None):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; see inputs.py)",
             "config": workload_config(args, B, K, V, {
+                "input_sets": len(sets),
                 "l2": (f"rotating {len(sets)} input sets; {len(sets) * req_per_launch / 1e6:.0f} MB"
                        f" required bytes per rotation = {len(sets) * req_per_launch / l2:.1f}x "
                        f"L2 ({l2 / 1e6:.0f} MB)"),
@@ -537,7 +565,9 @@ def main(argv=None):
             "n_accepted_hist": nhist.tolist(),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": traffic, "kernel_us": kernel_us},
+                         "traffic": traffic, "kernel_us": kernel_us,
+                         **({"note": "L2-resident rotation: not an HBM figure"}
+                            if l2_resident else {})},
             "gpu_launches": launches * kernels_per_step,
             "status_bits": status,
             "clocks": clk,
