@@ -98,3 +98,46 @@ def test_bad_temperature_rejected(tau):
     zp, zq, t, ua, ur = make_logits(2, 100, 2, 1.0, seed=1)
     with pytest.raises(sv.SpecVerifyError):
         sv.verify_sample_logits(zp, zq, t, ua, ur, tau)
+
+
+def test_repeated_calls_reuse_the_workspace_cleanly():
+    """The queue counters, group records and arrival counts return to zero at
+    the end of every call: repeated calls on one workspace, alternating inputs
+    and sizes, give the same outputs and no status bits."""
+    B, V, K, tau = 160, 6000, 4, 1.0
+    a = make_logits(B, V, K, tau, seed=41)
+    b = make_logits(B, V, K, tau, seed=42)
+    small = make_logits(9, 2500, 2, tau, seed=43)
+    ws = sv.Workspace(B, K, V)
+    first = {}
+    for r in range(3):
+        for name, x in (("a", a), ("b", b)):
+            n, nx = sv.verify_sample_logits(*x, tau, ws=ws)
+            got = (n.cpu().numpy(), nx.cpu().numpy())
+            if r == 0:
+                first[name] = got
+                run(*x, tau)      # the oracle agrees with the first call
+            else:
+                assert np.array_equal(got[0], first[name][0])
+                assert np.array_equal(got[1], first[name][1])
+        sv.verify_sample_logits(*small, tau)   # another size on its own workspace in between
+    assert ws.status() == 0
+
+
+def test_plain_load_workers_at_a_large_batch():
+    """Rows off a 16-byte boundary take the plain-load workers; here with more
+    sequences than SMs, so the queue runs many groups at once."""
+    B, V, K, tau = 200, 4001, 4, 0.9
+    zp, zq, t, ua, ur = make_logits(B, V + 1, K, tau, seed=77)
+    zp = zp[..., 1:]
+    zq = zq[..., 1:]
+    t = torch.clamp(t, max=V - 1)
+    n0, expl = run(zp, zq, t, ua, ur, tau)
+    assert len(expl) <= 2, expl
+    assert len(set(n0.tolist())) > 2
+
+
+def test_empty_batch():
+    zp, zq, t, ua, ur = make_logits(1, 100, 3, 1.0, seed=5)
+    n, nx = sv.verify_sample_logits(zp[:0], zq[:0], t[:0], ua[:0], ur[:0], 1.0)
+    assert n.numel() == 0 and nx.numel() == 0

@@ -435,3 +435,14 @@ def test_edge_full():
     assert np.all(n[bt.meta["same"]] == 16)
     del bt
     _free()
+
+
+def test_empty_batch_every_entry_point():
+    """B = 0 is a valid call: nothing is launched and nothing is written."""
+    bt = make_inputs(3, "cuda", seed=9, B=3, V=2000, K=4)
+    p, q, t, ua, ur = bt.p[:0], bt.q[:0], bt.t[:0], bt.u_acc[:0], bt.u_res[:0]
+    for n, nx in (sv.verify_greedy(p, t), sv.verify_sample(p, q, t, ua, ur),
+                  sv.verify_round(bt.mode[:0], p, q, t, ua, ur)):
+        assert n.numel() == 0 and nx.numel() == 0
+    a, e = sv.alpha(p, q)
+    assert a.numel() == 0 and e.numel() == 0
