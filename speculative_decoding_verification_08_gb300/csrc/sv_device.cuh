@@ -789,7 +789,37 @@ __device__ int draw_core(int nseg, int64_t V, const float2 *seg, const float2 *b
     // the segment, the running mass before it, and the time T is past every segment
     int sg = -1;
     dd sbefore = zero;
-    if (L >= 0) {
+    if (L >= 0 && per <= kSegRegs) {
+        // every lane walks its own segments from its exclusive prefix (the
+        // same additions lane L alone would make); lane L's result is used
+        dd excl = shfl_up_dd(inc, 1);
+        if (lane == 0) excl = zero;
+        dd acc = dd_add(zero, excl), last_before = acc, fbefore = zero;
+        int last = -1, found = -1;
+#pragma unroll
+        for (int r = 0; r < kSegRegs; ++r) {
+            if (r0 + r < r1 && found < 0) {
+                const dd x = v[r];
+                const dd nx = dd_add(acc, x);
+                if (x.hi != 0.f) {
+                    last = r0 + r;
+                    last_before = acc;
+                    if (dd_gt(nx, T)) {
+                        found = r0 + r;
+                        fbefore = acc;
+                    }
+                }
+                acc = nx;
+            }
+        }
+        if (found < 0) {
+            found = last;
+            fbefore = last_before;
+        }
+        sg = __shfl_sync(0xffffffffu, found, L);
+        sbefore = shfl_dd(fbefore, L);
+    } else if (L >= 0) {
+        // rows longer than 32 * kSegRegs segments: lane L walks, loading the rest
         if (lane == L) {
             dd acc = before, last_before = before;
             int last = -1;
