@@ -141,3 +141,19 @@ def test_empty_batch():
     zp, zq, t, ua, ur = make_logits(1, 100, 3, 1.0, seed=5)
     n, nx = sv.verify_sample_logits(zp[:0], zq[:0], t[:0], ua[:0], ur[:0], 1.0)
     assert n.numel() == 0 and nx.numel() == 0
+
+
+def test_pinned_host_rows():
+    """Logits in page-locked host memory are read in place by the plain-load
+    workers (no copy).  With 16-byte-aligned rows the same rows on the device
+    take the bulk-copy workers, so equal outputs also check that the two
+    kernels compute bit for bit the same."""
+    B, V, K, tau = 24, 5004, 3, 1.1
+    zp, zq, t, ua, ur = make_logits(B, V, K, tau, seed=61)
+    n1, x1 = sv.verify_sample_logits(zp, zq, t, ua, ur, tau)
+    hp, hq = zp.cpu().pin_memory(), zq.cpu().pin_memory()
+    ht, hua, hur = t.cpu().pin_memory(), ua.cpu().pin_memory(), ur.cpu().pin_memory()
+    n2, x2 = sv.verify_sample_logits(hp, hq, ht, hua, hur, tau)
+    assert np.array_equal(n1.cpu().numpy(), n2.cpu().numpy())
+    assert np.array_equal(x1.cpu().numpy(), x2.cpu().numpy())
+    run(zp, zq, t, ua, ur, tau)
