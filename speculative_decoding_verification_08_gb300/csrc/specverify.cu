@@ -33,6 +33,12 @@
 #ifndef SV_ITEM_SEGS_SAMPLE
 #define SV_ITEM_SEGS_SAMPLE 128
 #endif
+#ifndef SV_ITEM_TAIL_PCT
+#define SV_ITEM_TAIL_PCT 25
+#endif
+#ifndef SV_ITEM_TAIL_SEGS
+#define SV_ITEM_TAIL_SEGS 16
+#endif
 #ifndef SV_ITEM_SEGS
 #define SV_ITEM_SEGS 32
 #endif
@@ -263,6 +269,21 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
     P.nchunks = (int32_t)((int64_t)P.B * cps);
     P.isegs = (int32_t)std::min<int64_t>(nseg, rule == sv::kSample ? SV_ITEM_SEGS_SAMPLE : SV_ITEM_SEGS);
     P.ichunks = (int32_t)((nseg + P.isegs - 1) / P.isegs);
+    P.ibig = P.ichunks;
+    P.itail = 0;
+    if (P.ichunks > 1 && SV_ITEM_TAIL_PCT > 0) {
+        // guided sizes: big chunks cover about the first (100 - SV_ITEM_TAIL_PCT) %
+        // of a row, small ones the rest; the small ones are queued after every
+        // big one, so the last items handed out are short
+        const int64_t big = std::max<int64_t>(
+            1, (nseg * (100 - SV_ITEM_TAIL_PCT) + 50 * (int64_t)P.isegs) / (100 * (int64_t)P.isegs));
+        const int64_t rest = nseg - big * P.isegs;
+        if (rest > 0) {
+            P.ibig = (int32_t)big;
+            P.itail = (int32_t)std::min<int64_t>(SV_ITEM_TAIL_SEGS, rest);
+            P.ichunks = (int32_t)(big + (rest + P.itail - 1) / P.itail);
+        }
+    }
     int sms = 0, occ = 0, tma_occ = 0, item_occ = 0;
     if (!device_info(rule, &sms, &occ, &tma_occ, &item_occ)) return SV_ECUDA;
     // bulk copies read device memory only: rows on the host take the plain loads

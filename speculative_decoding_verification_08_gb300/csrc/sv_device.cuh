@@ -99,7 +99,9 @@ struct Params {
     int32_t nchunks;            // bulk-copy path: chunks of the batch
     int32_t rows_on_host;       // host side: p or q is page-locked host memory
     int32_t ichunks;            // item kernel: items (chunks) per sequence
-    int32_t isegs;              // item kernel: segments per item
+    int32_t isegs;              // item kernel: segments per big item
+    int32_t ibig;               // item kernel: big items per sequence (the first ones of its row)
+    int32_t itail;              // item kernel: segments per small item (the rest of the row), 0: none
     // workspace
     uint32_t *status;
     uint32_t *queue;            // bulk-copy path: next chunk to hand out

@@ -2,10 +2,13 @@
 // (sequence, chunk) work items (sm_103a); used when every row starts on a
 // 16-byte boundary and the batch has at least one sequence per SM.
 //
-// A work item is `ichunks`-th part of one sequence: `isegs` consecutive
-// 1024-element segments of the rows that sequence needs.  Items are handed out
-// in order from a device-wide counter, so every CTA streams until the batch is
-// done and no SM is left with a larger share of the bytes than the others.
+// A work item is one of a sequence's `ichunks` parts: a run of consecutive
+// 1024-element segments of the rows that sequence needs.  When a row takes
+// several items, its first ~three quarters come in big items of `isegs`
+// segments and the rest in small ones of `itail`; every sequence's big items
+// are numbered before any small one.  Items are handed out in order from a
+// device-wide counter, so every CTA streams until the batch is done, and the
+// last items handed out -- the ones that set when the round ends -- are short.
 // Each CTA runs three roles:
 //  * a producer warp takes the next item, finds what the item needs one item
 //    ahead of use (sampling: the first rejection n from gathered p_i(t_i),
@@ -236,10 +239,23 @@ struct ItemProducer {
         ItemPre x = {};
         x.b = P.B;
         if (item >= P.B * P.ichunks) return x;
-        const int b = item / P.ichunks, c = item - b * P.ichunks;
+        // every sequence's big items first (sequence-major), then the small ones
+        int b;
+        const int nbig = P.B * P.ibig;
+        if (item < nbig) {
+            b = item / P.ibig;
+            const int c = item - b * P.ibig;
+            x.s0 = c * P.isegs;
+            x.s1 = min(P.nseg, x.s0 + P.isegs);
+        } else {
+            const int nsmall = P.ichunks - P.ibig;
+            const int j = item - nbig;
+            b = j / nsmall;
+            const int c = j - b * nsmall;
+            x.s0 = P.ibig * P.isegs + c * P.itail;
+            x.s1 = min(P.nseg, x.s0 + P.itail);
+        }
         x.b = b;
-        x.s0 = c * P.isegs;
-        x.s1 = min(P.nseg, x.s0 + P.isegs);
         x.rule = kRule == kPerSequence ? (int)ld_early(P.mode + b) : kRule;
         const int64_t tb = (int64_t)b * P.K;
         if (lane < P.K) x.t0 = ld_early(P.t + tb + lane);
