@@ -618,9 +618,16 @@ constexpr int kLgPartBytes = kLgStageSegs * kSeg * 4;
 constexpr int kLgStageBytes = 2 * kLgPartBytes;
 static_assert(kLgChunkSegs % kLgStageSegs == 0, "a chunk is whole stages");
 static_assert(kLgStages <= 32, "stage bookkeeping is a 32-bit mask");
-// Consumer warps: eight, or fewer when the ring is short -- a ticket's parity
-// wait needs consumers <= stages + 1 (see wait_ticket).
-constexpr int kLgConsumers = kLgStages + 1 < kTmaConsumers ? kLgStages + 1 : kTmaConsumers;
+// A stage is taken by kLgStageSegs consumers, one segment each (a ticket is a
+// share of a stage), so no warp holds a stage for more than one segment's
+// work.  A share's parity wait is unambiguous while no consumer can take a
+// share of the same position two fills ahead: the other consumers can hold
+// at most (stages - 1) * shares + shares - 1 filled shares beyond it, so
+// consumers <= stages * shares + 1.  Seven consumers (registers allow no
+// more at two CTAs per SM).
+constexpr int kLgShares = kLgStageSegs;
+constexpr int kLgConsumers = 7;
+static_assert(kLgConsumers <= kLgStages * kLgShares + 1, "too few ring stages for the consumers");
 constexpr int kLgProducerWarp = kLgConsumers;
 
 // A chunk the producer has taken.
@@ -635,7 +642,7 @@ struct LgShared {
     unsigned long long full[kLgStages];
     unsigned long long empty[kLgStages];
     LgStage meta[kLgStages];
-    int left[kLgSlots];  // stages of the chunk not yet done (0: free)
+    int left[kLgSlots];  // stage shares of the chunk not yet done (0: free)
 };
 static_assert(sizeof(LgShared) <= kTmaBufOffset, "shared header too large");
 constexpr int kLgRingThreads = (kLgConsumers + 1) * 32;
@@ -707,7 +714,8 @@ __device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &
             }
         }
         if (free)
-            *(volatile int *)&sh.left[slot] = (int)((s1 - s0 + kLgStageSegs - 1) / kLgStageSegs);
+            *(volatile int *)&sh.left[slot] =
+                (int)((s1 - s0 + kLgStageSegs - 1) / kLgStageSegs) * kLgShares;
     }
     if (!__shfl_sync(0xffffffffu, free, 0)) {
         pr.ok = false;
@@ -772,8 +780,8 @@ __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *b
         if (lane == 0) hn = atomicAdd(L.head, 1ull);
         lg_issue_chunk(L, sh, pr, ch, nchunks_here, lane);
     }
-    // tell every consumer to stop
-    for (int w = 0; w < kLgConsumers; ++w) {
+    // tell every consumer to stop (each stop stage serves kLgShares of them)
+    for (int w = 0; w < (kLgConsumers + kLgShares - 1) / kLgShares; ++w) {
         LgStage m = {};
         pr.issue(m);
     }
@@ -832,13 +840,14 @@ __device__ __noinline__ void lg_ragged_mass(const float *sp, const float *sq, co
     store_sums(seg, blk, m.s, v, lane);
 }
 
-// Waits (bounded) until ring position t % kLgStages holds the fill of ticket t
-// (the same two-step wait as wait_ticket, on this ring's size; kLgConsumers
-// keeps it unambiguous).
+// Waits (bounded) until the stage of share ticket t holds its fill (the same
+// two-step wait as wait_ticket, per stage ticket t / kLgShares, on this ring's
+// size; kLgConsumers keeps it unambiguous).
 __device__ __forceinline__ bool lg_wait_ticket(unsigned long long *full, unsigned long long *empty,
                                                int t) {
-    const int k = t % kLgStages;
-    const uint32_t phase = (uint32_t)(t / kLgStages) & 1u;
+    const int ts = t / kLgShares;
+    const int k = ts % kLgStages;
+    const uint32_t phase = (uint32_t)(ts / kLgStages) & 1u;
     return mbar_wait(&empty[k], phase ^ 1u) && mbar_wait(&full[k], phase);
 }
 
@@ -862,7 +871,8 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
         int t = 0;
         if (lane == 0) t = atomicAdd(&sh.ticket, 1);
         t = __shfl_sync(0xffffffffu, t, 0);
-        const int k = t % kLgStages;
+        const int k = (t / kLgShares) % kLgStages;
+        const int j = t % kLgShares;  // this share's segment of the stage
         const float *sp = reinterpret_cast<const float *>(buf + (size_t)k * kLgStageBytes);
         const float *sq = reinterpret_cast<const float *>(buf + (size_t)k * kLgStageBytes + kLgPartBytes);
         if (!__all_sync(0xffffffffu, lg_wait_ticket(sh.full, sh.empty, t))) {
@@ -875,11 +885,11 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
             return;
         }
         const bool pair = m.g1 != nullptr;
+        const int o = j * kSeg;  // the segment's offset in the stage
         if (m.kind == (int)kLgNorm) {
-            for (int j = 0; j < m.ns; ++j) {
-                const int o = j * kSeg;  // the segment's offset in the stage
+            if (j < m.ns) {
                 RowNorm oa, ob = none;
-                if (o + kSeg <= m.c) {   // a full segment, straight from shared memory
+                if (o + kSeg <= m.c) {  // a full segment, straight from shared memory
                     const float4 *p4 = reinterpret_cast<const float4 *>(sp + o);
                     const float4 *q4 = reinterpret_cast<const float4 *>(sq + o);
                     float4 xa[kVecPerLane], xb[kVecPerLane];
@@ -888,50 +898,53 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
                         xa[v] = p4[lane + 32 * v];
                         if (pair) xb[v] = q4[lane + 32 * v];
                     }
+                    release_stage(sh.empty, k, lane);
                     oa = seg_norm(xa, L.c);
                     if (pair) ob = seg_norm(xb, L.c);
                 } else {
                     const int n = min(kSeg, m.n - o), c = max(0, min(kSeg, m.c - o));
                     oa = lg_ragged_norm(sp + o, m.g0 + o, n, c, L.c, lane);
                     if (pair) ob = lg_ragged_norm(sq + o, m.g1 + o, n, c, L.c, lane);
+                    release_stage(sh.empty, k, lane);
                 }
                 if (lane == 0) lg_store_pair(L, m.b, m.s + j, oa, ob);
+            } else {
+                release_stage(sh.empty, k, lane);
             }
-            release_stage(sh.empty, k, lane);
             if (lg_chunk_done(sh, m.slot, lane)) lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
         } else {
             const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};
             const float ia = __frcp_rn(np.s.hi), ib = pair ? __frcp_rn(nq.s.hi) : 0.f;
             float2 *seg = L.seg + (int64_t)m.b * L.nseg;
             float2 *blk = L.blk + (int64_t)m.b * L.nseg * kBlocks;
-            for (int j = 0; j < m.ns; ++j) {
-                const int o = j * kSeg;
-                if (o + kSeg <= m.c) {
-                    const float4 *p4 = reinterpret_cast<const float4 *>(sp + o);
-                    const float4 *q4 = reinterpret_cast<const float4 *>(sq + o);
-                    dd v[kBlocks];
+            if (j < m.ns && o + kSeg <= m.c) {
+                const float4 *p4 = reinterpret_cast<const float4 *>(sp + o);
+                const float4 *q4 = reinterpret_cast<const float4 *>(sq + o);
+                dd v[kBlocks];
 #pragma unroll
-                    for (int w = 0; w < kBlocks; ++w) {
-                        const float4 x = p4[lane + 32 * w];
-                        const float4 y = pair ? q4[lane + 32 * w] : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[w] = dd{sum4(make_float4(lg_mass(x.x, y.x, pair, np, nq, ia, ib, L.c),
-                                                   lg_mass(x.y, y.y, pair, np, nq, ia, ib, L.c),
-                                                   lg_mass(x.z, y.z, pair, np, nq, ia, ib, L.c),
-                                                   lg_mass(x.w, y.w, pair, np, nq, ia, ib, L.c))),
-                                  0.f};
-                    }
-                    store_sums(seg, blk, m.s + j, v, lane);
-                } else {
-                    LgStage mj = m;
-                    mj.s = m.s + j;
-                    mj.n = min(kSeg, m.n - o);
-                    mj.c = max(0, min(kSeg, m.c - o));
-                    mj.g0 = m.g0 + o;
-                    mj.g1 = pair ? m.g1 + o : nullptr;
-                    lg_ragged_mass(sp + o, sq + o, mj, np, nq, ia, ib, seg, blk, L.c, lane);
+                for (int w = 0; w < kBlocks; ++w) {
+                    const float4 x = p4[lane + 32 * w];
+                    const float4 y = pair ? q4[lane + 32 * w] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[w] = dd{sum4(make_float4(lg_mass(x.x, y.x, pair, np, nq, ia, ib, L.c),
+                                               lg_mass(x.y, y.y, pair, np, nq, ia, ib, L.c),
+                                               lg_mass(x.z, y.z, pair, np, nq, ia, ib, L.c),
+                                               lg_mass(x.w, y.w, pair, np, nq, ia, ib, L.c))),
+                              0.f};
                 }
+                release_stage(sh.empty, k, lane);
+                store_sums(seg, blk, m.s + j, v, lane);
+            } else if (j < m.ns) {
+                LgStage mj = m;
+                mj.s = m.s + j;
+                mj.n = min(kSeg, m.n - o);
+                mj.c = max(0, min(kSeg, m.c - o));
+                mj.g0 = m.g0 + o;
+                mj.g1 = pair ? m.g1 + o : nullptr;
+                lg_ragged_mass(sp + o, sq + o, mj, np, nq, ia, ib, seg, blk, L.c, lane);
+                release_stage(sh.empty, k, lane);
+            } else {
+                release_stage(sh.empty, k, lane);
             }
-            release_stage(sh.empty, k, lane);
             if (lg_chunk_done(sh, m.slot, lane))
                 lg_mass_arrive(L, m.b, m.i, m.g, m.tasks, true, np, nq, ia, ib, lane);
         }
@@ -946,7 +959,7 @@ __global__ void __launch_bounds__(kLgRingThreads, 2) logits_ring_kernel(const Lo
     if (threadIdx.x == 0) {
         for (int i = 0; i < kLgStages; ++i) {
             mbar_init(&sh.full[i], 1);
-            mbar_init(&sh.empty[i], 1);
+            mbar_init(&sh.empty[i], kLgShares);  // released by every share
         }
         sh.ticket = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
