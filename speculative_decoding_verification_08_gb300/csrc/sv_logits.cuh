@@ -607,10 +607,10 @@ constexpr int kLgSlots = 32;
 // The ring: kLgStages stages, each kLgStageSegs consecutive segments of the
 // row pair (or of one row), p's part first.
 #ifndef SV_LG_STAGE_SEGS
-#define SV_LG_STAGE_SEGS 2
+#define SV_LG_STAGE_SEGS 4
 #endif
 #ifndef SV_LG_STAGES
-#define SV_LG_STAGES 6
+#define SV_LG_STAGES 3
 #endif
 constexpr int kLgStageSegs = SV_LG_STAGE_SEGS;
 constexpr int kLgStages = SV_LG_STAGES;
