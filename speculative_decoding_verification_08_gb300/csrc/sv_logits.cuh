@@ -575,13 +575,15 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const Logits
 // ---------------------------------------------------------------------------
 // bulk-copy workers (16-byte-aligned device rows): per CTA one producer warp
 // takes chunks of kLgChunkSegs segment tasks of one group from the queue and
-// moves their row segments into a ring of shared-memory stages with
-// cp.async.bulk; eight consumer warps take the stages in order and run the
-// tasks on them.  The producer waits for the group of its next chunk (bounded,
-// as above); the copies already issued keep the consumers busy meanwhile.
+// moves their row segments into a ring of shared-memory stages (kLgStageSegs
+// segments of each row per stage) with cp.async.bulk; kLgConsumers consumer
+// warps take the stages' segments in order, one segment per ticket, and run
+// the tasks on them.  The producer waits for the group of its next chunk
+// (bounded, as above); the copies already issued keep the consumers busy
+// meanwhile.
 
 struct LgStage {
-    const float *g0;  // global start of the p segment and of the q segment (null: one row)
+    const float *g0;  // global start of the stage's p part and of its q part (null: one row)
     const float *g1;
     unsigned long long g;  // group
     int64_t s;        // first segment
