@@ -36,6 +36,7 @@ KERNEL_SOURCES = [
     "speculative_decoding_verification_08_gb300/csrc/sv_tma.cuh",
     "speculative_decoding_verification_08_gb300/csrc/sv_item.cuh",
     "speculative_decoding_verification_08_gb300/csrc/sv_logits.cuh",
+    "speculative_decoding_verification_08_gb300/csrc/sv_alpha.cuh",
     "speculative_decoding_verification_08_gb300/csrc/specverify.cu",
 ]
 
