@@ -56,6 +56,10 @@
  *                            next_token = -1 for that sequence;
  *       SV_STATUS_ZERO_MASS  the distribution to draw from has zero mass;
  *       SV_STATUS_OVERFLOW   a commit would pass max_len (nothing written);
+ *                            from sv_verify_sample_logits: its workspace
+ *                            held a count it cannot have left there (a
+ *                            workspace reused without re-initialising it
+ *                            after SV_STATUS_TIMEOUT, or overwritten);
  *       SV_STATUS_BAD_MODE   a round mode other than 0 or 1 (n = 0, next = -1);
  *       SV_STATUS_TIMEOUT    a bounded wait inside a kernel gave up (the
  *                            round's outputs are not meaningful).

@@ -157,3 +157,30 @@ def test_pinned_host_rows():
     assert np.array_equal(n1.cpu().numpy(), n2.cpu().numpy())
     assert np.array_equal(x1.cpu().numpy(), x2.cpu().numpy())
     run(zp, zq, t, ua, ur, tau)
+
+
+def test_timeout_is_reported_and_the_context_stays_usable():
+    """A bounded wait that runs out ends the launch with SV_STATUS_TIMEOUT --
+    no hang, no fault -- and once the workspace is initialised again the same
+    context verifies correctly.  The wait is made to run out by presetting the
+    workspace's count of appended groups (the u64 at byte 24 of its header)
+    past the group list: every append then falls outside the list and is
+    dropped (SV_STATUS_OVERFLOW), so the workers wait for groups that never
+    come, each for the 250 ms limit."""
+    SV_STATUS_OVERFLOW, SV_STATUS_TIMEOUT = 4, 16
+    B, V, K, tau = 32, 4096, 3, 1.0
+    x = make_logits(B, V, K, tau, seed=5150)
+    ws = sv.Workspace(B, K, V)
+    ws.buf.view(torch.int64)[3] = 1 << 40
+    sv.verify_sample_logits(*x, tau, ws=ws)
+    st = ws.status()
+    assert st & SV_STATUS_TIMEOUT and st & SV_STATUS_OVERFLOW, st
+    # the context is fine: initialise the workspace again and verify
+    assert sv.load().sv_workspace_init(ws.ptr, ctypes.c_size_t(ws.nbytes), None) == 0
+    n1, x1 = sv.verify_sample_logits(*x, tau, ws=ws)
+    assert ws.status() == 0
+    n2, x2 = sv.verify_sample_logits(*x, tau)     # a fresh workspace: the same bits
+    assert np.array_equal(n1.cpu().numpy(), n2.cpu().numpy())
+    assert np.array_equal(x1.cpu().numpy(), x2.cpu().numpy())
+    n0, expl = run(*x, tau)
+    assert len(expl) <= 1
