@@ -82,7 +82,12 @@ struct ItemSlot {
     int miss;      // greedy: kFlagBase - first missed row seen in this item
     int sbuf;      // shared-memory sum buffer holding this item's sums, or -1
     unsigned long long keys[kMaxK + 1];  // greedy: packed (value, index) maximum per row
+    unsigned long long tkey0;  // greedy: pack_key(p_0(t_0), t_0) once known, else 0
 };
+
+// ItemMeta::tok of a greedy row-0 stage issued before the draft data arrived:
+// the token's key is read from the item slot (ItemSlot::tkey0) instead.
+constexpr int kTokInSlot = -2;
 
 // What a consumer needs to know about a stage beyond its item slot (the
 // sequence, n and hence the row pointers live there): 32 bytes, written with
@@ -93,7 +98,7 @@ struct __align__(16) ItemMeta {
     int kind;    // StageKind
     int nparts;  // segments in the stage (kMass, kArgmax: 1 or 2)
     int row;     // greedy: row index
-    int tok;     // greedy: the row's draft token, -1 for the bonus row
+    int tok;     // greedy: the row's draft token, -1 for the bonus row, kTokInSlot
     float pt;    // greedy: p_row(tok)
     int pad;
 };
@@ -338,14 +343,43 @@ struct ItemProducer {
         return __shfl_sync(0xffffffffu, stages, 0);
     }
 
-    // Greedy rows 0..K of the item's segments, in order, two segments per
-    // stage.  The sequence's flag is read one row ahead of its use, so the
-    // check costs no wait.
-    __device__ int stream_greedy(const ItemPre &c, int x) {
+    // Lane 0 only: greedy row i's stages for segments [from, to) of item
+    // slot x, two segments per stage, until a miss in an earlier row shows up
+    // in the slot or in `flag` (the sequence's flag as last read).
+    __device__ int put_greedy_row(int b, int x, int i, int tok, float pt, int from, int to, int flag,
+                                  bool &stop) {
+        const float *pr = prow(P, b, i);
+        ItemMeta m = {};
+        m.kind = kArgmax;
+        m.slot = x;
+        m.row = i;
+        m.tok = tok;
+        m.pt = pt;
         int stages = 0;
-        int seen = 0;  // the sequence's flag as last read (lane 0)
+        for (int s = from; s < to; s += 2) {
+            if (max(*(volatile int *)&sh.slot[x].miss, flag) > kFlagBase - i) {
+                stop = true;  // an earlier row missed
+                break;
+            }
+            m.s = s;
+            m.nparts = s + 1 < to ? 2 : 1;
+            const int c1 = m.nparts == 2 ? copy_len(s + 1) : 0;
+            if (!put(m, pr + (int64_t)s * kSeg, copy_len(s), pr + (int64_t)(s + 1) * kSeg, c1)) {
+                ok = false;
+                stop = true;
+                break;
+            }
+            ++stages;
+        }
+        return stages;
+    }
+
+    // Greedy rows first..K of the item's segments, in order.  The sequence's
+    // flag is read one row ahead of its use, so the check costs no wait.
+    __device__ int stream_greedy(const ItemPre &c, int x, int first = 0, int seen = 0) {
+        int stages = 0;
         bool stop = !ok;
-        for (int i = 0; i <= P.K && !stop; ++i) {
+        for (int i = first; i <= P.K && !stop; ++i) {
             int tok = -1;
             float pt = 0.f;
             if (i < P.K) {
@@ -355,28 +389,7 @@ struct ItemProducer {
             if (lane == 0) {
                 const int flag_now = seen;
                 seen = ld_volatile(P.miss + c.b);  // used at the next row
-                const float *pr = prow(P, c.b, i);
-                ItemMeta m = {};
-                m.kind = kArgmax;
-                m.slot = x;
-                m.row = i;
-                m.tok = tok;
-                m.pt = pt;
-                for (int s = c.s0; s < c.s1; s += 2) {
-                    if (max(*(volatile int *)&sh.slot[x].miss, flag_now) > kFlagBase - i) {
-                        stop = true;  // an earlier row missed
-                        break;
-                    }
-                    m.s = s;
-                    m.nparts = s + 1 < c.s1 ? 2 : 1;
-                    const int c1 = m.nparts == 2 ? copy_len(s + 1) : 0;
-                    if (!put(m, pr + (int64_t)s * kSeg, copy_len(s), pr + (int64_t)(s + 1) * kSeg, c1)) {
-                        ok = false;
-                        stop = true;
-                        break;
-                    }
-                    ++stages;
-                }
+                stages += put_greedy_row(c.b, x, i, tok, pt, c.s0, c.s1, flag_now, stop);
                 if (*(volatile int *)&sh.slot[x].miss >= kFlagBase - i) stop = true;
             }
             stop = __shfl_sync(0xffffffffu, stop, 0) != 0;
@@ -384,7 +397,139 @@ struct ItemProducer {
         sync_ok();
         return __shfl_sync(0xffffffffu, stages, 0);
     }
+
+    // A greedy item begun but not gathered.  Row 0 is read whatever the
+    // draft, so its first `early` stages go out before the gather waits for
+    // the draft ids; the row's token key goes into the slot once p_0(t_0) is
+    // in, after the row's last stage; rows 1..K then as above.  ns becomes
+    // kNBad when a draft id is invalid (nothing past the early stages is read).
+    __device__ int stream_greedy_lazy(ItemPre &c, int x, int early, int &ns) {
+        const int split = min(c.s1, c.s0 + 2 * early);
+        const int tok0 = P.K > 0 ? kTokInSlot : -1;
+        int stages = 0, seen = 0;
+        bool stop = !ok;
+        if (lane == 0 && !stop) {
+            seen = ld_volatile(P.miss + c.b);
+            stages = put_greedy_row(c.b, x, 0, tok0, 0.f, c.s0, split, 0, stop);
+        }
+        sync_ok();
+        gather(c);
+        if (c.bad) {
+            ns = kNBad;
+            return __shfl_sync(0xffffffffu, stages, 0);
+        }
+        if (lane == 0 && ok) {
+            stages += put_greedy_row(c.b, x, 0, tok0, 0.f, split, c.s1, 0, stop);
+            if (P.K > 0) *(volatile unsigned long long *)&sh.slot[x].tkey0 = pack_key(c.pt0, c.t0);
+            if (*(volatile int *)&sh.slot[x].miss >= kFlagBase) stop = true;
+        }
+        sync_ok();
+        stages = __shfl_sync(0xffffffffu, stages, 0);
+        seen = __shfl_sync(0xffffffffu, seen, 0);
+        if (__shfl_sync(0xffffffffu, stop, 0) || !ok) return stages;
+        return stages + stream_greedy(c, x, 1, seen);
+    }
+
+    // Lane 0 of the warp waits (bounded) for a free item slot: its index, or
+    // -1 once a wait gave up.
+    __device__ int free_slot(IdleClock &clk) {
+        while (ok) {
+            unsigned m = 0;
+#pragma unroll
+            for (int i = 0; i < kItemSlots; ++i)
+                if (*(volatile int *)&sh.slot[i].state == 0) m |= 1u << i;
+            if (m) {
+                clk.progress();
+                return __ffs(m) - 1;
+            }
+            if (!clk.idle()) ok = false;
+        }
+        return -1;
+    }
 };
+
+// After the last item: stop the consumers, then the retire warp; the last CTA
+// to stop taking items resets the counter for the next round.
+__device__ void item_produce_end(const Params &P, ItemShared &sh, ItemProducer &pr, int lane) {
+    // this CTA reads no more rows into its ring: the next grid may start taking
+    // SM slots as they free up (it waits for this grid to end before it reads)
+    grid_dependents_may_launch();
+    if (lane == 0 && pr.ok) {
+        ItemMeta m = {};
+        m.kind = kStop;
+        for (int i = 0; i < kTmaConsumers && pr.ok; ++i)  // one stop per consumer
+            pr.ok = pr.put(m, nullptr, 0, nullptr, 0);
+    }
+    pr.sync_ok();
+    if (!pr.ok && lane == 0) atomicOr(P.status, kStatusTimeout);
+    if (lane == 0) {
+        __threadfence_block();
+        *(volatile int *)&sh.producer_done = pr.ok ? 1 : 2;
+        __threadfence();
+        if (atomicAdd(P.queue + 1, 1u) == gridDim.x - 1) {
+            atomicExch(P.queue, 0u);
+            atomicExch(P.queue + 1, 0u);
+        }
+    }
+    if (!pr.ok && lane == 0) {
+        // a wait gave up: let the copies still in flight land before leaving
+        // (ring position i last held fill i + kStages * r, r = its round)
+        for (int i = 0; i < kStages && i < pr.fills; ++i) {
+            const int r = (pr.fills - 1 - i) / kStages;
+            mbar_wait(&sh.full[i], (uint32_t)r & 1u);
+        }
+    }
+}
+
+// The greedy producer.  A CTA holds one item at a time and claims the next
+// once the current one's copies are out (CTA c starts with item c).  A greedy
+// item needs no draft data before its first copies, so there is nothing to
+// fetch ahead, and the last items go to the CTAs that finish first.
+#ifndef SV_GREEDY_EARLY
+#define SV_GREEDY_EARLY 2
+#endif
+__device__ void item_produce_greedy(const Params &P, ItemShared &sh, unsigned char *buf, int lane) {
+    ItemProducer pr(P, sh, buf, lane);
+    IdleClock clk;
+    int item = (int)blockIdx.x;
+    while (pr.ok) {
+        ItemPre c = pr.begin<kGreedy>(item);
+        if (c.b >= P.B) break;
+        const int x = __shfl_sync(0xffffffffu, pr.free_slot(clk), 0);
+        pr.sync_ok();
+        if (x < 0) break;
+        ItemSlot &sl = sh.slot[x];
+        for (int i = lane; i <= P.K; i += 32) sl.keys[i] = 0ull;
+        unsigned claim = 0;
+        if (lane == 0) {
+            sl.b = c.b;
+            sl.rule = kGreedy;
+            sl.ns = 1;
+            sl.issued = 0;
+            sl.consumed = 0;
+            sl.miss = 0;
+            sl.sbuf = -1;
+            sl.tkey0 = 0ull;
+            __threadfence_block();
+            *(volatile int *)&sl.state = 1;
+        }
+        __syncwarp();
+        int ns = 1;
+        const int stages = pr.stream_greedy_lazy(c, x, SV_GREEDY_EARLY, ns);
+        if (lane == 0) {
+            sl.ns = ns;
+            sl.issued = stages;
+            __threadfence_block();
+            *(volatile int *)&sl.state = 2;
+            // claimed once this item's copies are out, while the ring still
+            // holds them (claimed earlier, the item measured slower)
+            claim = atomicAdd(P.queue, 1u);
+        }
+        __syncwarp();
+        item = (int)gridDim.x + (int)__shfl_sync(0xffffffffu, claim, 0);
+    }
+    item_produce_end(P, sh, pr, lane);
+}
 
 template <int kRule>
 __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf,
@@ -401,20 +546,8 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
     pr.gather(nxt);
     ItemPre nxt2 = pr.begin<kRule>(pr.take());
     while (pr.ok && cur.b < P.B) {
-        // a free item slot (the decider frees them)
-        int x = -1;
-        while (pr.ok) {
-            unsigned m = 0;
-#pragma unroll
-            for (int i = 0; i < kItemSlots; ++i)
-                if (*(volatile int *)&sh.slot[i].state == 0) m |= 1u << i;
-            if (m) {
-                x = __ffs(m) - 1;
-                clk.progress();
-                break;
-            }
-            if (!clk.idle()) pr.ok = false;
-        }
+        // a free item slot (the retire warp frees them)
+        const int x = pr.free_slot(clk);
         if (x < 0) break;
         const ItemPre c = cur;
         const int ns = pr.finish(c);
@@ -468,36 +601,7 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
         }
         __syncwarp();
     }
-    // this CTA reads no more rows into its ring: the next grid may start taking
-    // SM slots as they free up (it waits for this grid to end before it reads)
-    grid_dependents_may_launch();
-    // stop the consumers, then the retire warp
-    if (lane == 0 && pr.ok) {
-        ItemMeta m = {};
-        m.kind = kStop;
-        for (int i = 0; i < kTmaConsumers && pr.ok; ++i)  // one stop per consumer
-            pr.ok = pr.put(m, nullptr, 0, nullptr, 0);
-    }
-    pr.sync_ok();
-    if (!pr.ok && lane == 0) atomicOr(P.status, kStatusTimeout);
-    if (lane == 0) {
-        __threadfence_block();
-        *(volatile int *)&sh.producer_done = pr.ok ? 1 : 2;
-        // the last CTA to stop taking items resets the counter for the next round
-        __threadfence();
-        if (atomicAdd(P.queue + 1, 1u) == gridDim.x - 1) {
-            atomicExch(P.queue, 0u);
-            atomicExch(P.queue + 1, 0u);
-        }
-    }
-    if (!pr.ok && lane == 0) {
-        // a wait gave up: let the copies still in flight land before leaving
-        // (ring position i last held fill i + kStages * r, r = its round)
-        for (int i = 0; i < kStages && i < pr.fills; ++i) {
-            const int r = (pr.fills - 1 - i) / kStages;
-            mbar_wait(&sh.full[i], (uint32_t)r & 1u);
-        }
-    }
+    item_produce_end(P, sh, pr, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -556,14 +660,18 @@ __device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf
             if (m.nparts == 2)
                 stage_argmax(sq, n1, c1, g + kSeg, (int64_t)(m.s + 1) * kSeg, lane, bv, bi);
             release_stage(sh.empty, k, lane);
-            if (m.tok >= 0) {
-                const bool beats = bi >= 0 && (bv > m.pt || (bv == m.pt && bi < m.tok));
-                if (__any_sync(0xffffffffu, beats) && lane == 0) {
-                    atomicMax(&sl.miss, kFlagBase - m.row);
-                    atomicMax(P.miss + b, kFlagBase - m.row);  // other CTAs stop sooner
-                }
-            }
             const unsigned long long key = warp_max_u64(pack_key(bv, bi));
+            // the draft token loses the row when a larger key (a larger value,
+            // or an equal one at a lower index) is in it; a row-0 stage taken
+            // before the token's key is known goes untested, which only costs
+            // the early stop (the decide reads the row maxima)
+            const unsigned long long tk =
+                m.tok >= 0 ? pack_key(m.pt, m.tok)
+                           : (m.tok == kTokInSlot ? *(volatile unsigned long long *)&sl.tkey0 : 0ull);
+            if (lane == 0 && tk && key > tk) {
+                atomicMax(&sl.miss, kFlagBase - m.row);
+                atomicMax(P.miss + b, kFlagBase - m.row);  // other CTAs stop sooner
+            }
             if (lane == 0 && key) atomicMax(&sl.keys[m.row], key);
         }
         __syncwarp();
@@ -593,12 +701,19 @@ __device__ void item_decide_sequence(const Params &P, unsigned long long *dbar, 
         if (ns == kNBad) {
             st = kStatusBadToken;
         } else {
-            // the miss flag and every row's key in one round trip
-            const int f = __shfl_sync(0xffffffffu, lane == 0 ? ld_l2(P.miss + b) : 0, 0);
+            // every row's key and draft token in one round trip.  An item stops
+            // streaming a row only after a miss in an earlier row, so every row
+            // up to the first miss is whole, and the first row whose maximum is
+            // not its draft token is that miss.
+            const int64_t tb = (int64_t)b * P.K;
             const unsigned long long k0 = lane <= P.K ? ld_l2(best + lane) : 0ull;
             const unsigned long long k1 = lane + 32 <= P.K ? ld_l2(best + lane + 32) : 0ull;
             const unsigned long long k2 = lane + 64 <= P.K ? ld_l2(best + lane + 64) : 0ull;
-            n = f ? kFlagBase - f : P.K;
+            const int32_t t0 = lane < P.K ? ld_early(P.t + tb + lane) : -1;
+            const int32_t t1 = lane + 32 < P.K ? ld_early(P.t + tb + lane + 32) : -1;
+            const unsigned m0 = __ballot_sync(0xffffffffu, lane < P.K && key_index(k0) != t0);
+            const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < P.K && key_index(k1) != t1);
+            n = m0 ? __ffs(m0) - 1 : (m1 ? 32 + __ffs(m1) - 1 : P.K);
             const unsigned long long mine = n < 32 ? k0 : (n < 64 ? k1 : k2);
             const unsigned long long key = __shfl_sync(0xffffffffu, mine, n & 31);
             next = key ? key_index(key) : 0;
@@ -839,7 +954,10 @@ __global__ void __launch_bounds__(kItemThreads, 2) item_round_kernel(const Param
     // launched as a programmatic dependent: the set-up above may overlap the
     // previous grid; nothing in global memory is touched before it is done
     wait_for_primary_grid();
-    if (warp == kItemProducerWarp) item_produce<kRule>(P, sh, buf, smem + kItemHeaderBytes, lane);
+    if (warp == kItemProducerWarp) {
+        if constexpr (kRule == kGreedy) item_produce_greedy(P, sh, buf, lane);
+        else item_produce<kRule>(P, sh, buf, smem + kItemHeaderBytes, lane);
+    }
     else if (warp == kItemRetireWarp) item_retire_loop(P, sh, lane);
     else if (warp == kItemDecideWarpA || warp == kItemDecideWarpB) {
         const int d = warp == kItemDecideWarpA ? 0 : 1;
