@@ -64,14 +64,14 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
 // Workspace layout:
 // [header | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] | arrive[B] |
 //  groups[B][K+2] | seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2] |
-//  fnorm[B][2]], every region 256-byte aligned; everything before seg must start
-// at zero (and every call leaves it so).  Header: status (u32 at 0), the
+//  fnorm[B][2] | order[B]], every region 256-byte aligned; everything before seg
+// must start at zero (and every call leaves it so).  Header: status (u32 at 0), the
 // chunk queue and its exit count (u32 at 4 and 8), the logits path's task
 // counter and appended groups (u64 at 16 and 24), finished sequences and
 // exited workers (u32 at 32 and 36).
 struct Layout {
     size_t status, queue, miss, nstate, done, ptok, best, arrive, groups, seg, blk, udd, norm,
-        fnorm, total;
+        fnorm, order, total;
 };
 constexpr size_t kLgHead = 16, kLgTail = 24, kLgDone = 32, kLgExit = 36;
 
@@ -105,6 +105,8 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     off += round_up((size_t)B * (size_t)K * 2 * sizeof(float2));
     L.fnorm = off;
     off += round_up((size_t)B * 2 * sizeof(float4));
+    L.order = off;
+    off += round_up((size_t)B * sizeof(int2));
     L.total = off;
     return L;
 }
@@ -315,9 +317,14 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
             case sv::kSample:
                 return launch_dependent(sv::item_round_kernel<sv::kSample>, (unsigned)grid,
                                         sv::kItemThreads, sv::kItemSmemBytes, P, st);
-            default:
+            default: {
+                // the order the items take the sequences in (greedy ones first)
+                int rc = launch_dependent(sv::mode_order_kernel, 1u, sv::kOrderThreads, 0, P, st);
+                if (rc != SV_OK) return rc;
+                g_last_kernels = 2;
                 return launch_dependent(sv::item_round_kernel<sv::kPerSequence>, (unsigned)grid,
                                         sv::kItemThreads, sv::kItemSmemBytes, P, st);
+            }
         }
     }
     const bool tma = aligned && tma_occ > 0;
@@ -427,6 +434,7 @@ int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
     P.seg = reinterpret_cast<float2 *>(base + L.seg);
     P.blk = reinterpret_cast<float2 *>(base + L.blk);
     P.udd = reinterpret_cast<float2 *>(base + L.udd);
+    P.order = reinterpret_cast<int2 *>(base + L.order);
     return SV_OK;
 }
 

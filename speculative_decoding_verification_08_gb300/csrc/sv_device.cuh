@@ -113,6 +113,8 @@ struct Params {
     float2 *seg;                // [B][nseg] double-fp32 segment sums
     float2 *blk;                // [B][nseg][kBlocks] double-fp32 128-element block sums
     float2 *udd;                // [B] u_resample split into two fp32 parts
+    int2 *order;                // [B] item kernel, mixed rounds: {sequence, mode} in the
+                                // order sequences are taken (greedy ones first)
 };
 
 // ---------------------------------------------------------------------------

@@ -166,6 +166,13 @@ __device__ __forceinline__ uint8_t ld_early(const uint8_t *p) {
     return (uint8_t)v;
 }
 
+// A load from L2 (not L1) of data a primary grid wrote before this grid's wait.
+__device__ __forceinline__ int2 ld_l2(const int2 *p) {
+    int2 v;
+    asm volatile("ld.global.cg.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
 // ---------------------------------------------------------------------------
 // producer
 
@@ -260,8 +267,16 @@ struct ItemProducer {
             x.s0 = P.ibig * P.isegs + c * P.itail;
             x.s1 = min(P.nseg, x.s0 + P.itail);
         }
+        if constexpr (kRule == kPerSequence) {
+            // mixed rounds take the sequences in the order mode_order_kernel
+            // wrote: every greedy one first
+            const int2 e = ld_l2(P.order + b);
+            b = e.x;
+            x.rule = e.y;
+        } else {
+            x.rule = kRule;
+        }
         x.b = b;
-        x.rule = kRule == kPerSequence ? (int)ld_early(P.mode + b) : kRule;
         const int64_t tb = (int64_t)b * P.K;
         if (lane < P.K) x.t0 = ld_early(P.t + tb + lane);
         if (lane + 32 < P.K) x.t1 = ld_early(P.t + tb + lane + 32);
@@ -923,6 +938,45 @@ __device__ void item_decide_loop(const Params &P, ItemShared &sh, unsigned long 
                 *(volatile int *)&sh.sbuf_busy[sb] = 0;  // the producer may reuse the buffer
             }
         }
+    }
+}
+
+// Mixed rounds: the order in which item_round_kernel<kPerSequence> takes the
+// sequences -- every greedy one first, then the rest, each group in batch
+// order -- written as {sequence, mode} to P.order.  Taking all the greedy
+// rows first measured faster than batch order on half-greedy batches (likely
+// because the round then ends on sampling items, whose sizes are known when
+// they are taken, rather than on greedy ones that may stop early).  One CTA; it lets the
+// item kernel be placed at once (that kernel reads P.order after its wait).
+constexpr int kOrderThreads = 256;
+
+__global__ void __launch_bounds__(kOrderThreads) mode_order_kernel(const Params P) {
+    grid_dependents_may_launch();
+    wait_for_primary_grid();
+    __shared__ int wsum[kOrderThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (P.B + kOrderThreads - 1) / kOrderThreads;
+    const int lo = min(P.B, tid * per), hi = min(P.B, lo + per);
+    int g = 0;
+    for (int b = lo; b < hi; ++b) g += P.mode[b] == 0;
+    int incl = g;  // inclusive scan of the greedy counts over the block
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kOrderThreads / 32; ++w) {
+        const int c = wsum[w];
+        if (w < warp) before += c;
+        total += c;
+    }
+    int gpos = before + incl - g;     // greedy sequences before lo
+    int rpos = total + (lo - gpos);   // the others: after every greedy one
+    for (int b = lo; b < hi; ++b) {
+        const int m = P.mode[b];
+        P.order[m == 0 ? gpos++ : rpos++] = make_int2(b, m);
     }
 }
 

@@ -427,6 +427,59 @@ def test_mixed_round_full():
     _free()
 
 
+def _mode_pattern(pattern, B, seed):
+    rng = np.random.default_rng(seed)
+    if pattern == "all_greedy":
+        m = np.zeros(B, np.uint8)
+    elif pattern == "all_sample":
+        m = np.ones(B, np.uint8)
+    elif pattern == "alternate":
+        m = (np.arange(B) % 2).astype(np.uint8)
+    elif pattern == "sample_block_first":
+        m = (np.arange(B) < B // 3).astype(np.uint8)
+    else:  # random, with a few invalid modes
+        m = rng.integers(0, 2, size=B).astype(np.uint8)
+        m[rng.choice(B, size=5, replace=False)] = [2, 255, 7, 2, 128]
+    return m
+
+
+@pytest.mark.parametrize("B,V,pattern", [
+    (777, 6000, "all_greedy"), (777, 6000, "all_sample"), (777, 6000, "alternate"),
+    (777, 6000, "sample_block_first"), (777, 6000, "invalid"), (5003, 700, "alternate"),
+    (5003, 700, "invalid")])
+def test_mixed_round_item_path_mode_patterns(B, V, pattern):
+    """With a sequence per SM or more, a mixed round is one item launch that
+    takes the greedy sequences first; every mode pattern (including invalid
+    modes, and B not a multiple of the ordering kernel's threads) gives the
+    oracle's outputs and commit, sequence by sequence."""
+    K, L = 5, 12
+    bt = make_inputs(4, "cuda", seed=4100 + B + len(pattern), B=B, V=V, K=K)
+    md = _mode_pattern(pattern, B, seed=B)
+    mode = torch.from_numpy(md).cuda()
+    p, q, t, ua, ur, _ = bt.numpy()
+    rng = np.random.default_rng(11)
+    lengths0 = rng.integers(0, 6, size=B).astype(np.int32)
+    tokens0 = np.full((B, L), -9, np.int32)
+    n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur, nthreads=8)
+    tok_ref, len_ref = tokens0.copy(), lengths0.copy()
+    oracle.commit(t, n0, x0, tok_ref, len_ref)
+    tok = torch.from_numpy(tokens0).cuda()
+    lens = torch.from_numpy(lengths0).cuda()
+    for _ in range(2):  # the second call reuses the workspace the first left
+        tok.copy_(torch.from_numpy(tokens0))
+        lens.copy_(torch.from_numpy(lengths0))
+        n1, x1, s1 = gpu_round(bt, mode=mode, tokens=tok, lengths=lens)
+        assert sv.last_kernel_count() == 2, "expected the ordering kernel and the item kernel"
+        bnd = compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1)
+        if bnd:
+            BOUNDARY_REPORT.append((f"mixed {pattern} B={B}", bnd))
+        same = x1 == x0  # a boundary-explained draw commits the GPU's own token
+        np.testing.assert_array_equal(lens.cpu().numpy(), len_ref)
+        np.testing.assert_array_equal(tok.cpu().numpy()[same], tok_ref[same])
+    if pattern == "invalid":
+        assert s1 == sv.STATUS_BAD_MODE
+
+
 def test_edge_full():
     bt = make_inputs(5, "cuda")
     host = bt.numpy()
