@@ -19,12 +19,6 @@
 #include "sv_logits.cuh"
 #include "specverify.h"
 
-// 1: batches of 16-byte-aligned rows with at least one sequence per SM run as
-// one launch over (sequence, chunk) items; 0: they take the three-launch
-// chunked path.  Both give identical results.
-#ifndef SV_ITEM_PATH
-#define SV_ITEM_PATH 1
-#endif
 // Segments (1024 elements) per item of the single-launch kernel: sampling
 // rows are streamed whole by one CTA (a draw then needs no other CTA's sums
 // early, and an item switch costs the producer more than the finer balance
@@ -47,6 +41,21 @@
 #endif
 #ifndef SV_ITEM_SEGS_GREEDY
 #define SV_ITEM_SEGS_GREEDY 48
+#endif
+// Batches with fewer sequences than SMs: items sized so that the grid gets
+// about SV_ITEM_SMALL_B_PER_CTA items per CTA, a multiple of 8 segments from
+// SV_ITEM_SMALL_B_MIN_SEGS to 64 (SV_ITEM_SMALL_B_SEGS > 0 fixes the size
+// instead).  At B = 128, V = 262144 and B = 64, V = 32000 two items per CTA
+// measured fastest, and faster than a three-launch pipeline over fixed
+// 8-segment chunks (scan, bulk-copy stream, decide).
+#ifndef SV_ITEM_SMALL_B_SEGS
+#define SV_ITEM_SMALL_B_SEGS 0
+#endif
+#ifndef SV_ITEM_SMALL_B_PER_CTA
+#define SV_ITEM_SMALL_B_PER_CTA 2
+#endif
+#ifndef SV_ITEM_SMALL_B_MIN_SEGS
+#define SV_ITEM_SMALL_B_MIN_SEGS 8
 #endif
 
 namespace {
@@ -118,7 +127,6 @@ thread_local int32_t g_last_kernels = 0;
 struct DeviceInfo {
     int sms = 0;
     int occupancy[3] = {0, 0, 0};      // resident CTAs per SM, register stream kernels
-    int tma_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, bulk-copy stream kernels
     int item_occupancy[3] = {0, 0, 0};  // resident CTAs per SM, single-launch item kernels
 };
 
@@ -136,20 +144,6 @@ int item_occupancy_of() {
     return n;
 }
 
-template <int kRule>
-int tma_occupancy_of() {
-    if (cudaFuncSetAttribute(sv::tma_stream_kernel<kRule>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sv::kTmaSmemBytes) != cudaSuccess)
-        return 0;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv::tma_stream_kernel<kRule>,
-                                                      sv::kTmaThreads,
-                                                      sv::kTmaSmemBytes) != cudaSuccess)
-        return 0;
-    return n;
-}
-
 std::mutex g_info_mu;
 DeviceInfo g_info[64];
 
@@ -163,7 +157,7 @@ int occupancy_of() {
 }
 
 // SM count and per-kernel residency of the current device, queried once.
-bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *item_occ) {
+bool device_info(int rule, int *sms, int *occ, int *item_occ) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     std::lock_guard<std::mutex> lock(g_info_mu);
@@ -175,9 +169,6 @@ bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *item_occ) {
         d.occupancy[sv::kGreedy] = occupancy_of<sv::kGreedy>();
         d.occupancy[sv::kSample] = occupancy_of<sv::kSample>();
         d.occupancy[sv::kPerSequence] = occupancy_of<sv::kPerSequence>();
-        d.tma_occupancy[sv::kGreedy] = tma_occupancy_of<sv::kGreedy>();
-        d.tma_occupancy[sv::kSample] = tma_occupancy_of<sv::kSample>();
-        d.tma_occupancy[sv::kPerSequence] = tma_occupancy_of<sv::kPerSequence>();
         d.item_occupancy[sv::kGreedy] = item_occupancy_of<sv::kGreedy>();
         d.item_occupancy[sv::kSample] = item_occupancy_of<sv::kSample>();
         d.item_occupancy[sv::kPerSequence] = item_occupancy_of<sv::kPerSequence>();
@@ -185,7 +176,6 @@ bool device_info(int rule, int *sms, int *occ, int *tma_occ, int *item_occ) {
     }
     *sms = d.sms;
     *occ = d.occupancy[rule] > 0 ? d.occupancy[rule] : 1;
-    *tma_occ = d.tma_occupancy[rule];
     *item_occ = d.item_occupancy[rule];
     return true;
 }
@@ -245,39 +235,47 @@ bool aligned_rows(const float *base, int64_t stride) {
     return base && (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && (stride & 3) == 0;
 }
 
-// One round: three kernels chained on the stream -- scan (per-sequence data),
-// stream (the bulk-copy pipeline when every row is 16-byte aligned, else the
-// register path), decide.  The later two are programmatic dependents.
+// One round on rows the bulk copies cannot take (not 16-byte aligned, or in
+// host memory): three kernels chained on the stream -- scan (per-sequence
+// data), the register stream over segments, decide.  The later two are
+// programmatic dependents.
 template <int kRule>
-int launch_round(const sv::Params &P, bool tma, unsigned grid, cudaStream_t st) {
+int launch_round(const sv::Params &P, unsigned grid, cudaStream_t st) {
     const unsigned per_seq = (unsigned)((P.B + sv::kWarps - 1) / sv::kWarps);
     sv::scan_kernel<kRule><<<per_seq, sv::kThreads, 0, st>>>(P);
     if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
-    const int rc = tma ? launch_dependent(sv::tma_stream_kernel<kRule>, grid, sv::kTmaThreads,
-                                          sv::kTmaSmemBytes, P, st)
-                       : launch_dependent(sv::stream_kernel<kRule>, grid, sv::kThreads, 0, P, st);
+    const int rc = launch_dependent(sv::stream_kernel<kRule>, grid, sv::kThreads, 0, P, st);
     if (rc != SV_OK) return rc;
     const unsigned decide_grid = (unsigned)((P.B + sv::kDecideWarps - 1) / sv::kDecideWarps);
     return launch_dependent(sv::decide_kernel<kRule>, decide_grid, sv::kDecideWarps * 32, 0, P, st);
 }
 
-// Picks the round's kernels.  With every row 16-byte aligned and at least one
-// sequence per SM: one persistent launch over (sequence, chunk) items.  With
-// aligned rows and fewer sequences: scan -> bulk-copy stream over chunks of
-// segments -> decide.  Otherwise: scan -> register stream -> decide.
-// Persistent grids hold as many CTAs as the SMs fit at once (or the tuning
-// override), never more than there is work for.
+// Picks the round's kernels.  With every row 16-byte aligned and in device
+// memory: one persistent launch over (sequence, chunk) items (a mixed round
+// adds the one-CTA ordering kernel before it).  Otherwise: scan -> register
+// stream -> decide.  Persistent grids hold as many CTAs as the SMs fit at once
+// (or the tuning override), never more than there is work for.
 int launch(int rule, sv::Params P, sv_stream_t stream) {
     const int64_t nseg = num_segments(P.V);
     const int64_t items = (int64_t)P.B * nseg;
     if (items > INT32_MAX / 2) return SV_EINVAL;
     P.nseg = (int32_t)nseg;
     P.items = (int32_t)items;
-    const int64_t cps = (nseg + sv::kChunkSegs - 1) / sv::kChunkSegs;
-    P.nchunks = (int32_t)((int64_t)P.B * cps);
-    P.isegs = (int32_t)std::min<int64_t>(nseg, rule == sv::kSample   ? SV_ITEM_SEGS_SAMPLE
-                                               : rule == sv::kGreedy ? SV_ITEM_SEGS_GREEDY
-                                                                     : SV_ITEM_SEGS);
+    int sms = 0, occ = 0, item_occ = 0;
+    if (!device_info(rule, &sms, &occ, &item_occ)) return SV_ECUDA;
+    const bool small_b = P.B < sms;
+    int64_t isegs = rule == sv::kSample   ? SV_ITEM_SEGS_SAMPLE
+                    : rule == sv::kGreedy ? SV_ITEM_SEGS_GREEDY
+                                          : SV_ITEM_SEGS;
+    if (small_b) {
+        const int64_t ctas = std::max<int64_t>(1, (int64_t)sms * item_occ);
+        isegs = SV_ITEM_SMALL_B_SEGS > 0
+                    ? SV_ITEM_SMALL_B_SEGS
+                    : std::min<int64_t>(64, std::max<int64_t>(
+                                                SV_ITEM_SMALL_B_MIN_SEGS,
+                                                nseg * P.B / (SV_ITEM_SMALL_B_PER_CTA * ctas) / 8 * 8));
+    }
+    P.isegs = (int32_t)std::min<int64_t>(nseg, isegs);
     P.ichunks = (int32_t)((nseg + P.isegs - 1) / P.isegs);
     P.ibig = P.ichunks;
     P.itail = 0;
@@ -290,18 +288,17 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
         const int64_t rest = nseg - big * P.isegs;
         if (rest > 0) {
             P.ibig = (int32_t)big;
-            P.itail = (int32_t)std::min<int64_t>(SV_ITEM_TAIL_SEGS, rest);
+            P.itail = (int32_t)std::min<int64_t>(
+                std::min<int64_t>(SV_ITEM_TAIL_SEGS, std::max<int32_t>(1, P.isegs / 2)), rest);
             P.ichunks = (int32_t)(big + (rest + P.itail - 1) / P.itail);
         }
     }
-    int sms = 0, occ = 0, tma_occ = 0, item_occ = 0;
-    if (!device_info(rule, &sms, &occ, &tma_occ, &item_occ)) return SV_ECUDA;
     // bulk copies read device memory only: rows on the host take the plain loads
     const bool aligned = !P.rows_on_host && aligned_rows(P.p, P.ps) &&
                          (rule == sv::kGreedy || P.K == 0 || aligned_rows(P.q, P.qs));
     const int32_t forced = g_ctas_per_sm.load();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (SV_ITEM_PATH && aligned && item_occ > 0 && P.B >= sms) {
+    if (aligned && item_occ > 0) {
         int64_t grid = (int64_t)sms * (forced > 0 ? std::min<int64_t>(forced, item_occ) : item_occ);
         grid = std::min<int64_t>(grid, (int64_t)P.B * P.ichunks);
         P.warps = (int32_t)(grid * sv::kWarps);
@@ -327,23 +324,16 @@ int launch(int rule, sv::Params P, sv_stream_t stream) {
             }
         }
     }
-    const bool tma = aligned && tma_occ > 0;
-    int64_t grid;
-    if (tma) {
-        grid = (int64_t)sms * (forced > 0 ? std::min<int64_t>(forced, tma_occ) : tma_occ);
-        if (grid > P.nchunks) grid = P.nchunks;
-    } else {
-        grid = (int64_t)sms * (forced > 0 ? forced : occ);
-        const int64_t needed = (items + sv::kWarps - 1) / sv::kWarps;
-        if (grid > needed) grid = needed;
-    }
+    int64_t grid = (int64_t)sms * (forced > 0 ? forced : occ);
+    const int64_t needed = (items + sv::kWarps - 1) / sv::kWarps;
+    if (grid > needed) grid = needed;
     P.warps = (int32_t)(grid * sv::kWarps);
     g_last_grid = grid;
     g_last_kernels = 3;
     switch (rule) {
-        case sv::kGreedy: return launch_round<sv::kGreedy>(P, tma, (unsigned)grid, st);
-        case sv::kSample: return launch_round<sv::kSample>(P, tma, (unsigned)grid, st);
-        default: return launch_round<sv::kPerSequence>(P, tma, (unsigned)grid, st);
+        case sv::kGreedy: return launch_round<sv::kGreedy>(P, (unsigned)grid, st);
+        case sv::kSample: return launch_round<sv::kSample>(P, (unsigned)grid, st);
+        default: return launch_round<sv::kPerSequence>(P, (unsigned)grid, st);
     }
 }
 

@@ -3,12 +3,9 @@
 // shares, and the plain-load path.
 //
 // A row of V probabilities is cut into 1024-element segments, each made of
-// eight 128-element blocks.  Three launch paths give identical outputs:
+// eight 128-element blocks.  Two launch paths give identical outputs:
 //  * sv_item.cuh: one persistent launch over (sequence, chunk) items, rows
-//    moved into shared memory by bulk copies (16-byte aligned device rows and
-//    at least one sequence per SM);
-//  * sv_tma.cuh with this file: scan -> bulk-copy stream over chunks of
-//    segments -> decide (aligned device rows, smaller batches);
+//    moved into shared memory by bulk copies (16-byte aligned device rows);
 //  * this file: scan -> plain-load stream -> decide (any alignment, and rows
 //    in page-locked host memory).
 // In the three-launch chain the scan kernel caches per-sequence data (the
@@ -96,7 +93,6 @@ struct Params {
     int32_t *tokens;            // optional commit target [B][max_len]
     int32_t *lengths;
     int32_t max_len;
-    int32_t nchunks;            // bulk-copy path: chunks of the batch
     int32_t rows_on_host;       // host side: p or q is page-locked host memory
     int32_t ichunks;            // item kernel: items (chunks) per sequence
     int32_t isegs;              // item kernel: segments per big item
@@ -104,7 +100,7 @@ struct Params {
     int32_t itail;              // item kernel: segments per small item (the rest of the row), 0: none
     // workspace
     uint32_t *status;
-    uint32_t *queue;            // bulk-copy path: next chunk to hand out
+    uint32_t *queue;            // item kernel: next item to hand out, and exited CTAs
     int32_t *miss;              // [B] greedy: kFlagBase - first missed row
     int32_t *nstate;            // [B] first rejection + 1 (sampling), 1 (greedy), kNBad
     int32_t *done;              // [B] item kernel: items of the sequence retired this round
@@ -1078,7 +1074,6 @@ constexpr int kDecideWarps = 2;  // small CTAs spread the per-sequence work over
 template <int kRule>
 __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(const Params P) {
     wait_for_primary_grid();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *P.queue = 0u;  // the stream kernel is done with it
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
     if (b >= P.B) return;

@@ -1,6 +1,6 @@
 // sv_item.cuh -- a whole verification round as one persistent kernel over
 // (sequence, chunk) work items (sm_103a); used when every row starts on a
-// 16-byte boundary and the batch has at least one sequence per SM.
+// 16-byte boundary and lies in device memory.
 //
 // A work item is one of a sequence's `ichunks` parts: a run of consecutive
 // 1024-element segments of the rows that sequence needs.  When a row takes

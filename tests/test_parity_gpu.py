@@ -427,6 +427,28 @@ def test_mixed_round_full():
     _free()
 
 
+@pytest.mark.parametrize("V", [131072 + 9 * 1024 + 4, 300000])  # rows 16-byte aligned
+def test_item_path_rows_in_several_items(V):
+    """Rows longer than one sampling item (128 segments of 1024) on the
+    single-launch item kernel (160 sequences, more than the SMs): a residual row's
+    sums then come from several CTAs, and the last item to retire draws."""
+    B, K = 160, 2
+    bt = make_inputs(3, "cuda", seed=V % 1000, B=B, V=V, K=K)
+    host = bt.numpy()
+    check_sample(bt, host, label=f"rows in several items V={V}")
+    assert sv.last_kernel_count() == 1
+    check_greedy(bt, host)
+    p, q, t, ua, ur, _ = host
+    md = (np.arange(B) % 2).astype(np.uint8)
+    n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur, nthreads=8)
+    n1, x1, s1 = gpu_round(bt, mode=torch.from_numpy(md).cuda())
+    bnd = compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1)
+    if bnd:
+        BOUNDARY_REPORT.append((f"rows in several items V={V}", bnd))
+    del bt
+    _free()
+
+
 def _mode_pattern(pattern, B, seed):
     rng = np.random.default_rng(seed)
     if pattern == "all_greedy":
@@ -448,8 +470,8 @@ def _mode_pattern(pattern, B, seed):
     (777, 6000, "sample_block_first"), (777, 6000, "invalid"), (5003, 700, "alternate"),
     (5003, 700, "invalid")])
 def test_mixed_round_item_path_mode_patterns(B, V, pattern):
-    """With a sequence per SM or more, a mixed round is one item launch that
-    takes the greedy sequences first; every mode pattern (including invalid
+    """On aligned device rows a mixed round is the ordering kernel and one item
+    launch that takes the greedy sequences first; every mode pattern (including invalid
     modes, and B not a multiple of the ordering kernel's threads) gives the
     oracle's outputs and commit, sequence by sequence."""
     K, L = 5, 12
