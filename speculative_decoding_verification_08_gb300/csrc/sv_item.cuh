@@ -415,9 +415,10 @@ struct ItemProducer {
 
     // A greedy item begun but not gathered.  Row 0 is read whatever the
     // draft, so its first `early` stages go out before the gather waits for
-    // the draft ids; the row's token key goes into the slot once p_0(t_0) is
-    // in, after the row's last stage; rows 1..K then as above.  ns becomes
-    // kNBad when a draft id is invalid (nothing past the early stages is read).
+    // the draft ids; the row's token key goes into the slot as soon as
+    // p_0(t_0) is in, before the rest of the row; rows 1..K then as above.
+    // ns becomes kNBad when a draft id is invalid (nothing past the early
+    // stages is read).
     __device__ int stream_greedy_lazy(ItemPre &c, int x, int early, int &ns) {
         const int split = min(c.s1, c.s0 + 2 * early);
         const int tok0 = P.K > 0 ? kTokInSlot : -1;
@@ -434,8 +435,11 @@ struct ItemProducer {
             return __shfl_sync(0xffffffffu, stages, 0);
         }
         if (lane == 0 && ok) {
-            stages += put_greedy_row(c.b, x, 0, tok0, 0.f, split, c.s1, 0, stop);
+            // the token's key first: the rest of row 0 is then tested as it
+            // arrives, a miss shows up before row 1, and no row-1 stage is
+            // issued for nothing
             if (P.K > 0) *(volatile unsigned long long *)&sh.slot[x].tkey0 = pack_key(c.pt0, c.t0);
+            stages += put_greedy_row(c.b, x, 0, tok0, 0.f, split, c.s1, 0, stop);
             if (*(volatile int *)&sh.slot[x].miss >= kFlagBase) stop = true;
         }
         sync_ok();
@@ -683,7 +687,8 @@ __device__ void item_consume(const Params &P, ItemShared &sh, unsigned char *buf
             const unsigned long long tk =
                 m.tok >= 0 ? pack_key(m.pt, m.tok)
                            : (m.tok == kTokInSlot ? *(volatile unsigned long long *)&sl.tkey0 : 0ull);
-            if (lane == 0 && tk && key > tk) {
+            // (once per row: a later stage that misses too changes nothing)
+            if (lane == 0 && tk && key > tk && *(volatile int *)&sl.miss < kFlagBase - m.row) {
                 atomicMax(&sl.miss, kFlagBase - m.row);
                 atomicMax(P.miss + b, kFlagBase - m.row);  // other CTAs stop sooner
             }
