@@ -86,3 +86,36 @@ def test_invalid_arguments_rejected_on_host(lib):
                                dummy, dummy, dummy, 0, ws, big, None) == -1
     assert lib.sv_set_ctas_per_sm(-1) == -1
     assert lib.sv_get_status(None, None, None) == -1
+
+
+def test_alpha_logits_and_noalloc_reject_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    dummy = P(4096)           # never dereferenced: every call below fails its checks first
+    ws = P(1 << 20)
+    big = 1 << 30
+    # acceptance-rate diagnostic: rows, strides, the alpha output and the workspace
+    def alpha(p=dummy, ps=10, q=dummy, qs=10, B=2, K=3, V=10, a=dummy, e=dummy, w=ws, n=big):
+        return lib.sv_alpha(p, ps, q, qs, B, K, V, a, e, w, n, None)
+    assert alpha(p=None) == -1 and alpha(ps=9) == -1
+    assert alpha(q=None) == -1 and alpha(qs=9) == -1 and alpha(a=None) == -1
+    assert alpha(K=65) == -1 and alpha(V=0) == -1 and alpha(B=-1) == -1
+    assert alpha(B=0, p=None, q=None, a=None, e=None, w=None, n=0) == 0
+    assert alpha(w=None) == -2 and alpha(w=P((1 << 20) + 16)) == -2 and alpha(n=64) == -2
+
+    # sampling from logits: the temperature must be a positive finite number
+    def logits(temp=1.0, zq=dummy, ua=dummy, ur=dummy, zqs=10, K=3):
+        return lib.sv_verify_sample_logits(dummy, 10, zq, zqs, dummy, ua, ur, 2, K, 10,
+                                           ctypes.c_float(temp), dummy, dummy, ws, big, None)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert logits(temp=bad) == -1, bad
+    assert logits(zq=None) == -1 and logits(ua=None) == -1 and logits(ur=None) == -1
+    assert logits(zqs=9) == -1 and logits(K=65) == -1
+
+    # the allocation-free call refuses sizes its fixed scratch cannot hold,
+    # before it looks for a device
+    B, K, V = 4096, 5, 128256
+    assert sv.workspace_size(B, K, V) > sv.NOALLOC_SCRATCH_BYTES
+    assert lib.sv_verify_sample_noalloc(dummy, V, dummy, V, dummy, dummy, dummy, B, K, V, dummy,
+                                        dummy, None) == sv.SV_ETOOLARGE
+    assert lib.sv_verify_sample_noalloc(dummy, V, None, V, dummy, dummy, dummy, B, K, V, dummy,
+                                        dummy, None) == -1
