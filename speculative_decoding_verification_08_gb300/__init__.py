@@ -174,15 +174,18 @@ class Workspace:
 _ws_cache = {}
 
 
-def _workspace(ws, B, K, V, device):
+def _workspace(ws, B, K, V, device, stream=None):
+    """The caller's workspace, or one kept for these sizes and this stream.
+    Calls that share a workspace must be ordered on one stream, so calls on
+    different streams never share an implicit one."""
     if ws is not None:
         if not ws.fits(B, K, V):
             raise SpecVerifyError("workspace too small for these sizes")
         return ws
-    key = (str(device), B, K, V)
+    key = (str(device), B, K, V, _stream_handle(stream).value)
     w = _ws_cache.get(key)
     if w is None:
-        w = Workspace(B, K, V, device)
+        w = Workspace(B, K, V, device, stream)
         _ws_cache[key] = w
     return w
 
@@ -258,7 +261,7 @@ def verify_greedy(p, t, *, ws=None, n_out=None, next_out=None, stream=None):
     dev = _device_of(p)
     t = _vec(t, B * K, "t", torch.int32, dev)
     n_out, next_out = _outputs(B, dev, n_out, next_out)
-    w = _workspace(ws, B, K, V, dev)
+    w = _workspace(ws, B, K, V, dev, stream)
     rc = load().sv_verify_greedy(_ptr(p), ps, _ptr(t), B, K, V, _ptr(n_out), _ptr(next_out),
                                  w.ptr, w.nbytes, _stream_handle(stream))
     _check(rc, "sv_verify_greedy")
@@ -279,7 +282,7 @@ def verify_sample(p, q, t, u_acc, u_res, *, ws=None, n_out=None, next_out=None, 
     u_acc = _vec(u_acc, B * K, "u_acc", torch.float32, dev)
     u_res = _vec(u_res, B, "u_res", torch.float64, dev)
     n_out, next_out = _outputs(B, dev, n_out, next_out)
-    w = _workspace(ws, B, K, V, dev)
+    w = _workspace(ws, B, K, V, dev, stream)
     rc = load().sv_verify_sample(_ptr(p), ps, _ptr(q), qs, _ptr(t), _ptr(u_acc), _ptr(u_res),
                                  B, K, V, _ptr(n_out), _ptr(next_out), w.ptr, w.nbytes,
                                  _stream_handle(stream))
@@ -330,7 +333,7 @@ def verify_sample_logits(zp, zq, t, u_acc, u_res, temperature: float = 1.0, *, w
     u_acc = _vec(u_acc, B * K, "u_acc", torch.float32, dev)
     u_res = _vec(u_res, B, "u_res", torch.float64, dev)
     n_out, next_out = _outputs(B, dev, n_out, next_out)
-    w = _workspace(ws, B, K, V, dev)
+    w = _workspace(ws, B, K, V, dev, stream)
     _check(load().sv_verify_sample_logits(_ptr(zp), ps, _ptr(zq), qs, _ptr(t), _ptr(u_acc),
                                           _ptr(u_res), B, K, V, float(temperature), _ptr(n_out),
                                           _ptr(next_out), w.ptr, w.nbytes,
@@ -356,7 +359,7 @@ def alpha(p, q, *, ws=None, alpha_out=None, expected_out=None, stream=None):
         expected_out = torch.empty(B, dtype=torch.float64, device=dev)
     _vec(alpha_out.reshape(-1), B * K, "alpha_out", torch.float64, dev)
     _vec(expected_out, B, "expected_out", torch.float64, dev)
-    w = _workspace(ws, B, K, V, dev)
+    w = _workspace(ws, B, K, V, dev, stream)
     _check(load().sv_alpha(_ptr(p), ps, _ptr(q3), qs, B, K, V, _ptr(alpha_out),
                            _ptr(expected_out), w.ptr, w.nbytes, _stream_handle(stream)),
            "sv_alpha")
@@ -387,7 +390,7 @@ def verify_round(mode, p, q, t, u_acc, u_res, *, tokens=None, lengths=None, ws=N
         _vec(tokens, B * max_len, "tokens", torch.int32, dev)
         _vec(lengths, B, "lengths", torch.int32, dev)
     n_out, next_out = _outputs(B, dev, n_out, next_out)
-    w = _workspace(ws, B, K, V, dev)
+    w = _workspace(ws, B, K, V, dev, stream)
     rc = load().sv_verify_round(_ptr(mode), _ptr(p), ps, _ptr(q), qs, _ptr(t), _ptr(u_acc),
                                 _ptr(u_res), B, K, V, _ptr(n_out), _ptr(next_out), _ptr(tokens),
                                 _ptr(lengths), max_len, w.ptr, w.nbytes, _stream_handle(stream))

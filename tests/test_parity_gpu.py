@@ -371,6 +371,19 @@ def test_workspace_reused_across_sizes():
                 BOUNDARY_REPORT.append((f"reused workspace {B}x{V}", bnd))
 
 
+def test_implicit_workspaces_are_per_stream():
+    """Calls that share a workspace must be ordered on one stream, so the
+    binding keeps one implicit workspace per (sizes, stream)."""
+    dev = torch.device("cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    w1 = sv._workspace(None, 4, 3, 1000, dev, s1)
+    w2 = sv._workspace(None, 4, 3, 1000, dev, s2)
+    assert w1 is not w2
+    assert sv._workspace(None, 4, 3, 1000, dev, s1) is w1
+    assert sv._workspace(None, 4, 3, 1000, dev) is not w1   # the current stream
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("mapped", [True, False])
 def test_host_resident_inputs(mapped):
     """Inputs in pinned host memory, read in place (mapped) or copied first:
