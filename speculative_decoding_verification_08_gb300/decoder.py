@@ -9,6 +9,12 @@ and the verification keeps the accepted proposals and appends the emitted
 token.  Verification and the commit into the token buffer run on the GPU
 (``sv_verify_round``); only the callbacks and the loop are host code.
 
+``PendingTokenDecoder`` drives a target that keeps a cache of the tokens it
+has processed, with the deferred ("pending") correction token of the SPEL
+page, section 1.2 (Speculative decoding), and the llms-explorer post's
+backend: one target pass per round over [pending, d_0, ..., d_{k-1}], the
+rejected drafts rolled back, the emitted token left pending for the next pass.
+
 The governor follows the SPEL page, section 1.3 (Dynamic Speculation
 Governor): it keeps the ratio of accepted to proposed tokens over a rolling
 window of rounds and stops drafting for the rest of the call once that ratio
@@ -65,28 +71,46 @@ class SpeculationGovernor:
         return self.speculating
 
 
-class SpeculativeDecoder:
-    """Speculative decoding of one sequence with user callbacks (the page's
-    ``SpeculativeDecoder(draft_step, target_step, k=4, greedy=True)``).
+class DeviceVerifier:
+    """One verification round on the GPU (``sv_verify_round``) with the commit
+    into the caller's device token buffer: the step both drivers take each
+    round.  Keeps one workspace per (B, K, V).
 
-    ``generate(prompt_ids, max_new)`` returns the new token ids.  Greedy mode
-    emits exactly the stream plain greedy decoding of the target would;
-    sampling mode draws its uniforms from a seeded CUDA generator, so a fixed
-    seed gives a fixed stream.  ``trace`` records (proposed, n_accepted,
-    next_token) per round."""
+    ``__call__(mode, p, q, t, u_acc, u_res, tokens, lengths)`` takes the
+    tensors of ``verify_round`` (q is None when K = 0) and returns
+    (n_accepted [B], next_token [B]) on the device."""
 
-    def __init__(self, draft_step: Callable, target_step: Callable, k: int = 4,
-                 greedy: bool = True, seed: int = 0, governor: Optional[SpeculationGovernor] = None,
-                 device=None):
+    def __init__(self, device=None):
+        torch = _torch()
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self._ws = {}
+
+    def __call__(self, mode, p, q, t, u_acc, u_res, tokens, lengths):
+        B, K, V = p.shape[0], t.shape[1], p.shape[2]
+        key = (B, K, V)
+        if key not in self._ws:
+            self._ws[key] = Workspace(B, K, V, self.device)
+        return verify_round(mode, p, q if K > 0 else None, t, u_acc, u_res, tokens=tokens,
+                            lengths=lengths, ws=self._ws[key])
+
+
+class _RoundDriver:
+    """What both drivers share: the draft callback, the rule, the uniforms'
+    generator, the governor, the device token buffer and one verification
+    round over given rows."""
+
+    def __init__(self, draft_step: Callable, k: int, greedy: bool, seed: int,
+                 governor: Optional[SpeculationGovernor], device, verify: Optional[Callable]):
         if k < 1:
             raise ValueError("k must be >= 1")
         torch = _torch()
-        self.draft_step, self.target_step = draft_step, target_step
+        self.draft_step = draft_step
         self.k, self.greedy = k, greedy
         self.device = torch.device("cuda") if device is None else torch.device(device)
         self.gen = torch.Generator(device=self.device)
         self.gen.manual_seed(seed)
         self.governor = governor
+        self.verify = DeviceVerifier(self.device) if verify is None else verify
         self.trace: List[Tuple[int, int, int]] = []
 
     def _probs(self, x, rows: int, V: Optional[int], what: str):
@@ -98,56 +122,160 @@ class SpeculativeDecoder:
             raise SpecVerifyError(f"{what}: expected [{rows}][V], got {tuple(x.shape)}")
         return x.contiguous()
 
-    def _round(self, prefix: Sequence[int], tokens_buf, lengths_buf, ws_cache: dict):
-        """One verification round appended to tokens_buf; returns (proposed, n, next)."""
-        torch = _torch()
-        spec = self.governor is None or self.governor.speculating
-        k = self.k if spec else 0
-        if k > 0:
-            toks, qprobs = self.draft_step(list(prefix), k)
-            t = torch.as_tensor(list(toks), dtype=torch.int32, device=self.device).reshape(1, k)
-            target = self._probs(self.target_step(list(prefix), list(toks)), k + 1, None, "target")
-            q = self._probs(qprobs, k, target.shape[1], "draft probs").unsqueeze(0)
-        else:
-            t = torch.zeros(1, 0, dtype=torch.int32, device=self.device)
-            target = self._probs(self.target_step(list(prefix), []), 1, None, "target")
-            q = None
-        V = target.shape[1]
-        mode = torch.tensor([0 if self.greedy else 1], dtype=torch.uint8, device=self.device)
-        ua = torch.rand(1, k, generator=self.gen, device=self.device)
-        ur = torch.rand(1, generator=self.gen, device=self.device, dtype=torch.float64)
-        if q is None:
-            q = torch.zeros(1, 0, V, device=self.device)
-        key = (k, V)
-        if key not in ws_cache:
-            ws_cache[key] = Workspace(1, k, V, self.device)
-        n, nxt = verify_round(mode, target.unsqueeze(0), q if k > 0 else None, t, ua, ur,
-                              tokens=tokens_buf, lengths=lengths_buf, ws=ws_cache[key])
-        n, nxt = int(n.item()), int(nxt.item())
-        if nxt < 0:
-            raise SpecVerifyError("verification produced no token (invalid draft ids or "
-                                  "zero-mass rows)")
-        return k, n, nxt
+    def _k(self) -> int:
+        """Drafts this round: k while the governor lets the call speculate, else 0."""
+        return self.k if self.governor is None or self.governor.speculating else 0
 
-    def generate(self, prompt_ids: Sequence[int], max_new: int = 128,
-                 eos_id: Optional[int] = None) -> List[int]:
+    def _draft(self, prefix: Sequence[int], k: int):
+        """(draft tokens [k] as ints, draft probs [k][V] or None)."""
+        if k == 0:
+            return [], None
+        toks, qprobs = self.draft_step(list(prefix), k)
+        toks = [int(x) for x in toks]
+        if len(toks) != k:
+            raise SpecVerifyError(f"draft_step returned {len(toks)} tokens, expected {k}")
+        return toks, qprobs
+
+    def _buffers(self, prefix: Sequence[int], max_new: int):
         torch = _torch()
-        prefix = list(int(x) for x in prompt_ids)
         start = len(prefix)
         cap = start + max_new + self.k + 1
         tokens_buf = torch.zeros(1, cap, dtype=torch.int32, device=self.device)
-        tokens_buf[0, :start] = torch.tensor(prefix, dtype=torch.int32)
+        tokens_buf[0, :start] = torch.tensor(list(prefix), dtype=torch.int32)
         lengths_buf = torch.tensor([start], dtype=torch.int32, device=self.device)
-        ws_cache: dict = {}
+        return tokens_buf, lengths_buf
+
+    def _verify(self, toks, qprobs, target_rows, tokens_buf, lengths_buf):
+        """Verifies the drafts toks against target_rows [k+1][V] (draft probs
+        qprobs [k][V]) and appends the kept drafts and the emitted token to
+        the token buffer; returns (n_accepted, next_token)."""
+        torch = _torch()
+        k = len(toks)
+        target = self._probs(target_rows, k + 1, None, "target")
+        V = target.shape[1]
+        if k > 0:
+            t = torch.as_tensor(toks, dtype=torch.int32, device=self.device).reshape(1, k)
+            q = self._probs(qprobs, k, V, "draft probs").unsqueeze(0)
+        else:
+            t = torch.zeros(1, 0, dtype=torch.int32, device=self.device)
+            q = torch.zeros(1, 0, V, device=self.device)
+        mode = torch.tensor([0 if self.greedy else 1], dtype=torch.uint8, device=self.device)
+        ua = torch.rand(1, k, generator=self.gen, device=self.device)
+        ur = torch.rand(1, generator=self.gen, device=self.device, dtype=torch.float64)
+        n, nxt = self.verify(mode, target.unsqueeze(0), q, t, ua, ur, tokens_buf, lengths_buf)
+        n, nxt = int(n[0].item()), int(nxt[0].item())
+        if nxt < 0:
+            raise SpecVerifyError("verification produced no token (invalid draft ids or "
+                                  "zero-mass rows)")
+        return n, nxt
+
+    @staticmethod
+    def _eos_cut(out: List[int], eos_id: Optional[int], max_new: int) -> Optional[List[int]]:
+        if eos_id is not None and eos_id in out:
+            return out[:out.index(eos_id) + 1][:max_new]
+        return None
+
+
+class SpeculativeDecoder(_RoundDriver):
+    """Speculative decoding of one sequence with user callbacks (the page's
+    ``SpeculativeDecoder(draft_step, target_step, k=4, greedy=True)``).
+
+    ``generate(prompt_ids, max_new)`` returns the new token ids.  Greedy mode
+    emits exactly the stream plain greedy decoding of the target would;
+    sampling mode draws its uniforms from a seeded CUDA generator, so a fixed
+    seed gives a fixed stream.  ``trace`` records (proposed, n_accepted,
+    next_token) per round."""
+
+    def __init__(self, draft_step: Callable, target_step: Callable, k: int = 4,
+                 greedy: bool = True, seed: int = 0, governor: Optional[SpeculationGovernor] = None,
+                 device=None, verify: Optional[Callable] = None):
+        super().__init__(draft_step, k, greedy, seed, governor, device, verify)
+        self.target_step = target_step
+
+    def generate(self, prompt_ids: Sequence[int], max_new: int = 128,
+                 eos_id: Optional[int] = None) -> List[int]:
+        prefix = list(int(x) for x in prompt_ids)
+        start = len(prefix)
+        tokens_buf, lengths_buf = self._buffers(prefix, max_new)
         self.trace = []
         while len(prefix) - start < max_new:
-            k, n, nxt = self._round(prefix, tokens_buf, lengths_buf, ws_cache)
+            k = self._k()
+            toks, qprobs = self._draft(prefix, k)
+            rows = self.target_step(list(prefix), list(toks))
+            n, nxt = self._verify(toks, qprobs, rows, tokens_buf, lengths_buf)
             self.trace.append((k, n, nxt))
-            length = int(lengths_buf.item())
-            prefix = tokens_buf[0, :length].tolist()     # the committed history
+            prefix = tokens_buf[0, :int(lengths_buf.item())].tolist()   # the committed history
             if self.governor is not None and k > 0:
                 self.governor.record(n, k)
-            if eos_id is not None and eos_id in prefix[start:]:
-                out = prefix[start:]
-                return out[:out.index(eos_id) + 1][:max_new]
+            cut = self._eos_cut(prefix[start:], eos_id, max_new)
+            if cut is not None:
+                return cut
+        return prefix[start:start + max_new]
+
+
+class PendingTokenDecoder(_RoundDriver):
+    """Speculative decoding of one sequence against a target that keeps a
+    cache of the tokens it has processed, with a deferred ("pending")
+    correction token.
+
+    The token a round emits is not run through the target at once.  The next
+    round runs the target once over [pending, d_0, ..., d_{k-1}]: row j of
+    that pass is the distribution that follows the prefix, the pending token
+    and d_0..d_{j-1}, which are exactly the k + 1 rows verification needs.
+    The accepted drafts stay in the cache, the rejected ones are rolled back,
+    and the emitted token (correction or bonus) becomes the next pending
+    token.  Every round therefore costs one target pass, and no round needs a
+    separate pass for the token it emits.  The stream is the one
+    ``SpeculativeDecoder`` produces with the same callbacks and seed.
+
+    ``target`` provides
+      ``forward(tokens) -> probs [len(tokens)][V]``: appends tokens to its
+        cache; row j is the distribution of the token after tokens[j];
+      ``rollback(n)``: drops the last n tokens from its cache.
+    ``draft_step(prefix, k) -> (tokens [k], probs [k][V])`` as for
+    ``SpeculativeDecoder``.  ``target_passes`` counts forward calls (the
+    prompt's prefill included) and ``trace`` records (proposed, n_accepted,
+    next_token) per round."""
+
+    def __init__(self, draft_step: Callable, target, k: int = 4, greedy: bool = True,
+                 seed: int = 0, governor: Optional[SpeculationGovernor] = None, device=None,
+                 verify: Optional[Callable] = None):
+        super().__init__(draft_step, k, greedy, seed, governor, device, verify)
+        self.target = target
+        self.target_passes = 0
+
+    def _forward(self, tokens: List[int]):
+        self.target_passes += 1
+        return self.target.forward(list(tokens))
+
+    def generate(self, prompt_ids: Sequence[int], max_new: int = 128,
+                 eos_id: Optional[int] = None) -> List[int]:
+        """New token ids after prompt_ids (at least one token).  The target's
+        cache must be empty; on return it holds every committed token but
+        the last (still pending)."""
+        prefix = list(int(x) for x in prompt_ids)
+        if not prefix:
+            raise ValueError("the prompt needs at least one token")
+        start = len(prefix)
+        tokens_buf, lengths_buf = self._buffers(prefix, max_new)
+        self.trace = []
+        self.target_passes = 0
+        if len(prefix) > 1:
+            self._forward(prefix[:-1])          # prefill; its rows are not needed
+        pending = prefix[-1]
+        while len(prefix) - start < max_new:
+            k = self._k()
+            toks, qprobs = self._draft(prefix, k)
+            rows = self._forward([pending] + toks)
+            n, nxt = self._verify(toks, qprobs, rows, tokens_buf, lengths_buf)
+            if k > n:
+                self.target.rollback(k - n)     # the rejected drafts leave the cache
+            pending = nxt
+            self.trace.append((k, n, nxt))
+            prefix = tokens_buf[0, :int(lengths_buf.item())].tolist()   # the committed history
+            if self.governor is not None and k > 0:
+                self.governor.record(n, k)
+            cut = self._eos_cut(prefix[start:], eos_id, max_new)
+            if cut is not None:
+                return cut
         return prefix[start:start + max_new]

@@ -1,10 +1,13 @@
-"""The round driver and the speculation governor.
+"""The round drivers and the speculation governor.
 
-The governor is host logic (CPU tests).  The driver runs its verification on
-the GPU: greedy decoding through it must give exactly the stream plain greedy
-decoding of the target gives ("spec-verify", section "Method"), with or without
-the governor switching to one-token rounds; sampled rounds must agree with
-the oracle on the same rows and uniforms."""
+The governor is host logic (CPU tests).  The drivers run their verification
+on the GPU: greedy decoding through them must give exactly the stream plain
+greedy decoding of the target gives ("spec-verify", section "Method"), with
+or without the governor switching to one-token rounds; sampled rounds must
+agree with the oracle on the same rows and uniforms.  The drivers' own
+bookkeeping (drafts, the pending token, rollbacks, the commit, target passes)
+is also checked on the CPU, with the oracle standing in for the verification
+step through the drivers' ``verify`` hook."""
 import hashlib
 
 import numpy as np
@@ -13,7 +16,9 @@ import torch
 
 import oracle
 import speculative_decoding_verification_08_gb300 as sv
-from speculative_decoding_verification_08_gb300.decoder import SpeculationGovernor, SpeculativeDecoder
+from speculative_decoding_verification_08_gb300.decoder import (PendingTokenDecoder,
+                                                                 SpeculationGovernor,
+                                                                 SpeculativeDecoder)
 
 V = 48
 
@@ -158,3 +163,113 @@ def test_sampling_rounds_match_the_oracle():
         assert (int(n0[0]), int(x0[0])) == (n, nxt)
         prefix = prefix + list(toks[:n]) + [nxt]
     assert prefix[len(prompt):len(prompt) + 50] == out
+
+
+# ---------------------------------------------------------------------------
+# the pending-token driver, and the drivers' bookkeeping on the CPU
+
+class CachedToyTarget:
+    """The toy target with a cache of processed tokens: forward(tokens)
+    appends them and returns one row per token (the distribution of the token
+    after it); rollback(n) drops the last n."""
+
+    def __init__(self):
+        self.cache = []
+        self.passes = 0
+
+    def forward(self, tokens):
+        self.passes += 1
+        rows = []
+        for x in tokens:
+            self.cache.append(int(x))
+            rows.append(target_row(self.cache))
+        return np.stack(rows)
+
+    def rollback(self, n):
+        assert 0 < n <= len(self.cache)
+        del self.cache[-n:]
+
+
+def oracle_verify(mode, p, q, t, ua, ur, tokens, lengths):
+    """The verification step with the commit, computed by the oracle on CPU
+    tensors (test stand-in for the drivers' device verifier)."""
+    n, x, _ = oracle.verify_round(mode.numpy(), p.numpy(), q.numpy(), t.numpy(), ua.numpy(),
+                                  ur.numpy())
+    assert oracle.commit(t.numpy(), n, x, tokens.numpy(), lengths.numpy()) == 0
+    return torch.from_numpy(n), torch.from_numpy(x)
+
+
+def committed_length(prompt, trace):
+    return len(prompt) + sum(n + 1 for _, n, _ in trace)
+
+
+@pytest.mark.parametrize("k", [1, 3, 4, 7])
+def test_pending_driver_greedy_on_cpu(k):
+    draft_step, _ = make_callbacks(noise=0.6)
+    target = CachedToyTarget()
+    dec = PendingTokenDecoder(draft_step, target, k=k, greedy=True, device="cpu",
+                              verify=oracle_verify)
+    prompt = [1, 2, 3]
+    out = dec.generate(prompt, max_new=60)
+    assert out == plain_greedy(prompt, 60)
+    # one target pass per round, plus the prompt's prefill
+    assert target.passes == dec.target_passes == len(dec.trace) + 1
+    # the cache holds every committed token but the pending one
+    total = committed_length(prompt, dec.trace)
+    assert target.cache == (prompt + plain_greedy(prompt, total))[:total - 1]
+    assert any(n > 0 for _, n, _ in dec.trace) and any(n < k for _, n, _ in dec.trace)
+
+
+def test_uncached_driver_greedy_on_cpu():
+    draft_step, target_step = make_callbacks(noise=0.6)
+    dec = SpeculativeDecoder(draft_step, target_step, k=4, greedy=True, device="cpu",
+                             verify=oracle_verify)
+    assert dec.generate([4, 4], max_new=40) == plain_greedy([4, 4], 40)
+
+
+def test_pending_and_uncached_drivers_sample_the_same_stream():
+    """Same callbacks and seed: the cached target's rows equal the recomputed
+    ones, so both drivers make the same draws."""
+    k, prompt = 4, [7, 1, 8]
+    draft_a, target_step = make_callbacks(noise=0.8, greedy_draft=False, seed=11)
+    plain = SpeculativeDecoder(draft_a, target_step, k=k, greedy=False, seed=5, device="cpu",
+                               verify=oracle_verify)
+    out_a = plain.generate(prompt, max_new=50)
+    draft_b, _ = make_callbacks(noise=0.8, greedy_draft=False, seed=11)
+    target = CachedToyTarget()
+    pend = PendingTokenDecoder(draft_b, target, k=k, greedy=False, seed=5, device="cpu",
+                               verify=oracle_verify)
+    out_b = pend.generate(prompt, max_new=50)
+    assert out_a == out_b and plain.trace == pend.trace
+    assert len(out_b) == 50 and target.passes == len(pend.trace) + 1
+    assert any(n < k for _, n, _ in pend.trace)
+
+
+def test_pending_driver_governor_and_one_token_prompt_on_cpu():
+    draft_step, _ = make_callbacks(noise=8.0)           # a poor draft: zero-accept rounds
+    gov = SpeculationGovernor(window=4, alpha_threshold=0.4)
+    target = CachedToyTarget()
+    dec = PendingTokenDecoder(draft_step, target, k=4, greedy=True, governor=gov, device="cpu",
+                              verify=oracle_verify)
+    out = dec.generate([5], max_new=30)
+    assert out == plain_greedy([5], 30)
+    assert not gov.speculating
+    ks = [k for k, _, _ in dec.trace]
+    assert 0 in ks and all(k == 0 for k in ks[ks.index(0):])
+    assert target.passes == len(dec.trace)               # a one-token prompt needs no prefill
+    total = committed_length([5], dec.trace)
+    assert target.cache == ([5] + plain_greedy([5], total))[:total - 1]
+    with pytest.raises(ValueError):
+        dec.generate([], max_new=3)
+
+
+@pytest.mark.gpu
+def test_pending_driver_on_the_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    draft_step, _ = make_callbacks(noise=0.6)
+    target = CachedToyTarget()
+    dec = PendingTokenDecoder(draft_step, target, k=4, greedy=True)
+    out = dec.generate([1, 2, 3], max_new=60)
+    assert out == plain_greedy([1, 2, 3], 60)
+    assert target.passes == len(dec.trace) + 1
