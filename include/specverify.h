@@ -62,7 +62,14 @@
  *                            after SV_STATUS_TIMEOUT, or overwritten);
  *       SV_STATUS_BAD_MODE   a round mode other than 0 or 1 (n = 0, next = -1);
  *       SV_STATUS_TIMEOUT    a bounded wait inside a kernel gave up (the
- *                            round's outputs are not meaningful).
+ *                            round's outputs are not meaningful);
+ *       SV_STATUS_BAD_VALUE  only from a library built with -DSV_DEBUG=1,
+ *                            which checks every input row before a call's
+ *                            kernels: a probability that is negative, NaN
+ *                            or infinite (for sv_verify_sample_logits: a
+ *                            logit that is NaN or infinite).  The regular
+ *                            build does not look, and such inputs give
+ *                            unspecified results.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -87,6 +94,7 @@ typedef struct CUstream_st *sv_stream_t;
 #define SV_STATUS_OVERFLOW 4u
 #define SV_STATUS_BAD_MODE 8u
 #define SV_STATUS_TIMEOUT 16u
+#define SV_STATUS_BAD_VALUE 32u
 
 #define SV_MAX_K 64
 

@@ -34,6 +34,7 @@ STATUS_ZERO_MASS = 2
 STATUS_OVERFLOW = 4
 STATUS_BAD_MODE = 8
 STATUS_TIMEOUT = 16
+STATUS_BAD_VALUE = 32   # debug builds only (built with SV_DEBUG=1)
 MAX_K = 64
 
 # every symbol include/specverify.h declares
@@ -67,41 +68,46 @@ def load():
             raise SpecVerifyError(
                 f"{LIBRARY} is missing: build it with "
                 "speculative_decoding_verification_08_gb300.build() (no CPU fallback exists)")
-        lib = ctypes.CDLL(LIBRARY)
-        P = ctypes.c_void_p
-        i32, i64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        lib.sv_workspace_size.argtypes = [i32, i32, i64]
-        lib.sv_workspace_size.restype = sz
-        lib.sv_workspace_init.argtypes = [P, sz, P]
-        lib.sv_workspace_init.restype = ctypes.c_int
-        lib.sv_verify_greedy.argtypes = [P, i64, P, i32, i32, i64, P, P, P, sz, P]
-        lib.sv_verify_greedy.restype = ctypes.c_int
-        lib.sv_verify_sample.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P, sz, P]
-        lib.sv_verify_sample.restype = ctypes.c_int
-        lib.sv_verify_round.argtypes = [P, P, i64, P, i64, P, P, P, i32, i32, i64, P, P,
-                                        P, P, i32, P, sz, P]
-        lib.sv_verify_round.restype = ctypes.c_int
-        lib.sv_get_status.argtypes = [P, P, P]
-        lib.sv_get_status.restype = ctypes.c_int
-        lib.sv_set_ctas_per_sm.argtypes = [i32]
-        lib.sv_set_ctas_per_sm.restype = ctypes.c_int
-        lib.sv_last_grid_size.argtypes = []
-        lib.sv_last_grid_size.restype = i64
-        lib.sv_last_kernel_count.argtypes = []
-        lib.sv_last_kernel_count.restype = i32
-        lib.sv_alpha.argtypes = [P, i64, P, i64, i32, i32, i64, P, P, P, sz, P]
-        lib.sv_alpha.restype = ctypes.c_int
-        lib.sv_verify_sample_logits.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64,
-                                                ctypes.c_float, P, P, P, sz, P]
-        lib.sv_verify_sample_logits.restype = ctypes.c_int
-        lib.sv_status_string.argtypes = [ctypes.c_int]
-        lib.sv_status_string.restype = ctypes.c_char_p
-        lib.sv_version.argtypes = []
-        lib.sv_version.restype = ctypes.c_int
-        lib.sv_verify_sample_noalloc.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P]
-        lib.sv_verify_sample_noalloc.restype = ctypes.c_int
-        _lib = lib
-        return lib
+        _lib = _declare(ctypes.CDLL(LIBRARY))
+        return _lib
+
+
+def _declare(lib):
+    """Sets the argument and result types of every C-ABI call on a loaded
+    copy of the library (the regular build, or a debug build)."""
+    P = ctypes.c_void_p
+    i32, i64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.sv_workspace_size.argtypes = [i32, i32, i64]
+    lib.sv_workspace_size.restype = sz
+    lib.sv_workspace_init.argtypes = [P, sz, P]
+    lib.sv_workspace_init.restype = ctypes.c_int
+    lib.sv_verify_greedy.argtypes = [P, i64, P, i32, i32, i64, P, P, P, sz, P]
+    lib.sv_verify_greedy.restype = ctypes.c_int
+    lib.sv_verify_sample.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P, sz, P]
+    lib.sv_verify_sample.restype = ctypes.c_int
+    lib.sv_verify_round.argtypes = [P, P, i64, P, i64, P, P, P, i32, i32, i64, P, P,
+                                    P, P, i32, P, sz, P]
+    lib.sv_verify_round.restype = ctypes.c_int
+    lib.sv_get_status.argtypes = [P, P, P]
+    lib.sv_get_status.restype = ctypes.c_int
+    lib.sv_set_ctas_per_sm.argtypes = [i32]
+    lib.sv_set_ctas_per_sm.restype = ctypes.c_int
+    lib.sv_last_grid_size.argtypes = []
+    lib.sv_last_grid_size.restype = i64
+    lib.sv_last_kernel_count.argtypes = []
+    lib.sv_last_kernel_count.restype = i32
+    lib.sv_alpha.argtypes = [P, i64, P, i64, i32, i32, i64, P, P, P, sz, P]
+    lib.sv_alpha.restype = ctypes.c_int
+    lib.sv_verify_sample_logits.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64,
+                                            ctypes.c_float, P, P, P, sz, P]
+    lib.sv_verify_sample_logits.restype = ctypes.c_int
+    lib.sv_status_string.argtypes = [ctypes.c_int]
+    lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_version.argtypes = []
+    lib.sv_version.restype = ctypes.c_int
+    lib.sv_verify_sample_noalloc.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P]
+    lib.sv_verify_sample_noalloc.restype = ctypes.c_int
+    return lib
 
 
 def status_string(code: int) -> str:

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "specverify.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "sv_tma.cuh"),
                      os.path.join(CSRC, "sv_item.cuh"), os.path.join(CSRC, "sv_alpha.cuh"),
-                     os.path.join(CSRC, "sv_logits.cuh"),
+                     os.path.join(CSRC, "sv_logits.cuh"), os.path.join(CSRC, "sv_debug.cuh"),
                      os.path.join(INCLUDE, "specverify.h")]
 LIBRARY = os.path.join(PKG, "libspecverify.so")
 
@@ -46,3 +46,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIBRARY)
     return LIBRARY
+
+
+def build_debug(out: str) -> str:
+    """Compiles a debug build of the library into `out` (SV_DEBUG=1: every
+    call checks its input rows for negative, NaN or infinite values before
+    its kernels and reports them as SV_STATUS_BAD_VALUE).  The regular build
+    is left as it is."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *NVCC_FLAGS, "-DSV_DEBUG=1", "-I", INCLUDE, "-o", tmp, *SOURCES]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out

@@ -19,6 +19,16 @@
 #include "sv_logits.cuh"
 #include "specverify.h"
 
+// A debug build (-DSV_DEBUG=1) checks the inputs' values before each call's
+// kernels and reports NaN, negative or infinite probabilities as
+// SV_STATUS_BAD_VALUE; the default build contains no such check.
+#ifndef SV_DEBUG
+#define SV_DEBUG 0
+#endif
+#if SV_DEBUG
+#include "sv_debug.cuh"
+#endif
+
 // Segments (1024 elements) per item of the single-launch kernel: sampling
 // rows are streamed whole by one CTA (a draw then needs no other CTA's sums
 // early, and an item switch costs the producer more than the finer balance
@@ -428,6 +438,21 @@ int bind_workspace(sv::Params &P, void *ws, size_t bytes) {
     return SV_OK;
 }
 
+// Debug builds: the value check of p (and of q when with_q) on the stream,
+// ahead of the verification kernels; a no-op otherwise.
+int debug_check(const sv::Params &P, bool with_q, bool finite_only, cudaStream_t st) {
+#if SV_DEBUG
+    if (sv::check_values(P.p, P.ps, (int64_t)P.B * (P.K + 1), P.V, finite_only, P.status, st))
+        return SV_ECUDA;
+    if (with_q && P.K > 0 &&
+        sv::check_values(P.q, P.qs, (int64_t)P.B * P.K, P.V, finite_only, P.status, st))
+        return SV_ECUDA;
+#else
+    (void)P, (void)with_q, (void)finite_only, (void)st;
+#endif
+    return SV_OK;
+}
+
 int common_checks(const float *p, int64_t ps, const int32_t *t, int32_t B, int32_t K, int64_t V,
                   const int32_t *n_out, const int32_t *next_out) {
     if (!sizes_ok(B, K, V)) return SV_EINVAL;
@@ -485,6 +510,7 @@ int sv_verify_greedy(const float *p, int64_t p_row_stride, const int32_t *t, int
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
     if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
+    if ((rc = debug_check(P, false, false, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kGreedy, P, stream);
 }
 
@@ -501,6 +527,7 @@ int sv_verify_sample(const float *p, int64_t p_row_stride, const float *q, int64
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
     if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
+    if ((rc = debug_check(P, true, false, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kSample, P, stream);
 }
 
@@ -522,6 +549,7 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride, c
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
     if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
+    if ((rc = debug_check(P, true, false, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kPerSequence, P, stream);
 }
 
@@ -554,6 +582,12 @@ int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row
         return SV_EINVAL;
     A.norm = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + L.norm);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+#if SV_DEBUG
+    uint32_t *status = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.status);
+    if (sv::check_values(A.p, A.ps, (int64_t)B * (K + 1), V, false, status, st) ||
+        (K > 0 && sv::check_values(A.q, A.qs, (int64_t)B * K, V, false, status, st)))
+        return SV_ECUDA;
+#endif
     g_last_grid = (int64_t)B * K;
     g_last_kernels = 0;
     if (K > 0) {
@@ -591,6 +625,7 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     if ((rc = bind_workspace(P, workspace, workspace_bytes)) != SV_OK) return rc;
     if ((rc = place_arrays(P)) != SV_OK) return rc;
     if ((rc = prepare_state(P, workspace, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
+    if ((rc = debug_check(P, true, true, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     const Layout W = layout(B, K, V);
     char *ws = static_cast<char *>(workspace);
     sv::LogitsParams L{};
@@ -671,6 +706,8 @@ const char *sv_status_string(int code) {
         case (int)SV_STATUS_OVERFLOW: return "commit would pass max_len";
         case (int)SV_STATUS_BAD_MODE: return "round mode other than 0 (greedy) or 1 (sampling)";
         case (int)SV_STATUS_TIMEOUT: return "a bounded wait inside a kernel gave up";
+        case (int)SV_STATUS_BAD_VALUE:
+            return "an input probability is negative, NaN or infinite (debug builds)";
         default: return "unknown code";
     }
 }
@@ -734,5 +771,6 @@ extern "C" int sv_verify_sample_noalloc(const float *p, int64_t p_row_stride, co
                                nullptr, B, K, V, n_accepted, next_token);
     if ((rc = bind_workspace(P, scratch, SV_NOALLOC_SCRATCH_BYTES)) != SV_OK) return rc;
     if ((rc = place_arrays(P)) != SV_OK) return rc;
+    if ((rc = debug_check(P, true, false, reinterpret_cast<cudaStream_t>(stream))) != SV_OK) return rc;
     return launch(sv::kSample, P, stream);
 }

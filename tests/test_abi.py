@@ -119,3 +119,15 @@ def test_alpha_logits_and_noalloc_reject_bad_arguments_on_host(lib):
                                         dummy, None) == sv.SV_ETOOLARGE
     assert lib.sv_verify_sample_noalloc(dummy, V, None, V, dummy, dummy, dummy, B, K, V, dummy,
                                         dummy, None) == -1
+
+
+def test_debug_build_compiles_and_exports_every_symbol(lib, tmp_path):
+    """The SV_DEBUG=1 variant (input values checked before each call's
+    kernels) builds beside the regular library and offers the same calls."""
+    from speculative_decoding_verification_08_gb300 import _build
+    dbg = sv._declare(ctypes.CDLL(_build.build_debug(str(tmp_path / "libspecverify_debug.so"))))
+    for name in declared_symbols():
+        assert hasattr(dbg, name), name
+    assert dbg.sv_workspace_size(256, 5, 128256) == lib.sv_workspace_size(256, 5, 128256)
+    assert b"NaN" in dbg.sv_status_string(sv.STATUS_BAD_VALUE)
+    assert sv.status_string(sv.STATUS_BAD_VALUE) == dbg.sv_status_string(sv.STATUS_BAD_VALUE).decode()
