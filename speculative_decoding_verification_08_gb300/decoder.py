@@ -74,7 +74,9 @@ class SpeculationGovernor:
 class DeviceVerifier:
     """One verification round on the GPU (``sv_verify_round``) with the commit
     into the caller's device token buffer: the step both drivers take each
-    round.  Keeps one workspace per (B, K, V).
+    round.  Keeps one workspace per (K, V), replaced only by a larger batch:
+    a smaller batch reuses it (the library clears per-size state itself when
+    the sizes change between calls on one workspace).
 
     ``__call__(mode, p, q, t, u_acc, u_res, tokens, lengths)`` takes the
     tensors of ``verify_round`` (q is None when K = 0) and returns
@@ -87,11 +89,11 @@ class DeviceVerifier:
 
     def __call__(self, mode, p, q, t, u_acc, u_res, tokens, lengths):
         B, K, V = p.shape[0], t.shape[1], p.shape[2]
-        key = (B, K, V)
-        if key not in self._ws:
-            self._ws[key] = Workspace(B, K, V, self.device)
+        w = self._ws.get((K, V))
+        if w is None or not w.fits(B, K, V):
+            w = self._ws[(K, V)] = Workspace(B, K, V, self.device)
         return verify_round(mode, p, q if K > 0 else None, t, u_acc, u_res, tokens=tokens,
-                            lengths=lengths, ws=self._ws[key])
+                            lengths=lengths, ws=w)
 
 
 class _RoundDriver:
@@ -279,3 +281,125 @@ class PendingTokenDecoder(_RoundDriver):
             if cut is not None:
                 return cut
         return prefix[start:start + max_new]
+
+
+class BatchedSpeculativeDecoder:
+    """Speculative decoding of several sequences at once: one mixed
+    verification round per step over every sequence still running (a
+    per-sequence rule, greedy or sampling, and the commit into a device token
+    buffer of one row per sequence), as the batched kernels are built for.
+
+    ``draft_step(prefixes, k) -> (tokens [B'][k], probs [B'][k][V])`` and
+    ``target_step(prefixes, proposed) -> probs [B'][k + 1][V]`` take the
+    prefixes of the B' running sequences, in the order ``generate`` was given
+    them.  ``greedy`` is one flag for all sequences or one per sequence.  The
+    governor, if any, sees the batch's accepted and proposed totals per round
+    and, once it trips, every sequence continues with one-token rounds.
+    ``trace`` records (proposed, [(sequence, n_accepted, next_token), ...])
+    per round."""
+
+    def __init__(self, draft_step: Callable, target_step: Callable, k: int = 4, greedy=True,
+                 seed: int = 0, governor: Optional[SpeculationGovernor] = None, device=None,
+                 verify: Optional[Callable] = None):
+        if k < 1:
+            raise ValueError("k must be >= 1")
+        torch = _torch()
+        self.draft_step, self.target_step = draft_step, target_step
+        self.k, self.greedy = k, greedy
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.gen = torch.Generator(device=self.device)
+        self.gen.manual_seed(seed)
+        self.governor = governor
+        self.verify = DeviceVerifier(self.device) if verify is None else verify
+        self.trace: List[Tuple[int, List[Tuple[int, int, int]]]] = []
+
+    def _modes(self, B: int) -> List[int]:
+        flags = [self.greedy] * B if isinstance(self.greedy, bool) else list(self.greedy)
+        if len(flags) != B:
+            raise ValueError(f"greedy: expected {B} flags, got {len(flags)}")
+        return [0 if g else 1 for g in flags]
+
+    def _tensor(self, x, dtype):
+        """Callback output (a tensor, an array or nested lists) on the device."""
+        import numpy as np
+        torch = _torch()
+        if isinstance(x, torch.Tensor):
+            return x.to(device=self.device, dtype=dtype)
+        if isinstance(x, (list, tuple)):
+            x = np.stack([np.asarray(r) for r in x]) if len(x) else np.zeros((0,))
+        return torch.as_tensor(np.asarray(x), dtype=dtype, device=self.device)
+
+    def _rows(self, x, shape: Tuple[int, ...], what: str):
+        x = self._tensor(x, _torch().float32)
+        if tuple(x.shape[:-1]) != shape:
+            raise SpecVerifyError(f"{what}: expected {list(shape)} rows of V, got {tuple(x.shape)}")
+        return x.contiguous()
+
+    def generate(self, prompts: Sequence[Sequence[int]], max_new: int = 128,
+                 eos_id: Optional[int] = None) -> List[List[int]]:
+        torch = _torch()
+        prefixes = [[int(x) for x in pr] for pr in prompts]
+        B = len(prefixes)
+        if B == 0:
+            return []
+        starts = [len(pr) for pr in prefixes]
+        modes = self._modes(B)
+        cap = max(starts) + max_new + self.k + 1
+        tokens_buf = torch.zeros(B, cap, dtype=torch.int32, device=self.device)
+        for b, pr in enumerate(prefixes):
+            tokens_buf[b, :len(pr)] = torch.tensor(pr, dtype=torch.int32)
+        lengths_buf = torch.tensor(starts, dtype=torch.int32, device=self.device)
+        live = list(range(B))
+        self.trace = []
+        while live:
+            k = self.k if self.governor is None or self.governor.speculating else 0
+            L = len(live)
+            pre = [list(prefixes[b]) for b in live]
+            if k > 0:
+                toks, qprobs = self.draft_step(pre, k)
+                t = self._tensor(toks, torch.int32).reshape(L, k).contiguous()
+                rows = self.target_step(pre, t.cpu().tolist())
+            else:
+                t = torch.zeros(L, 0, dtype=torch.int32, device=self.device)
+                rows = self.target_step(pre, [[] for _ in live])
+            p = self._rows(rows, (L, k + 1), "target")
+            V = p.shape[-1]
+            q = (self._rows(qprobs, (L, k), "draft probs") if k > 0
+                 else torch.zeros(L, 0, V, device=self.device))
+            if q.shape[-1] != V:
+                raise SpecVerifyError("draft and target rows differ in V")
+            mode = torch.tensor([modes[b] for b in live], dtype=torch.uint8, device=self.device)
+            ua = torch.rand(L, k, generator=self.gen, device=self.device)
+            ur = torch.rand(L, generator=self.gen, device=self.device, dtype=torch.float64)
+            idx = torch.tensor(live, dtype=torch.int64, device=self.device)
+            whole = L == B
+            tok = tokens_buf if whole else tokens_buf.index_select(0, idx)
+            lens = lengths_buf if whole else lengths_buf.index_select(0, idx)
+            n, nxt = self.verify(mode, p, q, t, ua, ur, tok, lens)
+            if not whole:                      # the running rows back into place
+                tokens_buf.index_copy_(0, idx, tok)
+                lengths_buf.index_copy_(0, idx, lens)
+            n, nxt = n.cpu().tolist(), nxt.cpu().tolist()
+            if min(nxt) < 0:
+                raise SpecVerifyError("verification produced no token (invalid draft ids or "
+                                      "zero-mass rows)")
+            self.trace.append((k, [(b, int(n[i]), int(nxt[i])) for i, b in enumerate(live)]))
+            lengths = lengths_buf.cpu().tolist()
+            rows_host = tokens_buf.cpu()
+            done = []
+            for b in live:
+                prefixes[b] = rows_host[b, :lengths[b]].tolist()
+                out = prefixes[b][starts[b]:]
+                if len(out) >= max_new or (eos_id is not None and eos_id in out):
+                    done.append(b)
+            if self.governor is not None and k > 0:
+                self.governor.record(sum(int(x) for x in n), k * L)
+            live = [b for b in live if b not in done]
+        results = []
+        for b in range(B):
+            out = prefixes[b][starts[b]:]
+            if eos_id is not None and eos_id in out:
+                out = out[:out.index(eos_id) + 1]
+            results.append(out[:max_new])
+        return results
+

@@ -16,7 +16,8 @@ import torch
 
 import oracle
 import speculative_decoding_verification_08_gb300 as sv
-from speculative_decoding_verification_08_gb300.decoder import (PendingTokenDecoder,
+from speculative_decoding_verification_08_gb300.decoder import (BatchedSpeculativeDecoder,
+                                                                 PendingTokenDecoder,
                                                                  SpeculationGovernor,
                                                                  SpeculativeDecoder)
 
@@ -273,3 +274,77 @@ def test_pending_driver_on_the_gpu():
     out = dec.generate([1, 2, 3], max_new=60)
     assert out == plain_greedy([1, 2, 3], 60)
     assert target.passes == len(dec.trace) + 1
+
+
+# ---------------------------------------------------------------------------
+# the batched driver (bookkeeping on the CPU, the oracle in the verify hook)
+
+def batched_callbacks(noise=0.6, greedy_draft=True, seed=0):
+    draft_one, target_one = make_callbacks(noise, greedy_draft, seed)
+
+    def draft_step(prefixes, k):
+        out = [draft_one(pr, k) for pr in prefixes]
+        return [t for t, _ in out], np.stack([q for _, q in out])
+
+    def target_step(prefixes, proposed):
+        return np.stack([target_one(pr, pp) for pr, pp in zip(prefixes, proposed)])
+
+    return draft_step, target_step
+
+
+PROMPTS = [[1, 2, 3], [7], [4, 4, 4, 4, 4], [9, 8], [3, 1, 4, 1, 5, 9]]
+
+
+def test_batched_driver_greedy_on_cpu():
+    draft_step, target_step = batched_callbacks(noise=0.6)
+    dec = BatchedSpeculativeDecoder(draft_step, target_step, k=4, greedy=True, device="cpu",
+                                    verify=oracle_verify)
+    outs = dec.generate(PROMPTS, max_new=40)
+    assert outs == [plain_greedy(pr, 40) for pr in PROMPTS]
+    ns = [n for _, rnd in dec.trace for _, n, _ in rnd]
+    assert 0 < max(ns) and min(ns) < 4
+
+
+def test_batched_driver_mixed_modes_and_eos_on_cpu():
+    """Greedy sequences still decode exactly; an end token retires a sequence
+    early, so later rounds verify a subset of the batch."""
+    plains = [plain_greedy(pr, 40) for pr in PROMPTS]
+    eos = plains[0][6]
+    flags = [True, False, True, False, True]
+    draft_step, target_step = batched_callbacks(noise=0.7, greedy_draft=False, seed=3)
+    dec = BatchedSpeculativeDecoder(draft_step, target_step, k=3, greedy=flags, seed=9,
+                                    device="cpu", verify=oracle_verify)
+    outs = dec.generate(PROMPTS, max_new=40, eos_id=eos)
+    for b, (out, plain) in enumerate(zip(outs, plains)):
+        if eos in out:
+            assert out.index(eos) == len(out) - 1
+        else:
+            assert len(out) == 40
+        if flags[b]:
+            want = plain[:plain.index(eos) + 1] if eos in plain else plain
+            assert out == want, b
+    sizes = [len(rnd) for _, rnd in dec.trace]
+    assert sizes[0] == len(PROMPTS) and min(sizes) < len(PROMPTS)   # a subset ran
+
+
+def test_batched_driver_governor_and_single_sequence_sampling_on_cpu():
+    draft_step, target_step = batched_callbacks(noise=8.0)           # zero-accept rounds
+    gov = SpeculationGovernor(window=2, alpha_threshold=0.4)
+    dec = BatchedSpeculativeDecoder(draft_step, target_step, k=4, greedy=True, governor=gov,
+                                    device="cpu", verify=oracle_verify)
+    outs = dec.generate(PROMPTS[:3], max_new=25)
+    assert outs == [plain_greedy(pr, 25) for pr in PROMPTS[:3]]
+    ks = [k for k, _ in dec.trace]
+    assert not gov.speculating and 0 in ks and all(k == 0 for k in ks[ks.index(0):])
+    # one sequence: the same uniforms as the single-sequence driver, the same stream
+    one_d, one_t = make_callbacks(noise=0.8, greedy_draft=False, seed=21)
+    single = SpeculativeDecoder(one_d, one_t, k=4, greedy=False, seed=77, device="cpu",
+                                verify=oracle_verify)
+    want = single.generate([2, 7, 1], max_new=30)
+    draft_step, target_step = batched_callbacks(noise=0.8, greedy_draft=False, seed=21)
+    dec = BatchedSpeculativeDecoder(draft_step, target_step, k=4, greedy=False, seed=77,
+                                    device="cpu", verify=oracle_verify)
+    assert dec.generate([[2, 7, 1]], max_new=30) == [want]
+    with pytest.raises(ValueError):
+        BatchedSpeculativeDecoder(draft_step, target_step, greedy=[True], device="cpu",
+                                  verify=oracle_verify).generate(PROMPTS[:2], max_new=3)
