@@ -63,6 +63,10 @@ def parse_args(argv=None):
                     help="end-to-end leg copies all inputs to the device each step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--trace", action="store_true",
+                    help="build the trace variant of the library, record one launch of the "
+                         "item kernel after the warm-up and print its timeline summary "
+                         "(no timing line)")
     a = ap.parse_args(argv)
     if a.mode is None:
         a.mode = DEFAULT_MODE[a.config]
@@ -385,6 +389,12 @@ def main(argv=None):
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     sv.build()
     lib = sv.load()
+    if args.trace:
+        # the same calls through a trace build of the library (SV_TRACE=1)
+        import tempfile
+        from speculative_decoding_verification_08_gb300 import _build
+        out = os.path.join(tempfile.mkdtemp(prefix="specverify_trace"), "libspecverify_trace.so")
+        lib = sv._declare(ctypes.CDLL(_build.build_trace(out)))
     if args.ctas_per_sm:
         sv.set_ctas_per_sm(args.ctas_per_sm)
 
@@ -472,6 +482,15 @@ def main(argv=None):
         warm_up()
         req_per_launch, req, dense, nhist = required_per_launch()
     torch.cuda.empty_cache()
+    if args.trace:
+        # one more launch (the next input set of the rotation) with the buffer cleared
+        sv.trace_reset(stream, lib)
+        step(0)
+        summary = sv.trace_summary(sv.trace_read(stream, lib))
+        if rank == 0:
+            print(json.dumps({"trace": summary, "config": workload_config(args, B, K, V),
+                              "mode": args.mode}))
+        return 0
     status = ws.status(stream)
     kernels_per_step = sv.last_kernel_count()
     grid_ctas = int(sv.last_grid_size())     # of the timed launches (the e2e leg may differ)

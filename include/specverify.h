@@ -250,6 +250,27 @@ const char *sv_status_string(int code);
 /* Library ABI version (this header: 1). */
 int sv_version(void);
 
+/* Timeline of the single-launch item kernel, for performance work; the pages
+ * have no counterpart.  Only a library built with -DSV_TRACE=1 records it;
+ * in any other build both calls return SV_EINVAL.  Each CTA appends records
+ * of two uint64 words to its own region of a static device buffer
+ * (SV_TRACE_RECORDS records, SV_TRACE_CTA_RECORDS per CTA; later ones are
+ * dropped): word 0 is %globaltimer in ns, word 1 holds the event id in bits
+ * 56..63, the CTA in bits 32..55 and the event's argument in bits 0..31.
+ * Events: 0 CTA start, 1 item start (sequence), 2 stage issued (count),
+ * 3 item fully issued (stages), 4 item retired (sequence), 5 decision start
+ * (sequence), 6 decision end (sequence), 7 producer done.
+ *   sv_trace_reset: enqueues the clearing of the buffer on `stream` (empty
+ *     records have time 0).  Calls that record while another is traced mix
+ *     their records.
+ *   sv_trace_read: copies the first min(max_records, SV_TRACE_RECORDS)
+ *     records into `records` (host memory of 16 * max_records bytes), waits
+ *     for `stream`, and sets *count to the number copied. */
+#define SV_TRACE_CTA_RECORDS 512
+#define SV_TRACE_RECORDS (512u * 1024u)
+int sv_trace_reset(sv_stream_t stream);
+int sv_trace_read(void *records, size_t max_records, size_t *count, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

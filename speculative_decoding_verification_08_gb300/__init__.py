@@ -42,7 +42,8 @@ EXPORTED = (
     "sv_workspace_size", "sv_workspace_init", "sv_verify_greedy", "sv_verify_sample",
     "sv_verify_round", "sv_get_status", "sv_set_ctas_per_sm", "sv_last_grid_size",
     "sv_last_kernel_count", "sv_alpha", "sv_verify_sample_logits",
-    "sv_status_string", "sv_version", "sv_verify_sample_noalloc",
+    "sv_status_string", "sv_version", "sv_verify_sample_noalloc", "sv_trace_reset",
+    "sv_trace_read",
 )
 
 _lock = threading.Lock()
@@ -107,6 +108,10 @@ def _declare(lib):
     lib.sv_version.restype = ctypes.c_int
     lib.sv_verify_sample_noalloc.argtypes = [P, i64, P, i64, P, P, P, i32, i32, i64, P, P, P]
     lib.sv_verify_sample_noalloc.restype = ctypes.c_int
+    lib.sv_trace_reset.argtypes = [P]
+    lib.sv_trace_reset.restype = ctypes.c_int
+    lib.sv_trace_read.argtypes = [P, sz, ctypes.POINTER(sz), P]
+    lib.sv_trace_read.restype = ctypes.c_int
     return lib
 
 
@@ -486,3 +491,85 @@ class HostVerifier:
         self.next_host.copy_(self.next, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         return self.n_host, self.next_host
+
+
+# ---------------------------------------------------------------------------
+# timeline of the item kernel (a library built with SV_TRACE=1)
+
+TRACE_RECORDS = 512 * 1024
+TRACE_EVENTS = ("cta_begin", "item_begin", "stage", "item_issued", "item_retired",
+                "decide_begin", "decide_end", "producer_end")
+
+
+def trace_reset(stream=None, lib=None):
+    """Clears the trace buffer on the stream (a trace build; SpecVerifyError otherwise)."""
+    _check((lib or load()).sv_trace_reset(_stream_handle(stream)), "sv_trace_reset")
+
+
+def trace_read(stream=None, lib=None):
+    """The recorded events as a uint64 array [N][2] (time in ns, event word),
+    empty slots dropped; waits for the stream."""
+    import numpy as np
+    buf = np.zeros((TRACE_RECORDS, 2), dtype=np.uint64)
+    n = ctypes.c_size_t(0)
+    _check((lib or load()).sv_trace_read(buf.ctypes.data_as(ctypes.c_void_p), TRACE_RECORDS,
+                                         ctypes.byref(n), _stream_handle(stream)),
+           "sv_trace_read")
+    buf = buf[:n.value]
+    return buf[buf[:, 0] != 0]
+
+
+def trace_summary(records) -> dict:
+    """Where one traced launch's time went, in microseconds from the earliest
+    CTA start: the spread of CTA starts, each CTA's delay to its first stage,
+    the last stage issued, the last item retired, the last decision written,
+    decision times, and items and stages per CTA."""
+    import numpy as np
+    rec = np.asarray(records, dtype=np.uint64).reshape(-1, 2)
+    if rec.shape[0] == 0:
+        return {}
+    t = rec[:, 0].astype(np.int64)
+    w = rec[:, 1]
+    ev = (w >> np.uint64(56)).astype(np.int64)
+    cta = ((w >> np.uint64(32)) & np.uint64(0xFFFFFF)).astype(np.int64)
+    arg = (w & np.uint64(0xFFFFFFFF)).astype(np.int64)
+    begin = ev == TRACE_EVENTS.index("cta_begin")
+    t0 = t[begin].min() if begin.any() else t.min()
+    us = (t - t0) / 1e3
+
+    def last(name):
+        m = ev == TRACE_EVENTS.index(name)
+        return float(us[m].max()) if m.any() else None
+
+    first_stage = []
+    stage = ev == TRACE_EVENTS.index("stage")
+    for c in np.unique(cta[begin]):
+        mine = stage & (cta == c)
+        if mine.any():
+            first_stage.append(float(us[mine].min() - us[begin & (cta == c)].min()))
+    starts = {}
+    decide = []
+    for i in np.nonzero(ev == TRACE_EVENTS.index("decide_begin"))[0]:
+        starts[(int(cta[i]), int(arg[i]))] = us[i]
+    for i in np.nonzero(ev == TRACE_EVENTS.index("decide_end"))[0]:
+        s0 = starts.get((int(cta[i]), int(arg[i])))
+        if s0 is not None:
+            decide.append(float(us[i] - s0))
+    items = np.bincount(cta[ev == TRACE_EVENTS.index("item_begin")])
+    items = items[items > 0]
+
+    def stats(x):
+        return {"median": float(np.median(x)), "max": float(np.max(x))} if len(x) else None
+
+    return {
+        "ctas": int(np.unique(cta[begin]).size),
+        "cta_begin_spread_us": float(us[begin].max()) if begin.any() else None,
+        "first_stage_after_begin_us": stats(first_stage),
+        "last_stage_us": last("stage"),
+        "last_item_retired_us": last("item_retired"),
+        "last_decide_end_us": last("decide_end"),
+        "span_us": float(us.max()),
+        "decide_us": stats(decide),
+        "items_per_cta": stats(items) if items.size else None,
+        "stages": int(stage.sum()),
+    }

@@ -12,6 +12,7 @@ SOURCES = [os.path.join(CSRC, "specverify.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "sv_device.cuh"), os.path.join(CSRC, "sv_tma.cuh"),
                      os.path.join(CSRC, "sv_item.cuh"), os.path.join(CSRC, "sv_alpha.cuh"),
                      os.path.join(CSRC, "sv_logits.cuh"), os.path.join(CSRC, "sv_debug.cuh"),
+                     os.path.join(CSRC, "sv_trace.cuh"),
                      os.path.join(INCLUDE, "specverify.h")]
 LIBRARY = os.path.join(PKG, "libspecverify.so")
 
@@ -48,13 +49,24 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIBRARY
 
 
-def build_debug(out: str) -> str:
-    """Compiles a debug build of the library into `out` (SV_DEBUG=1: every
-    call checks its input rows for negative, NaN or infinite values before
-    its kernels and reports them as SV_STATUS_BAD_VALUE).  The regular build
-    is left as it is."""
+def build_variant(out: str, defines) -> str:
+    """Compiles the library with extra -D flags into `out`; the regular
+    build is left as it is."""
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-DSV_DEBUG=1", "-I", INCLUDE, "-o", tmp, *SOURCES]
+    cmd = [nvcc(), *NVCC_FLAGS, *defines, "-I", INCLUDE, "-o", tmp, *SOURCES]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
+
+
+def build_debug(out: str) -> str:
+    """A debug build (SV_DEBUG=1): every call checks its input rows for
+    negative, NaN or infinite values before its kernels and reports them as
+    SV_STATUS_BAD_VALUE."""
+    return build_variant(out, ["-DSV_DEBUG=1"])
+
+
+def build_trace(out: str) -> str:
+    """A trace build (SV_TRACE=1): the item kernel records a timeline that
+    sv_trace_read returns."""
+    return build_variant(out, ["-DSV_TRACE=1"])

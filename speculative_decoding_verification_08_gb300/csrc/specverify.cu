@@ -28,6 +28,10 @@
 #if SV_DEBUG
 #include "sv_debug.cuh"
 #endif
+// A trace build (-DSV_TRACE=1) records a timeline of the item kernel
+// (sv_trace.cuh); sv_trace_reset and sv_trace_read return SV_EINVAL otherwise.
+static_assert(SV_TRACE_CTA_RECORDS == sv::kTraceCtaCap && SV_TRACE_RECORDS == sv::kTraceRecords,
+              "trace buffer sizes in specverify.h and sv_trace.cuh differ");
 
 // Segments (1024 elements) per item of the single-launch kernel: sampling
 // rows are streamed whole by one CTA (a draw then needs no other CTA's sums
@@ -713,6 +717,38 @@ const char *sv_status_string(int code) {
 }
 
 int sv_version(void) { return 1; }
+
+int sv_trace_reset(sv_stream_t stream) {
+#if SV_TRACE
+    void *buf = nullptr;
+    if (cudaGetSymbolAddress(&buf, sv::sv_trace_buf) != cudaSuccess) return SV_ECUDA;
+    if (cudaMemsetAsync(buf, 0, sizeof(ulonglong2) * sv::kTraceRecords,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SV_ECUDA;
+    return SV_OK;
+#else
+    (void)stream;
+    return SV_EINVAL;
+#endif
+}
+
+int sv_trace_read(void *records, size_t max_records, size_t *count, sv_stream_t stream) {
+    if (count) *count = 0;
+    if (!records || !count) return SV_EINVAL;
+#if SV_TRACE
+    const size_t n = std::min(max_records, sv::kTraceRecords);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyFromSymbolAsync(records, sv::sv_trace_buf, n * sizeof(ulonglong2), 0,
+                                  cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return SV_ECUDA;
+    *count = n;
+    return SV_OK;
+#else
+    (void)max_records, (void)stream;
+    return SV_EINVAL;
+#endif
+}
 
 }  // extern "C"
 

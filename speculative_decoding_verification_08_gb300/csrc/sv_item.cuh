@@ -36,6 +36,7 @@
 #pragma once
 
 #include "sv_tma.cuh"
+#include "sv_trace.cuh"
 
 namespace sv {
 
@@ -218,6 +219,7 @@ struct ItemProducer {
         if (c0) bulk_copy_g2s(d, g0, 4u * c0, &sh.full[k]);
         if (c1) bulk_copy_g2s(d + kPartBytes, g1, 4u * c1, &sh.full[k]);
         ++fills;
+        SV_TRACE_EVENT(kTrStage, fills);
         if (++k == kStages) {
             k = 0;
             phase ^= 1u;
@@ -478,6 +480,7 @@ __device__ void item_produce_end(const Params &P, ItemShared &sh, ItemProducer &
         m.kind = kStop;
         for (int i = 0; i < kTmaConsumers && pr.ok; ++i)  // one stop per consumer
             pr.ok = pr.put(m, nullptr, 0, nullptr, 0);
+        SV_TRACE_EVENT(kTrProducerEnd, 0);
     }
     pr.sync_ok();
     if (!pr.ok && lane == 0) atomicOr(P.status, kStatusTimeout);
@@ -521,6 +524,7 @@ __device__ void item_produce_greedy(const Params &P, ItemShared &sh, unsigned ch
         for (int i = lane; i <= P.K; i += 32) sl.keys[i] = 0ull;
         unsigned claim = 0;
         if (lane == 0) {
+            SV_TRACE_EVENT(kTrItemBegin, c.b);
             sl.b = c.b;
             sl.rule = kGreedy;
             sl.ns = 1;
@@ -536,6 +540,7 @@ __device__ void item_produce_greedy(const Params &P, ItemShared &sh, unsigned ch
         int ns = 1;
         const int stages = pr.stream_greedy_lazy(c, x, SV_GREEDY_EARLY, ns);
         if (lane == 0) {
+            SV_TRACE_EVENT(kTrItemIssued, stages);
             sl.ns = ns;
             sl.issued = stages;
             __threadfence_block();
@@ -588,6 +593,7 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
         ItemSlot &sl = sh.slot[x];
         for (int i = lane; i <= P.K; i += 32) sl.keys[i] = 0ull;
         if (lane == 0) {
+            SV_TRACE_EVENT(kTrItemBegin, c.b);
             sl.b = c.b;
             sl.rule = c.rule;
             sl.ns = ns;
@@ -614,6 +620,7 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
             else stages = pr.stream_greedy(c, x);
         }
         if (lane == 0) {
+            SV_TRACE_EVENT(kTrItemIssued, stages);
             sl.issued = stages;
             __threadfence_block();
             *(volatile int *)&sl.state = 2;
@@ -847,6 +854,7 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
             if (lane == 0) *(volatile int *)&sl.state = 0;  // the producer may refill it now
             __syncwarp();
             did = true;
+            if (lane == 0) SV_TRACE_EVENT(kTrItemRetired, b);
             // a whole-row item with its sums in shared memory is its sequence
             if (sb < 0 && !item_retire(P, b, rule, ns, miss, k0, k1, k2, lane)) continue;
             // queue the sequence for the decide warps (once its entry's previous
@@ -932,10 +940,12 @@ __device__ void item_decide_loop(const Params &P, ItemShared &sh, unsigned long 
         __syncwarp();
         if (lane == 0) *(volatile int *)&e->w = 0;  // the entry may be reused
         if (sb < 0) __threadfence();  // the other items' results after their counts
+        if (lane == 0) SV_TRACE_EVENT(kTrDecideBegin, b);
         item_decide_sequence(P, dbar,
                              reinterpret_cast<float2 *>(sumbufs + d * kSumBufBytes + kSumBlkOffset),
                              sb >= 0 ? sumbufs + sb * kSumBufBytes : nullptr, dphase, b, rule, ns,
                              lane);
+        if (lane == 0) SV_TRACE_EVENT(kTrDecideEnd, b);
         if (sb >= 0) {
             __syncwarp();
             if (lane == 0) {
@@ -1007,12 +1017,14 @@ __global__ void __launch_bounds__(kItemThreads, 2) item_round_kernel(const Param
         sh.dq_head = 0;
         sh.dq_claim = 0;
         sh.ticket = 0;
+        SV_TRACE_INIT();
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     // launched as a programmatic dependent: the set-up above may overlap the
     // previous grid; nothing in global memory is touched before it is done
     wait_for_primary_grid();
+    if (threadIdx.x == 0) SV_TRACE_EVENT(kTrCtaBegin, 0);
     if (warp == kItemProducerWarp) {
         if constexpr (kRule == kGreedy) item_produce_greedy(P, sh, buf, lane);
         else item_produce<kRule>(P, sh, buf, smem + kItemHeaderBytes, lane);

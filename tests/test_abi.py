@@ -131,3 +131,49 @@ def test_debug_build_compiles_and_exports_every_symbol(lib, tmp_path):
     assert dbg.sv_workspace_size(256, 5, 128256) == lib.sv_workspace_size(256, 5, 128256)
     assert b"NaN" in dbg.sv_status_string(sv.STATUS_BAD_VALUE)
     assert sv.status_string(sv.STATUS_BAD_VALUE) == dbg.sv_status_string(sv.STATUS_BAD_VALUE).decode()
+
+
+def test_trace_calls_refused_outside_a_trace_build(lib):
+    n = ctypes.c_size_t(7)
+    buf = ctypes.create_string_buffer(64)
+    assert lib.sv_trace_reset(None) == -1
+    assert lib.sv_trace_read(buf, 4, ctypes.byref(n), None) == -1 and n.value == 0
+    assert lib.sv_trace_read(None, 4, ctypes.byref(n), None) == -1
+
+
+def test_trace_build_compiles_and_exports_every_symbol(tmp_path):
+    from speculative_decoding_verification_08_gb300 import _build
+    tr = sv._declare(ctypes.CDLL(_build.build_trace(str(tmp_path / "libspecverify_trace.so"))))
+    for name in declared_symbols():
+        assert hasattr(tr, name), name
+    n = ctypes.c_size_t(7)
+    assert tr.sv_trace_read(None, 4, ctypes.byref(n), None) == -1 and n.value == 0
+
+
+def test_trace_summary_of_known_records():
+    """Two CTAs, times in ns from an arbitrary origin."""
+    import numpy as np
+    E = {name: i for i, name in enumerate(sv.TRACE_EVENTS)}
+
+    def r(t, ev, cta, arg=0):
+        return [t, (E[ev] << 56) | (cta << 32) | arg]
+
+    T = 10_000_000
+    recs = np.array([
+        r(T, "cta_begin", 0), r(T + 500, "cta_begin", 1),
+        r(T + 1000, "item_begin", 0, 3), r(T + 1800, "stage", 0, 1), r(T + 2600, "stage", 0, 2),
+        r(T + 1500, "item_begin", 1, 4), r(T + 3500, "stage", 1, 1),
+        r(T + 9000, "item_retired", 0, 3), r(T + 9500, "decide_begin", 0, 3),
+        r(T + 12500, "decide_end", 0, 3), r(T + 11000, "item_retired", 1, 4),
+        r(T + 11200, "decide_begin", 1, 4), r(T + 12200, "decide_end", 1, 4),
+        r(T + 13000, "producer_end", 1),
+    ], dtype=np.uint64)
+    s = sv.trace_summary(recs)
+    assert s["ctas"] == 2 and s["stages"] == 3
+    assert s["cta_begin_spread_us"] == 0.5
+    assert s["first_stage_after_begin_us"] == {"median": 2.4, "max": 3.0}
+    assert s["last_stage_us"] == 3.5 and s["last_item_retired_us"] == 11.0
+    assert s["last_decide_end_us"] == 12.5 and s["span_us"] == 13.0
+    assert s["decide_us"] == {"median": 2.0, "max": 3.0}
+    assert s["items_per_cta"] == {"median": 1.0, "max": 1.0}
+    assert sv.trace_summary(np.zeros((0, 2), np.uint64)) == {}

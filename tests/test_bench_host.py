@@ -58,3 +58,10 @@ def test_max_over_ranks_gloo():
         res = dict(out)
     assert res[0][0] == res[1][0] == 15.0
     assert np.isclose(res[0][1], 1000 * 2 / 0.015)
+
+
+def test_trace_flag_parses():
+    import bench
+    a = bench.parse_args(["--trace", "--mode", "greedy"])
+    assert a.trace and a.mode == "greedy"
+    assert not bench.parse_args([]).trace
