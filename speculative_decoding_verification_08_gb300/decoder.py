@@ -97,9 +97,14 @@ class DeviceVerifier:
 
 
 class _RoundDriver:
-    """What both drivers share: the draft callback, the rule, the uniforms'
-    generator, the governor, the device token buffer and one verification
-    round over given rows."""
+    """What the single-sequence drivers share: the draft callback, the rule,
+    the uniforms' generator, the governor, the device token buffer and one
+    verification round over given rows.
+
+    ``verify`` is the verification step, called as ``DeviceVerifier`` is.  It
+    defaults to ``DeviceVerifier`` (the CUDA library); there is no CPU path.
+    The tests pass the oracle here to check a driver's own bookkeeping on a
+    machine without a GPU."""
 
     def __init__(self, draft_step: Callable, k: int, greedy: bool, seed: int,
                  governor: Optional[SpeculationGovernor], device, verify: Optional[Callable]):
@@ -295,6 +300,7 @@ class BatchedSpeculativeDecoder:
     them.  ``greedy`` is one flag for all sequences or one per sequence.  The
     governor, if any, sees the batch's accepted and proposed totals per round
     and, once it trips, every sequence continues with one-token rounds.
+    ``verify`` as for ``SpeculativeDecoder`` (default: ``DeviceVerifier``).
     ``trace`` records (proposed, [(sequence, n_accepted, next_token), ...])
     per round."""
 
