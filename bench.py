@@ -63,6 +63,8 @@ def parse_args(argv=None):
                     help="end-to-end leg copies all inputs to the device each step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--seed", type=int, default=0,
+                    help="offset of the input sets' seeds (0: the documented inputs)")
     ap.add_argument("--trace", action="store_true",
                     help="build the trace variant of the library, record one launch of the "
                          "item kernel after the warm-up and print its timeline summary "
@@ -83,10 +85,33 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def rank_seed(cfg: int, set_index: int, rank: int) -> int:
-    """Seed of input set `set_index` on `rank`: every rank verifies its own batch."""
+def rank_seed(cfg: int, set_index: int, rank: int, offset: int = 0) -> int:
+    """Seed of input set `set_index` on `rank`: every rank verifies its own
+    batch; `offset` (--seed) moves every set to other inputs."""
     from speculative_decoding_verification_08_gb300.inputs import SEED_BASE
-    return SEED_BASE + cfg + 1000 * set_index + 100000 * rank
+    return SEED_BASE + cfg + 1000 * set_index + 100000 * rank + 10_000_000 * offset
+
+
+class nvtx_range:
+    """An NVTX range (for ncu --nvtx filtering); nothing if torch lacks NVTX."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            import torch
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:
+            self.pushed = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            import torch
+            torch.cuda.nvtx.range_pop()
+        return False
 
 
 def reduce_max(x: float, device=None) -> float:
@@ -342,7 +367,7 @@ def run_reference(args):
     from speculative_decoding_verification_08_gb300.inputs import CONFIGS
     c = CONFIGS[args.config]
     B, K, V = c["B"], c["K"], c["V"]
-    host = host_inputs(args.config, rank_seed(args.config, 0, 0))
+    host = host_inputs(args.config, rank_seed(args.config, 0, 0, args.seed))
     ncpu = os.cpu_count() or 1
     # calibrate: sequences per step so that warmup + steps stay within ~2 minutes
     _, _, _, el = time_oracle(host, args.mode, K, 0.0, ncpu, max_rounds=1)
@@ -411,7 +436,7 @@ def main(argv=None):
         """Appends input sets and their precomputed C-ABI argument lists (the
         timed loop is one C call per step)."""
         for s_idx in range(len(sets), len(sets) + count):
-            bt = make_inputs(args.config, dev, seed=rank_seed(args.config, s_idx, rank))
+            bt = make_inputs(args.config, dev, seed=rank_seed(args.config, s_idx, rank, args.seed))
             n = torch.empty(B, dtype=torch.int32, device=dev)
             nx = torch.empty(B, dtype=torch.int32, device=dev)
             sets.append(bt)
@@ -449,9 +474,10 @@ def main(argv=None):
             raise RuntimeError(f"verify call failed: {sv.status_string(rc)}")
 
     def warm_up():
-        for k in range(max(args.warmup, len(calls))):   # every set's outputs at least once
-            step(k)
-        torch.cuda.synchronize(dev)
+        with nvtx_range("warmup"):
+            for k in range(max(args.warmup, len(calls))):   # every set's outputs at least once
+                step(k)
+            torch.cuda.synchronize(dev)
 
     def required_per_launch():
         """Algorithmic bytes per launch, from each set's n_accepted; with the
@@ -511,18 +537,19 @@ def main(argv=None):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
-    e0.record(stream)
-    if graph is None:
-        for k in range(args.steps):
-            step(k)
-        launches = args.steps
-    else:
-        reps = max(1, args.steps // len(calls))
-        with torch.cuda.stream(stream):
-            for _ in range(reps):
-                graph.replay()
-        launches = reps * len(calls)
-    e1.record(stream)
+    with nvtx_range("timed"):
+        e0.record(stream)
+        if graph is None:
+            for k in range(args.steps):
+                step(k)
+            launches = args.steps
+        else:
+            reps = max(1, args.steps // len(calls))
+            with torch.cuda.stream(stream):
+                for _ in range(reps):
+                    graph.replay()
+            launches = reps * len(calls)
+        e1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier()
