@@ -348,3 +348,41 @@ def test_batched_driver_governor_and_single_sequence_sampling_on_cpu():
     with pytest.raises(ValueError):
         BatchedSpeculativeDecoder(draft_step, target_step, greedy=[True], device="cpu",
                                   verify=oracle_verify).generate(PROMPTS[:2], max_new=3)
+
+
+def test_device_verifier_reuses_a_workspace_per_k_and_v(monkeypatch):
+    """One workspace per (K, V), replaced only when a larger batch comes (the
+    library clears per-size state itself); the CUDA calls are stubbed here."""
+    import speculative_decoding_verification_08_gb300.decoder as dm
+
+    made, used = [], []
+
+    class FakeWorkspace:
+        def __init__(self, B, K, V, device=None):
+            self.B, self.K, self.V = B, K, V
+            made.append((B, K, V))
+
+        def fits(self, B, K, V):
+            return K == self.K and V == self.V and B <= self.B
+
+    def fake_round(mode, p, q, t, ua, ur, tokens=None, lengths=None, ws=None):
+        used.append(ws)
+        return None, None
+
+    monkeypatch.setattr(dm, "Workspace", FakeWorkspace)
+    monkeypatch.setattr(dm, "verify_round", fake_round)
+    ver = dm.DeviceVerifier("cpu")
+
+    def call(B, K, V):
+        p = torch.zeros(B, K + 1, V)
+        ver(None, p, torch.zeros(B, K, V), torch.zeros(B, K, dtype=torch.int32), None, None,
+            None, None)
+
+    call(5, 4, 10)
+    call(3, 4, 10)          # smaller batch: the same workspace
+    call(5, 4, 10)
+    call(6, 4, 10)          # larger: a new one
+    call(2, 0, 10)          # another K: its own
+    call(4, 4, 10)
+    assert made == [(5, 4, 10), (6, 4, 10), (2, 0, 10)]
+    assert used[0] is used[1] is used[2] and used[3] is used[5] and used[3] is not used[0]
