@@ -97,7 +97,7 @@ class DeviceVerifier:
 
 
 class _RoundDriver:
-    """What the single-sequence drivers share: the draft callback, the rule,
+    """What the drivers share: the draft callback, the rule,
     the uniforms' generator, the governor, the device token buffer and one
     verification round over given rows.
 
@@ -288,7 +288,7 @@ class PendingTokenDecoder(_RoundDriver):
         return prefix[start:start + max_new]
 
 
-class BatchedSpeculativeDecoder:
+class BatchedSpeculativeDecoder(_RoundDriver):
     """Speculative decoding of several sequences at once: one mixed
     verification round per step over every sequence still running (a
     per-sequence rule, greedy or sampling, and the commit into a device token
@@ -307,16 +307,8 @@ class BatchedSpeculativeDecoder:
     def __init__(self, draft_step: Callable, target_step: Callable, k: int = 4, greedy=True,
                  seed: int = 0, governor: Optional[SpeculationGovernor] = None, device=None,
                  verify: Optional[Callable] = None):
-        if k < 1:
-            raise ValueError("k must be >= 1")
-        torch = _torch()
-        self.draft_step, self.target_step = draft_step, target_step
-        self.k, self.greedy = k, greedy
-        self.device = torch.device("cuda") if device is None else torch.device(device)
-        self.gen = torch.Generator(device=self.device)
-        self.gen.manual_seed(seed)
-        self.governor = governor
-        self.verify = DeviceVerifier(self.device) if verify is None else verify
+        super().__init__(draft_step, k, greedy, seed, governor, device, verify)
+        self.target_step = target_step
         self.trace: List[Tuple[int, List[Tuple[int, int, int]]]] = []
 
     def _modes(self, B: int) -> List[int]:
@@ -358,7 +350,7 @@ class BatchedSpeculativeDecoder:
         live = list(range(B))
         self.trace = []
         while live:
-            k = self.k if self.governor is None or self.governor.speculating else 0
+            k = self._k()
             L = len(live)
             pre = [list(prefixes[b]) for b in live]
             if k > 0:
