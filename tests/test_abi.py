@@ -177,3 +177,21 @@ def test_trace_summary_of_known_records():
     assert s["decide_us"] == {"median": 2.0, "max": 3.0}
     assert s["items_per_cta"] == {"median": 1.0, "max": 1.0}
     assert sv.trace_summary(np.zeros((0, 2), np.uint64)) == {}
+
+
+def test_binding_constants_match_the_header():
+    """Every #define of specverify.h that the binding mirrors has the same value."""
+    defs = {}
+    for name, expr in re.findall(r"#define\s+(SV_[A-Z0-9_]+)\s+(.+)", open(HEADER).read()):
+        defs[name] = eval(re.sub(r"(\d+)u\b", r"\1", expr.split("/*")[0]), {})
+    mirror = {
+        "SV_OK": sv.SV_OK, "SV_EINVAL": sv.SV_EINVAL, "SV_EWORKSPACE": sv.SV_EWORKSPACE,
+        "SV_ECUDA": sv.SV_ECUDA, "SV_ETOOLARGE": sv.SV_ETOOLARGE,
+        "SV_NOALLOC_SCRATCH_BYTES": sv.NOALLOC_SCRATCH_BYTES, "SV_MAX_K": sv.MAX_K,
+        "SV_STATUS_BAD_TOKEN": sv.STATUS_BAD_TOKEN, "SV_STATUS_ZERO_MASS": sv.STATUS_ZERO_MASS,
+        "SV_STATUS_OVERFLOW": sv.STATUS_OVERFLOW, "SV_STATUS_BAD_MODE": sv.STATUS_BAD_MODE,
+        "SV_STATUS_TIMEOUT": sv.STATUS_TIMEOUT, "SV_STATUS_BAD_VALUE": sv.STATUS_BAD_VALUE,
+        "SV_TRACE_RECORDS": sv.TRACE_RECORDS,
+    }
+    for name, value in mirror.items():
+        assert defs[name] == value, name
