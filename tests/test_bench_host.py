@@ -65,3 +65,37 @@ def test_trace_flag_parses():
     a = bench.parse_args(["--trace", "--mode", "greedy"])
     assert a.trace and a.mode == "greedy"
     assert not bench.parse_args([]).trace
+
+
+def _oracle_outputs(bt, mode):
+    import torch
+    import oracle
+    p, q, t, ua, ur, md = bt.numpy()
+    if mode == "greedy":
+        n, x, _ = oracle.verify_greedy(p, t)
+    elif mode == "sample":
+        n, x, _ = oracle.verify_sample(p, q, t, ua, ur)
+    else:
+        n, x, _ = oracle.verify_round(md, p, q, t, ua, ur)
+    return torch.from_numpy(np.array(n, dtype=np.int32)), torch.from_numpy(np.array(x, dtype=np.int32))
+
+
+@pytest.mark.parametrize("mode,cfg", [("sample", 3), ("greedy", 2), ("round", 4)])
+def test_bench_parity_leg_counts_and_takes_bytes_from_the_oracle(mode, cfg):
+    """The CPU-baseline leg's parity check: outputs equal to the oracle's give
+    no mismatch and the oracle's required bytes; one planted wrong token is a
+    decision mismatch, not a boundary case."""
+    from speculative_decoding_verification_08_gb300.inputs import make_inputs
+    sets = [make_inputs(cfg, "cpu", seed=77 + i, B=12, V=700, K=4) for i in range(2)]
+    outs = [_oracle_outputs(bt, mode) for bt in sets]
+    par, req = bench.oracle_parity(sets, outs, [], mode, 4, 700)
+    assert par["sets"] == 2 and par["sequences"] == 24
+    assert par["decision_mismatches"] == 0 and par["boundary_mismatches"] == 0
+    for bt, (n, _), r in zip(sets, outs, req):
+        md = (np.zeros(12) if mode == "greedy" else np.ones(12) if mode == "sample"
+              else bt.mode.numpy())
+        assert r == bench.required_bytes(md, n.numpy(), 4, 700)
+    n, x = outs[1]
+    x[3] = (x[3] + 1) % 700 if x[3] >= 0 else 5   # a token the oracle did not draw
+    par, _ = bench.oracle_parity(sets, outs, [], mode, 4, 700)
+    assert par["decision_mismatches"] == 1

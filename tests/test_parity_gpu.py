@@ -14,9 +14,6 @@ from oracle.compare import compare
 
 pytestmark = pytest.mark.gpu
 
-BOUNDARY_REPORT = []
-
-
 @pytest.fixture(scope="module", autouse=True)
 def built():
     if not torch.cuda.is_available():
@@ -24,8 +21,6 @@ def built():
     sv.build()
     sv.load()
     yield
-    if BOUNDARY_REPORT:
-        print("\nboundary-explained resample mismatches:", BOUNDARY_REPORT)
 
 
 def _free():
@@ -68,9 +63,8 @@ def check_sample(bt, host=None, label=""):
     p, q, t, ua, ur, md = host if host is not None else bt.numpy()
     n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
     n1, x1, s1 = gpu_sample(bt)
-    bnd = compare(p, q, ur, 1, bt.K, n0, x0, n1, x1, s0, s1)
-    if bnd:
-        BOUNDARY_REPORT.append((label or bt.meta.get("name"), bnd))
+    compare(p, q, ur, 1, bt.K, n0, x0, n1, x1, s0, s1,
+            label=label or bt.meta.get("name"))
     return n0
 
 
@@ -223,7 +217,7 @@ def test_commit_matches_oracle():
     tok = torch.from_numpy(tokens0).cuda()
     lens = torch.from_numpy(lengths0).cuda()
     n1, x1, s1 = gpu_round(bt, tokens=tok, lengths=lens)
-    bnd = compare(p, q, ur, md, K, n0, x0, n1, x1)
+    bnd = compare(p, q, ur, md, K, n0, x0, n1, x1, label="commit")
     assert s1 == (s0 | sc)
     if not bnd:
         assert np.array_equal(tok.cpu().numpy(), tok_ref)
@@ -283,8 +277,8 @@ def test_boundary_thresholds_are_counted_not_wrong():
     u = torch.from_numpy(ur).cuda()
     n1, x1 = sv.verify_sample(p, q, t, ua, u)
     n0, x0, s0 = oracle.verify_sample(ph, qh, t.cpu().numpy(), ua.cpu().numpy(), ur)
-    bnd = compare(ph, qh, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy())
-    BOUNDARY_REPORT.append(("boundary stress", len(bnd)))
+    compare(ph, qh, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(),
+            label="uniforms on oracle CDF boundaries")
 
 
 # ---------------------------------------------------------------------------
@@ -338,10 +332,8 @@ def test_sampling_full_fresh_and_reused_workspace():
             reused = sv.Workspace(bt.B, bt.K, bt.V)
         for ws in (fresh, reused):
             n1, x1 = sv.verify_sample(bt.p, bt.q, bt.t, bt.u_acc, bt.u_res, ws=ws)
-            bnd = compare(p, q, ur, 1, bt.K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(),
-                          s0, ws.status())
-            if bnd:
-                BOUNDARY_REPORT.append((f"sampling seed {seed}", bnd))
+            compare(p, q, ur, 1, bt.K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(), s0,
+                    ws.status(), label=f"sampling seed {seed}")
         del bt, fresh
         _free()
 
@@ -365,10 +357,8 @@ def test_workspace_reused_across_sizes():
         else:
             n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
             n1, x1 = sv.verify_sample(bt.p, bt.q, bt.t, bt.u_acc, bt.u_res, ws=ws)
-            bnd = compare(p, q, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(), s0,
-                          ws.status())
-            if bnd:
-                BOUNDARY_REPORT.append((f"reused workspace {B}x{V}", bnd))
+            compare(p, q, ur, 1, K, n0, x0, n1.cpu().numpy(), x1.cpu().numpy(), s0,
+                    ws.status(), label=f"reused workspace {B}x{V}")
 
 
 def test_implicit_workspaces_are_per_stream():
@@ -396,10 +386,8 @@ def test_host_resident_inputs(mapped):
     hv = sv.HostVerifier(B, K, V, sampling=True, mapped=mapped)
     n1, x1 = hv.sample(hp, hq, ht, hua, hur)
     n0, x0, s0 = oracle.verify_sample(p, q, t, ua, ur, nthreads=8)
-    bnd = compare(p, q, ur, 1, K, n0, x0, n1.numpy().copy(), x1.numpy().copy(), s0,
-                  hv.ws.status())
-    if bnd:
-        BOUNDARY_REPORT.append((f"host inputs mapped={mapped}", bnd))
+    compare(p, q, ur, 1, K, n0, x0, n1.numpy().copy(), x1.numpy().copy(), s0,
+            hv.ws.status(), label=f"host inputs mapped={mapped}")
     assert hv.h2d_bytes() > 0
     hg = sv.HostVerifier(B, K, V, sampling=False, mapped=mapped)
     n1, x1 = hg.greedy(hp, ht)
@@ -431,9 +419,8 @@ def test_mixed_round_full():
     p, q, t, ua, ur, md = bt.numpy()
     n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur, nthreads=16)
     n1, x1, s1 = gpu_round(bt)
-    bnd = compare(p, q, ur, md, bt.K, n0, x0, n1, x1, s0, s1)
-    if bnd:
-        BOUNDARY_REPORT.append(("mixed B=1024", bnd))
+    compare(p, q, ur, md, bt.K, n0, x0, n1, x1, s0, s1,
+            label="mixed B=1024")
     counts = np.bincount(n0, minlength=bt.K + 1)
     assert counts[0] > 0 and counts[bt.K] > 0
     del bt
@@ -455,9 +442,8 @@ def test_item_path_rows_in_several_items(V):
     md = (np.arange(B) % 2).astype(np.uint8)
     n0, x0, s0 = oracle.verify_round(md, p, q, t, ua, ur, nthreads=8)
     n1, x1, s1 = gpu_round(bt, mode=torch.from_numpy(md).cuda())
-    bnd = compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1)
-    if bnd:
-        BOUNDARY_REPORT.append((f"rows in several items V={V}", bnd))
+    compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1,
+            label=f"rows in several items V={V}")
     del bt
     _free()
 
@@ -505,9 +491,8 @@ def test_mixed_round_item_path_mode_patterns(B, V, pattern):
         lens.copy_(torch.from_numpy(lengths0))
         n1, x1, s1 = gpu_round(bt, mode=mode, tokens=tok, lengths=lens)
         assert sv.last_kernel_count() == 2, "expected the ordering kernel and the item kernel"
-        bnd = compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1)
-        if bnd:
-            BOUNDARY_REPORT.append((f"mixed {pattern} B={B}", bnd))
+        compare(p, q, ur, md, K, n0, x0, n1, x1, s0, s1,
+                label=f"mixed {pattern} B={B}")
         same = x1 == x0  # a boundary-explained draw commits the GPU's own token
         np.testing.assert_array_equal(lens.cpu().numpy(), len_ref)
         np.testing.assert_array_equal(tok.cpu().numpy()[same], tok_ref[same])
