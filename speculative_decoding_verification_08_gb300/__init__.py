@@ -498,7 +498,7 @@ class HostVerifier:
 # ---------------------------------------------------------------------------
 # timeline of the item kernel (a library built with SV_TRACE=1)
 
-TRACE_RECORDS = 512 * 1024
+TRACE_RECORDS = 2048 * 1024
 
 
 def trace_reset(stream=None, lib=None):
@@ -522,3 +522,9 @@ def trace_read(stream=None, lib=None):
 def trace_summary(records) -> dict:
     """Where one traced launch's time went (``trace.summary``)."""
     return _trace.summary(records)
+
+
+def trace_timeline(records) -> dict:
+    """Per-launch summaries of several consecutive traced launches and the
+    time between them (``trace.timeline``)."""
+    return _trace.timeline(records)

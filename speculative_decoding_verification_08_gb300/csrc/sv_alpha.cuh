@@ -5,16 +5,28 @@
 // expected accepted length E[b] = sum_{m=1..K} prod_{j<m} alpha[b][j] -- the
 // quantities of the rejection-sampling theorem behind the "spec-verify"
 // page's analytic accepted-length law (section "Measured").  Diagnostic only:
-// it reads every p_i and q_i row in full, twice.
+// it reads every p_i and q_i row in full.
 //
-// Three launches on one stream, the later two programmatic dependents:
-//  1. one CTA per (b, i) row pair sums P_i and Q_i in double-fp32 (the exact
-//     four-element sums of quad_mass, combined with Dekker additions);
-//  2. one CTA per row pair sums min(p * (1/P), q * (1/Q)) the same way, with
-//     the reciprocals rounded once to fp32 -- each term carries at most two
-//     fp32 roundings, so |alpha - exact| <= 2 * 2^-24 * alpha ~ 1.2e-7;
-//  3. one thread per sequence forms E[b] in fp64.
+// alpha needs the totals before the minima, so each row pair is read twice;
+// only the first read comes from DRAM.  One thread-block cluster of
+// kAlphaCluster CTAs takes a (b, i) row pair, CTA r an r-th of its segments:
+//  1. each CTA sums its slice of P_i and Q_i in double-fp32 (the exact
+//     four-element sums of quad_mass, combined with Dekker additions) and
+//     writes the pair of partials into every CTA of the cluster (distributed
+//     shared memory); after a cluster barrier every CTA adds the partials in
+//     rank order, so all hold the same P_i, Q_i;
+//  2. each CTA sums min(p * (1/P), q * (1/Q)) over its slice again -- the
+//     slice it read moments before, now an L2 hit -- with the reciprocals
+//     rounded once to fp32: each term carries at most two fp32 roundings, so
+//     |alpha - exact| <= 2 * 2^-24 * alpha ~ 1.2e-7; the partials go to the
+//     cluster's first CTA, which adds them in rank order;
+//  3. a dependent launch, one thread per sequence, forms E[b] in fp64.
+// The launch holds kAlphaCtasPerSm CTAs per SM (set by its shared memory),
+// so that the row pairs being read at once stay well inside L2 until their
+// second read.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "sv_device.cuh"
 
@@ -31,7 +43,6 @@ struct AlphaParams {
     int32_t B, K;
     int64_t V;
     int32_t nseg;
-    float2 *norm;       // workspace [B][K][2]: P_i, Q_i as double-fp32
     double *alpha;      // [B][K]
     double *expected;   // [B] or null
 };
@@ -51,19 +62,21 @@ __device__ __forceinline__ dd cta_sum_dd(dd v, dd *sh, int warp, int lane) {
     return t;
 }
 
-// Per-lane sums over one row pair: f(pv, qv) gives the four terms of a float4
-// pair; aligned full segments take 16-byte loads, the rest scalar loads.
+// Per-lane sums over segments [s0, s1) of a row pair: f(pv, qv) takes the
+// four terms of a float4 pair; aligned full segments take 16-byte loads, the
+// rest scalar loads.
 template <class F>
-__device__ __forceinline__ void row_pair_sums(const float *pr, const float *qr, int64_t V, int nseg,
-                                              bool vec, int warp, int lane, F f, dd &s0, dd &s1) {
-    for (int s = warp; s < nseg; s += kAlphaWarps) {
+__device__ __forceinline__ void slice_pair_sums(const float *pr, const float *qr, int64_t V, int s0,
+                                                int s1, bool vec, int warp, int lane, F f, dd &x0,
+                                                dd &x1) {
+    for (int s = s0 + warp; s < s1; s += kAlphaWarps) {
         const int64_t base = (int64_t)s * kSeg;
         const int64_t n = V - base < kSeg ? V - base : kSeg;
         if (vec && n == kSeg) {
 #pragma unroll 4
             for (int k = 0; k < kVecPerLane; ++k) {
                 const int64_t e = base + 4 * (lane + 32 * k);
-                f(ld_stream4(pr + e), ld_stream4(qr + e), s0, s1);
+                f(ld_stream4(pr + e), ld_stream4(qr + e), x0, x1);
             }
         } else {
             for (int64_t e = base + 4 * lane; e < base + n; e += 128) {
@@ -73,7 +86,7 @@ __device__ __forceinline__ void row_pair_sums(const float *pr, const float *qr, 
                 if (e + 1 < base + n) { a.y = ld_stream1(pr + e + 1); c.y = ld_stream1(qr + e + 1); }
                 if (e + 2 < base + n) { a.z = ld_stream1(pr + e + 2); c.z = ld_stream1(qr + e + 2); }
                 if (e + 3 < base + n) { a.w = ld_stream1(pr + e + 3); c.w = ld_stream1(qr + e + 3); }
-                f(a, c, s0, s1);
+                f(a, c, x0, x1);
             }
         }
     }
@@ -83,59 +96,94 @@ __device__ __forceinline__ bool alpha_vec(const AlphaParams &A) {
     return aligned16(A.p) && aligned16(A.q) && (A.ps & 3) == 0 && (A.qs & 3) == 0;
 }
 
-__global__ void __launch_bounds__(kAlphaThreads) alpha_norm_kernel(const AlphaParams A) {
-    __shared__ dd sh[2][kAlphaWarps];
-    grid_dependents_may_launch();
-    const int b = blockIdx.x / A.K, i = blockIdx.x - b * A.K;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float *pr = A.p + ((int64_t)b * (A.K + 1) + i) * A.ps;
-    const float *qr = A.q + ((int64_t)b * A.K + i) * A.qs;
-    dd sp = {0.f, 0.f}, sq = {0.f, 0.f};
-    row_pair_sums(pr, qr, A.V, A.nseg, alpha_vec(A), warp, lane,
-                  [](float4 a, float4 c, dd &s0, dd &s1) {
-                      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                      s0 = dd_add(s0, quad_mass<false>(a, z));
-                      s1 = dd_add(s1, quad_mass<false>(c, z));
-                  },
-                  sp, sq);
-    sp = warp_sum_dd(sp);
-    sq = warp_sum_dd(sq);
-    const dd P = cta_sum_dd(sp, sh[0], warp, lane);
-    const dd Q = cta_sum_dd(sq, sh[1], warp, lane);
-    if (threadIdx.x == 0) {
-        float2 *o = A.norm + ((int64_t)b * A.K + i) * 2;
-        o[0] = make_float2(P.hi, P.lo);
-        o[1] = make_float2(Q.hi, Q.lo);
-    }
+constexpr int kAlphaCluster = 8;
+// Resident CTAs per SM, set through the launch's dynamic shared memory: at 4,
+// 76 row pairs (78 MB at V = 128256) are being read at once, well inside the
+// 136 MB L2, and the second sweeps re-read 6 % from DRAM (at 6 per SM, 32 %,
+// for a call 2 % faster; at 2 or 3 per SM the calls were 30 % and 5 % slower).
+constexpr int kAlphaCtasPerSm = 4;
+constexpr int kAlphaSmemBytes = 200 * 1024 / kAlphaCtasPerSm;
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kAlphaThreads) alpha_min_kernel(const AlphaParams A) {
-    __shared__ dd sh[kAlphaWarps];
+// One cluster per (b, i) row pair (blockIdx.x / kAlphaCluster); see the top
+// of this file.
+__global__ void __cluster_dims__(kAlphaCluster, 1, 1) __launch_bounds__(kAlphaThreads)
+    alpha_pair_kernel(const AlphaParams A) {
+    namespace cg = cooperative_groups;
+    __shared__ dd sh[2][kAlphaWarps];
+    __shared__ dd pq[kAlphaCluster][2];   // every CTA's (P, Q) partials, written by their CTAs
+    __shared__ dd am[kAlphaCluster];      // the alpha partials (first CTA only)
+    __shared__ float recip[2];
+    // the cluster's CTAs have all started before any writes into another's
+    // shared memory (the wait is below, after this CTA's own first pass)
+    cluster_arrive_relaxed();
     grid_dependents_may_launch();
-    wait_for_primary_grid();  // the totals
-    const int b = blockIdx.x / A.K, i = blockIdx.x - b * A.K;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int64_t pair = (int64_t)(blockIdx.x / kAlphaCluster);
+    const int b = (int)(pair / A.K), i = (int)(pair - (int64_t)b * A.K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float2 *o = A.norm + ((int64_t)b * A.K + i) * 2;
-    const float2 P2 = ld_l2(o), Q2 = ld_l2(o + 1);
-    const double P = (double)P2.x + (double)P2.y, Q = (double)Q2.x + (double)Q2.y;
-    if (!(P > 0.0) || !(Q > 0.0)) {  // a row with no mass: no acceptance
-        if (threadIdx.x == 0) A.alpha[(int64_t)b * A.K + i] = 0.0;
-        return;
-    }
-    const float ip = (float)(1.0 / P), iq = (float)(1.0 / Q);
+    const int per = (A.nseg + kAlphaCluster - 1) / kAlphaCluster;
+    const int s0 = min(A.nseg, rank * per), s1 = min(A.nseg, s0 + per);
     const float *pr = A.p + ((int64_t)b * (A.K + 1) + i) * A.ps;
     const float *qr = A.q + ((int64_t)b * A.K + i) * A.qs;
-    dd s = {0.f, 0.f}, unused = {0.f, 0.f};
-    row_pair_sums(pr, qr, A.V, A.nseg, alpha_vec(A), warp, lane,
-                  [ip, iq](float4 a, float4 c, dd &s0, dd &) {
-                      const float4 m = make_float4(fminf(a.x * ip, c.x * iq), fminf(a.y * ip, c.y * iq),
-                                                   fminf(a.z * ip, c.z * iq), fminf(a.w * ip, c.w * iq));
-                      s0 = dd_add(s0, quad_mass<false>(m, make_float4(0.f, 0.f, 0.f, 0.f)));
-                  },
-                  s, unused);
-    s = warp_sum_dd(s);
-    const dd t = cta_sum_dd(s, sh, warp, lane);
-    if (threadIdx.x == 0) A.alpha[(int64_t)b * A.K + i] = (double)t.hi + (double)t.lo;
+    const bool vec = alpha_vec(A);
+    dd sp = {0.f, 0.f}, sq = {0.f, 0.f};
+    slice_pair_sums(pr, qr, A.V, s0, s1, vec, warp, lane,
+                    [](float4 a, float4 c, dd &x0, dd &x1) {
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                        x0 = dd_add(x0, quad_mass<false>(a, z));
+                        x1 = dd_add(x1, quad_mass<false>(c, z));
+                    },
+                    sp, sq);
+    sp = warp_sum_dd(sp);
+    sq = warp_sum_dd(sq);
+    const dd P_part = cta_sum_dd(sp, sh[0], warp, lane);
+    const dd Q_part = cta_sum_dd(sq, sh[1], warp, lane);
+    cluster_wait();
+    if (threadIdx.x < kAlphaCluster) {  // warp 0's lanes hold the totals: into CTA threadIdx.x
+        dd *dst = cluster.map_shared_rank(&pq[0][0], (int)threadIdx.x);
+        dst[2 * rank] = P_part;
+        dst[2 * rank + 1] = Q_part;
+    }
+    cluster.sync();
+    if (threadIdx.x == 0) {
+        dd P = pq[0][0], Q = pq[0][1];
+        for (int r = 1; r < kAlphaCluster; ++r) {
+            P = dd_add(P, pq[r][0]);
+            Q = dd_add(Q, pq[r][1]);
+        }
+        const double Pd = (double)P.hi + (double)P.lo, Qd = (double)Q.hi + (double)Q.lo;
+        // a row with no mass: no acceptance (0 marks it)
+        recip[0] = Pd > 0.0 && Qd > 0.0 ? (float)(1.0 / Pd) : 0.f;
+        recip[1] = Pd > 0.0 && Qd > 0.0 ? (float)(1.0 / Qd) : 0.f;
+    }
+    __syncthreads();
+    const float ip = recip[0], iq = recip[1];
+    dd m = {0.f, 0.f}, unused = {0.f, 0.f};
+    if (ip != 0.f)
+        slice_pair_sums(pr, qr, A.V, s0, s1, vec, warp, lane,
+                        [ip, iq](float4 a, float4 c, dd &x0, dd &) {
+                            const float4 v = make_float4(fminf(a.x * ip, c.x * iq), fminf(a.y * ip, c.y * iq),
+                                                         fminf(a.z * ip, c.z * iq), fminf(a.w * ip, c.w * iq));
+                            x0 = dd_add(x0, quad_mass<false>(v, make_float4(0.f, 0.f, 0.f, 0.f)));
+                        },
+                        m, unused);
+    m = warp_sum_dd(m);
+    const dd M_part = cta_sum_dd(m, sh[0], warp, lane);
+    if (threadIdx.x == 0) cluster.map_shared_rank(&am[0], 0)[rank] = M_part;
+    cluster.sync();  // after this no CTA touches another's shared memory
+    if (rank == 0 && threadIdx.x == 0) {
+        dd t = am[0];
+        for (int r = 1; r < kAlphaCluster; ++r) t = dd_add(t, am[r]);
+        A.alpha[pair] = ip != 0.f ? (double)t.hi + (double)t.lo : 0.0;
+    }
 }
 
 __global__ void alpha_length_kernel(const AlphaParams A) {

@@ -42,9 +42,6 @@ namespace sv {
 
 // Items a CTA holds at once: the one streaming, ones whose stages are still in
 // the ring, and ones waiting for the retire warp.
-#ifndef SV_ROTATE_SAMPLE
-#define SV_ROTATE_SAMPLE 0
-#endif
 #ifndef SV_ITEM_SLOTS
 #define SV_ITEM_SLOTS 4
 #endif
@@ -54,20 +51,10 @@ constexpr int kItemThreads = (kTmaConsumers + 2 + kItemDecideWarps) * 32;
 // Warp w issues on scheduler w % 4.  The producer's issue rate bounds the
 // stream, so it shares its scheduler only with the two decide warps (mostly
 // idle); the eight consumers and the retire warp fill the other three.
-#ifndef SV_ROLE_MAP
-#define SV_ROLE_MAP 1
-#endif
-#if SV_ROLE_MAP
 constexpr int kItemProducerWarp = 0;
 constexpr int kItemDecideWarpA = 4;
 constexpr int kItemDecideWarpB = 8;
 constexpr int kItemRetireWarp = 11;
-#else
-constexpr int kItemProducerWarp = 8;
-constexpr int kItemDecideWarpA = 10;
-constexpr int kItemDecideWarpB = 11;
-constexpr int kItemRetireWarp = 9;
-#endif
 static_assert(kItemThreads == 12 * 32, "role map assumes twelve warps");
 constexpr int kDecideQueue = 16;  // sequences a CTA has completed but not yet decided
 // Poll intervals of the retire and decide warps: they wait on shared state,
@@ -249,10 +236,10 @@ struct ItemProducer {
         return got;
     }
 
-    // The item's sequence, segment range and per-position data (loads issued,
-    // not waited for).
+    // The item's sequence and segment range (no load but a mixed round's
+    // order entry).
     template <int kRule>
-    __device__ ItemPre begin(int item) {
+    __device__ ItemPre locate(int item) {
         ItemPre x = {};
         x.b = P.B;
         if (item >= P.B * P.ichunks) return x;
@@ -282,14 +269,28 @@ struct ItemProducer {
             x.rule = kRule;
         }
         x.b = b;
-        const int64_t tb = (int64_t)b * P.K;
+        return x;
+    }
+
+    // Loads of the item's per-position data (issued, not waited for).
+    template <int kRule>
+    __device__ void load_draft(ItemPre &x) {
+        if (x.b >= P.B) return;
+        const int64_t tb = (int64_t)x.b * P.K;
         if (lane < P.K) x.t0 = ld_early(P.t + tb + lane);
         if (lane + 32 < P.K) x.t1 = ld_early(P.t + tb + lane + 32);
         if (kRule != kGreedy && P.u_acc) {  // (loaded for every rule in a mixed round)
             if (lane < P.K) x.u0 = ld_early(P.u_acc + tb + lane);
             if (lane + 32 < P.K) x.u1 = ld_early(P.u_acc + tb + lane + 32);
         }
-        if (kRule != kGreedy && lane == 0) x.ur = ld_early(P.u_res + b);
+        if (kRule != kGreedy && lane == 0) x.ur = ld_early(P.u_res + x.b);
+    }
+
+    // locate() and load_draft().
+    template <int kRule>
+    __device__ ItemPre begin(int item) {
+        ItemPre x = locate<kRule>(item);
+        load_draft<kRule>(x);
         return x;
     }
 
@@ -323,26 +324,16 @@ struct ItemProducer {
 
     __device__ int copy_len(int s) const { return seg_len(P.V, s) & ~3; }
 
-    // With SV_ROTATE_SAMPLE, where a sampling item of sequence b starts
-    // streaming row `row` of its `len` segments: position j of the stream is
-    // segment s0 + (j + r) % len.  Sums are kept by segment index, so no
-    // result changes; the rows' concurrent streams are spread over different
-    // offsets.  r is even, and 0 for an odd len, so a two-segment stage never
-    // wraps.  (One A/B: 48.90 -> 48.34 us at B = 256, V = 128256, K = 5;
-    // greedy rows measured slower with it, so they are not rotated.)
-    __device__ static int rot_offset(int b, int row, int len) {
-#if SV_ROTATE_SAMPLE
-        if ((len & 1) || len < 4) return 0;
-        return 2 * (int)(((unsigned)b * 13u + (unsigned)row * 5u) % (unsigned)(len / 2));
-#else
-        (void)b, (void)row, (void)len;
-        return 0;
-#endif
+    // Stages of a sampling item: its residual row pair (p_n, q_n), one
+    // segment of each row per stage, or the bonus row p_K, two segments per
+    // stage.
+    __device__ int sample_stages(const ItemPre &c, int n) const {
+        const int len = c.s1 - c.s0;
+        return n < P.K ? len : (len + 1) / 2;
     }
 
-    // Residual row pair (p_n, q_n) segment by segment, or the bonus row p_K
-    // two segments per stage.  The stage loop runs on lane 0 alone.
-    __device__ int stream_sample(const ItemPre &c, int n, int x) {
+    // Stages [j0, j1) of a sampling item; the stage loop runs on lane 0 alone.
+    __device__ int stream_sample(const ItemPre &c, int n, int x, int j0, int j1) {
         int stages = 0;
         if (lane == 0 && ok) {
             ItemMeta m = {};
@@ -352,12 +343,7 @@ struct ItemProducer {
                 const float *pr = prow(P, c.b, n), *qr = qrow(P, c.b, n);
                 m.kind = kPair;
                 m.nparts = 2;
-#if SV_ROTATE_SAMPLE
-                int s = c.s0 + rot_offset(c.b, n, c.s1 - c.s0);
-                for (int j = c.s0; j < c.s1; ++j) {
-#else
-                for (int s = c.s0; s < c.s1; ++s) {
-#endif
+                for (int s = c.s0 + j0; s < c.s0 + j1; ++s) {
                     m.s = s;
                     const int cc = copy_len(s);
                     if (!put(m, pr + (int64_t)s * kSeg, cc, qr + (int64_t)s * kSeg, cc)) {
@@ -365,24 +351,13 @@ struct ItemProducer {
                         break;
                     }
                     ++stages;
-#if SV_ROTATE_SAMPLE
-                    if (++s == c.s1) s = c.s0;
-#endif
                 }
             } else {
                 const float *pr = prow(P, c.b, P.K);
                 m.kind = kMass;
-#if SV_ROTATE_SAMPLE
-                const int len = c.s1 - c.s0, r = rot_offset(c.b, P.K, len);
-                for (int j = 0; j < len; j += 2) {
-                    const int s = c.s0 + (j + r) % len;
-                    m.s = s;
-                    m.nparts = j + 1 < len ? 2 : 1;
-#else
-                for (int s = c.s0; s < c.s1; s += 2) {
+                for (int s = c.s0 + 2 * j0; s < min(c.s1, c.s0 + 2 * j1); s += 2) {
                     m.s = s;
                     m.nparts = s + 1 < c.s1 ? 2 : 1;
-#endif
                     const int c1 = m.nparts == 2 ? copy_len(s + 1) : 0;
                     if (!put(m, pr + (int64_t)s * kSeg, copy_len(s), pr + (int64_t)(s + 1) * kSeg, c1)) {
                         ok = false;
@@ -451,14 +426,16 @@ struct ItemProducer {
         return __shfl_sync(0xffffffffu, stages, 0);
     }
 
-    // A greedy item begun but not gathered.  Row 0 is read whatever the
-    // draft, so its first `early` stages go out before the gather waits for
-    // the draft ids; the row's token key goes into the slot as soon as
-    // p_0(t_0) is in, before the rest of the row; rows 1..K then as above.
-    // ns becomes kNBad when a draft id is invalid (nothing past the early
-    // stages is read).
-    __device__ int stream_greedy_lazy(ItemPre &c, int x, int early, int &ns) {
+    // A greedy item whose draft ids are on their way.  Row 0 is read whatever
+    // the draft, so its first `early` stages go out before the gather waits
+    // for the ids, and `late` more while p_0(t_0) is on its way; the row's
+    // token key then goes into the slot, before the rest of the row (which
+    // is tested as it arrives, so a miss shows up before row 1 and no row-1
+    // stage is issued for nothing); rows 1..K as above.  ns becomes kNBad
+    // when a draft id is invalid (nothing past the early stages is read).
+    __device__ int stream_greedy_lazy(ItemPre &c, int x, int early, int late, int &ns) {
         const int split = min(c.s1, c.s0 + 2 * early);
+        const int split2 = min(c.s1, split + 2 * late);
         const int tok0 = P.K > 0 ? kTokInSlot : -1;
         int stages = 0, seen = 0;
         bool stop = !ok;
@@ -473,11 +450,9 @@ struct ItemProducer {
             return __shfl_sync(0xffffffffu, stages, 0);
         }
         if (lane == 0 && ok) {
-            // the token's key first: the rest of row 0 is then tested as it
-            // arrives, a miss shows up before row 1, and no row-1 stage is
-            // issued for nothing
+            stages += put_greedy_row(c.b, x, 0, tok0, 0.f, split, split2, 0, stop);
             if (P.K > 0) *(volatile unsigned long long *)&sh.slot[x].tkey0 = pack_key(c.pt0, c.t0);
-            stages += put_greedy_row(c.b, x, 0, tok0, 0.f, split, c.s1, 0, stop);
+            if (!stop) stages += put_greedy_row(c.b, x, 0, tok0, 0.f, split2, c.s1, 0, stop);
             if (*(volatile int *)&sh.slot[x].miss >= kFlagBase) stop = true;
         }
         sync_ok();
@@ -540,18 +515,26 @@ __device__ void item_produce_end(const Params &P, ItemShared &sh, ItemProducer &
 }
 
 // The greedy producer.  A CTA holds one item at a time and claims the next
-// once the current one's copies are out (CTA c starts with item c).  A greedy
-// item needs no draft data before its first copies, so there is nothing to
-// fetch ahead, and the last items go to the CTAs that finish first.
-#ifndef SV_GREEDY_EARLY
-#define SV_GREEDY_EARLY 2
-#endif
-__device__ void item_produce_greedy(const Params &P, ItemShared &sh, unsigned char *buf, int lane) {
+// once the current one's copies are out (CTA c starts with item c; claimed
+// earlier, the items measured slower, and later claims near the end of the
+// queue gained nothing).  A greedy item needs no draft data before its first
+// copies, so there is nothing to fetch ahead, and the last items go to the
+// CTAs that finish first.  Per item: the slot is published first, then the
+// draft ids are loaded while kGreedyEarly row-0 stages go out, then
+// kGreedyLate more while p_0(t_0) is loaded (so the producer does not wait
+// for either load), then the token's key and the rest.  The first item's slot
+// is set up before the wait for the previous grid (`prewait`): nothing in
+// global memory is touched until that wait.
+constexpr int kGreedyEarly = 2;
+constexpr int kGreedyLate = 2;
+
+__device__ void item_produce_greedy(const Params &P, ItemShared &sh, unsigned char *buf, int lane,
+                                    bool prewait) {
     ItemProducer pr(P, sh, buf, lane);
     IdleClock clk;
     int item = (int)blockIdx.x;
     while (pr.ok) {
-        ItemPre c = pr.begin<kGreedy>(item);
+        ItemPre c = pr.locate<kGreedy>(item);
         if (c.b >= P.B) break;
         const int x = __shfl_sync(0xffffffffu, pr.free_slot(clk), 0);
         pr.sync_ok();
@@ -573,20 +556,28 @@ __device__ void item_produce_greedy(const Params &P, ItemShared &sh, unsigned ch
             *(volatile int *)&sl.state = 1;
         }
         __syncwarp();
+        if (prewait) {
+            wait_for_primary_grid();
+            SV_TRACE_START_WARP();
+            prewait = false;
+        }
+        pr.load_draft<kGreedy>(c);
         int ns = 1;
-        const int stages = pr.stream_greedy_lazy(c, x, SV_GREEDY_EARLY, ns);
+        const int stages = pr.stream_greedy_lazy(c, x, kGreedyEarly, kGreedyLate, ns);
         if (lane == 0) {
             SV_TRACE_EVENT(kTrItemIssued, stages);
             sl.ns = ns;
             sl.issued = stages;
             __threadfence_block();
             *(volatile int *)&sl.state = 2;
-            // claimed once this item's copies are out, while the ring still
-            // holds them (claimed earlier, the item measured slower)
             claim = atomicAdd(P.queue, 1u);
         }
         __syncwarp();
         item = (int)gridDim.x + (int)__shfl_sync(0xffffffffu, claim, 0);
+    }
+    if (prewait) {  // no item at all (or a wait gave up before the first)
+        wait_for_primary_grid();
+        SV_TRACE_START_WARP();
     }
     item_produce_end(P, sh, pr, lane);
 }
@@ -652,7 +643,7 @@ __device__ void item_produce(const Params &P, ItemShared &sh, unsigned char *buf
         nxt2 = pr.begin<kRule>(pr.take());
         int stages = 0;
         if (ns != 0 && ns != kNBad) {
-            if (c.rule == kSample) stages = pr.stream_sample(c, ns - 1, x);
+            if (c.rule == kSample) stages = pr.stream_sample(c, ns - 1, x, 0, pr.sample_stages(c, ns - 1));
             else stages = pr.stream_greedy(c, x);
         }
         if (lane == 0) {
@@ -864,12 +855,19 @@ __device__ bool item_retire(const Params &P, int b, int rule, int ns, int miss,
     __syncwarp();
     int last = 0;
     if (lane == 0) {
-        __threadfence();  // this item's results before its count
-        last = atomicAdd(P.done + b, 1) == P.ichunks - 1;
+        // one acquire-release count: this item's results (the warp's, after
+        // __syncwarp) before it, and for the last item every other item's
+        // results after it
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(P.done + b) : "memory");
+        last = old == P.ichunks - 1;
     }
-    return __shfl_sync(0xffffffffu, last, 0) != 0;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    __syncwarp();  // lane 0's acquire, before every lane's reads of the other items' results
+    return last != 0;
 }
 
+template <int kRule>
 __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
     IdleClock clk;
     bool ok = true;
@@ -893,6 +891,15 @@ __device__ void item_retire_loop(const Params &P, ItemShared &sh, int lane) {
             if (lane == 0) SV_TRACE_EVENT(kTrItemRetired, b);
             // a whole-row item with its sums in shared memory is its sequence
             if (sb < 0 && !item_retire(P, b, rule, ns, miss, k0, k1, k2, lane)) continue;
+            if (kRule != kSample && rule == kGreedy) {
+                // a greedy decision is one round trip: made here, not queued
+                // (the decide warps' poll would cost more than it saves)
+                uint32_t unused = 0;
+                if (lane == 0) SV_TRACE_EVENT(kTrDecideBegin, b);
+                item_decide_sequence(P, nullptr, nullptr, nullptr, unused, b, rule, ns, lane);
+                if (lane == 0) SV_TRACE_EVENT(kTrDecideEnd, b);
+                continue;
+            }
             // queue the sequence for the decide warps (once its entry's previous
             // occupant has been read)
             const int h = sh.dq_head;
@@ -1059,18 +1066,26 @@ __global__ void __launch_bounds__(kItemThreads, 2) item_round_kernel(const Param
     __syncthreads();
     // launched as a programmatic dependent: the set-up above may overlap the
     // previous grid; nothing in global memory is touched before it is done
-    wait_for_primary_grid();
-    if (threadIdx.x == 0) SV_TRACE_EVENT(kTrCtaBegin, 0);
+    // (the greedy producer waits on its own, after setting up its first slot)
+    constexpr bool kPrewait = kRule == kGreedy;
+    if (!(kPrewait && warp == kItemProducerWarp)) {
+        wait_for_primary_grid();
+        SV_TRACE_START(kPrewait);
+    }
     if (warp == kItemProducerWarp) {
-        if constexpr (kRule == kGreedy) item_produce_greedy(P, sh, buf, lane);
+        if constexpr (kRule == kGreedy) item_produce_greedy(P, sh, buf, lane, kPrewait);
         else item_produce<kRule>(P, sh, buf, smem + kItemHeaderBytes, lane);
     }
-    else if (warp == kItemRetireWarp) item_retire_loop(P, sh, lane);
+    else if (warp == kItemRetireWarp) item_retire_loop<kRule>(P, sh, lane);
     else if (warp == kItemDecideWarpA || warp == kItemDecideWarpB) {
         const int d = warp == kItemDecideWarpA ? 0 : 1;
-        item_decide_loop(P, sh, &sh.dbar[d], smem + kItemHeaderBytes, d, lane);
+        // (a greedy round's decisions are all made by the retire warp; idle
+        // decide warps would only hold the CTA's exit back)
+        if constexpr (kRule != kGreedy)
+            item_decide_loop(P, sh, &sh.dbar[d], smem + kItemHeaderBytes, d, lane);
     }
     else item_consume(P, sh, buf, smem + kItemHeaderBytes, lane);
+    SV_TRACE_FINISH();
 }
 
 }  // namespace sv

@@ -195,3 +195,35 @@ def test_binding_constants_match_the_header():
     }
     for name, value in mirror.items():
         assert defs[name] == value, name
+
+
+def test_trace_timeline_of_two_launches():
+    """Two launches of two CTAs: each CTA's region holds launch 1's records,
+    then launch 2's, each part opening with the placement record."""
+    import numpy as np
+    E = {name: i for i, name in enumerate(sv.TRACE_EVENTS)}
+
+    def r(t, ev, cta, arg=0):
+        return [t, (E[ev] << 56) | (cta << 32) | arg]
+
+    T = 10_000_000
+    cta0 = [r(T - 300, "cta_placed", 0), r(T, "cta_begin", 0), r(T + 1000, "stage", 0, 1),
+            r(T + 5000, "cta_end", 0),
+            r(T + 4000, "cta_placed", 0), r(T + 7000, "cta_begin", 0),
+            r(T + 8000, "stage", 0, 1), r(T + 12000, "cta_end", 0)]
+    cta1 = [r(T - 200, "cta_placed", 1), r(T + 100, "cta_begin", 1), r(T + 6000, "cta_end", 1),
+            r(T + 5000, "cta_placed", 1), r(T + 7200, "cta_begin", 1),
+            r(T + 13000, "cta_end", 1)]
+    recs = np.array(cta0 + cta1, dtype=np.uint64)
+    parts = sv.trace.split_launches(recs)
+    assert [len(x) for x in parts] == [7, 7]
+    tl = sv.trace_timeline(recs)
+    assert len(tl["launches"]) == 2 and len(tl["between"]) == 1
+    b = tl["between"][0]
+    assert b["period_us"] == 7.0                      # first starts: T and T + 7000
+    assert b["prev_exit_to_start_us"] == 1.0          # last exit T + 6000, next start T + 7000
+    assert b["placed_before_prev_exit_us"] == 1.5     # median placement T + 4500
+    l0 = tl["launches"][0]
+    assert l0["cta_placed_us"] == {"median": -0.25, "max": -0.2}
+    assert l0["cta_end_us"] == {"median": 5.5, "max": 6.0}
+    assert l0["first_stage_after_begin_us"] == {"median": 1.0, "max": 1.0}
