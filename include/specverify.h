@@ -206,12 +206,18 @@ int sv_set_ctas_per_sm(int32_t ctas_per_sm);
  * rows of V f32 logits, laid out like p and q above.  Rows are read in order:
  * the pair (zp_i, zq_i) once for its normalisers and the accept test of
  * position i, the rejected pair (or zp_K) a second time for the draw.
- * Arithmetic is fp32 with exp2.approx and double-fp32 sums: an accept decision
- * can differ from an exact (fp64) softmax only when |u*q - p| < ~1e-5 * p, and
- * a drawn token only when u*R lies within ~2e-6 of normalised mass of a
- * boundary.  temperature must be positive and finite (else SV_EINVAL); logits
- * must be finite.  Greedy needs no warp: argmax softmax(z/T) = argmax z, so
- * sv_verify_greedy takes logits directly.  Workspace and status as above. */
+ * Arithmetic is fp32 with exp2.approx and double-fp32 sums.  An accept test
+ * is decided in fp32 only when its margin |u*q - p| exceeds a bound on the
+ * fast probabilities' error (derived from the fp32 exponent arguments, an
+ * ex2.approx error of at most 2^-20 and the normalisers' sums); otherwise the
+ * position's normalisers are recomputed in fp64 across the grid and the test
+ * is made in fp64, as in an exact softmax.  Accept decisions therefore equal
+ * those of an fp64 softmax except where two fp64 summation orders may round
+ * differently (|u*q - p| within ~1e-13 * p); a drawn token may differ only
+ * when u*R lies within ~2e-6 of normalised mass of a boundary.  temperature
+ * must be positive and finite (else SV_EINVAL); logits must be finite.
+ * Greedy needs no warp: argmax softmax(z/T) = argmax z, so sv_verify_greedy
+ * takes logits directly.  Workspace and status as above. */
 int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride,
                             const float *zq, int64_t zq_row_stride,
                             const int32_t *t, const float *u_accept, const double *u_resample,
@@ -227,7 +233,8 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride,
  * the mean number of accepted draft tokens of a sampling round: the
  * rejection-sampling theorem behind the "spec-verify" page's analytic
  * accepted-length law (section "Measured").  Not part of a verification
- * round: it reads every row p_0..p_{K-1} and q_0..q_{K-1} in full, twice.
+ * round: it reads every row p_0..p_{K-1} and q_0..q_{K-1} in full (once from
+ * memory; the second sweep over a row pair, after its totals, hits L2).
  * Layout and memory rules as above; alpha is [B][K] f64, expected_length [B]
  * f64.  |alpha - exact| <= 2 * 2^-24 * alpha (fp32 scaling of each term,
  * double-fp32 sums).  Uses the workspace of sv_workspace_size(B, K, V); any
@@ -241,7 +248,8 @@ int64_t sv_last_grid_size(void);
 
 /* Number of kernels the last call on this thread enqueued: 1 for the
  * single-launch verification path, 3 for the scan / stream / decide chain,
- * up to 3 for sv_alpha. */
+ * 2 for the mixed round (ordering kernel and item kernel), up to 2 for
+ * sv_alpha. */
 int32_t sv_last_kernel_count(void);
 
 /* Text for an SV_* return code or SV_STATUS_* bit. */
@@ -254,20 +262,23 @@ int sv_version(void);
  * have no counterpart.  Only a library built with -DSV_TRACE=1 records it;
  * in any other build both calls return SV_EINVAL.  Each CTA appends records
  * of two uint64 words to its own region of a static device buffer
- * (SV_TRACE_RECORDS records, SV_TRACE_CTA_RECORDS per CTA; later ones are
- * dropped): word 0 is %globaltimer in ns, word 1 holds the event id in bits
- * 56..63, the CTA in bits 32..55 and the event's argument in bits 0..31.
- * Events: 0 CTA start, 1 item start (sequence), 2 stage issued (count),
- * 3 item fully issued (stages), 4 item retired (sequence), 5 decision start
- * (sequence), 6 decision end (sequence), 7 producer done.
- *   sv_trace_reset: enqueues the clearing of the buffer on `stream` (empty
- *     records have time 0).  Calls that record while another is traced mix
- *     their records.
+ * (SV_TRACE_RECORDS records, SV_TRACE_CTA_RECORDS per CTA index over all
+ * launches since the last reset; later ones are dropped): word 0 is
+ * %globaltimer in ns, word 1 holds the event id in bits 56..63, the CTA in
+ * bits 32..55 and the event's argument in bits 0..31.  Consecutive launches
+ * append after one another, each CTA's records starting with event 8.
+ * Events: 0 CTA start (after the wait for the previous grid), 1 item start
+ * (sequence), 2 stage issued (count), 3 item fully issued (stages), 4 item
+ * retired (sequence), 5 decision start (sequence), 6 decision end
+ * (sequence), 7 producer done, 8 CTA placed (before that wait), 9 CTA exit.
+ *   sv_trace_reset: enqueues the clearing of the buffer and of the per-CTA
+ *     slot counts on `stream` (empty records have time 0).  Calls that
+ *     record while another is traced mix their records.
  *   sv_trace_read: copies the first min(max_records, SV_TRACE_RECORDS)
  *     records into `records` (host memory of 16 * max_records bytes), waits
  *     for `stream`, and sets *count to the number copied. */
-#define SV_TRACE_CTA_RECORDS 512
-#define SV_TRACE_RECORDS (512u * 1024u)
+#define SV_TRACE_CTA_RECORDS 2048
+#define SV_TRACE_RECORDS (2048u * 1024u)
 int sv_trace_reset(sv_stream_t stream);
 int sv_trace_read(void *records, size_t max_records, size_t *count, sv_stream_t stream);
 

@@ -117,7 +117,7 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     L.arrive = off;
     off += round_up((size_t)B * sizeof(int32_t));
     L.groups = off;
-    off += round_up((size_t)B * (size_t)(K + 2) * sizeof(unsigned long long));
+    off += round_up((size_t)B * (size_t)(2 * K + 2) * sizeof(unsigned long long));
     L.seg = off;
     off += round_up((size_t)B * (size_t)num_segments(V) * sizeof(float2));
     L.blk = off;
@@ -191,6 +191,19 @@ bool device_info(int rule, int *sms, int *occ, int *item_occ) {
     *sms = d.sms;
     *occ = d.occupancy[rule] > 0 ? d.occupancy[rule] : 1;
     *item_occ = d.item_occupancy[rule];
+    return true;
+}
+
+// The alpha kernel's dynamic shared memory limit, raised once per device.
+bool alpha_attr_set() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    static std::atomic<int> done[64];
+    if (done[dev].load()) return true;
+    if (cudaFuncSetAttribute(sv::alpha_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sv::kAlphaSmemBytes) != cudaSuccess)
+        return false;
+    done[dev].store(1);
     return true;
 }
 
@@ -584,7 +597,6 @@ int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row
     if (place(A.p) == kUnusable || place(A.q) == kUnusable || place(A.alpha) == kUnusable ||
         place(A.expected) == kUnusable)
         return SV_EINVAL;
-    A.norm = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + L.norm);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 #if SV_DEBUG
     uint32_t *status = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.status);
@@ -592,14 +604,18 @@ int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row
         (K > 0 && sv::check_values(A.q, A.qs, (int64_t)B * K, V, false, status, st)))
         return SV_ECUDA;
 #endif
-    g_last_grid = (int64_t)B * K;
+    const int64_t ctas = (int64_t)B * K * sv::kAlphaCluster;
+    if (ctas > INT32_MAX) return SV_EINVAL;
+    g_last_grid = ctas;
     g_last_kernels = 0;
     if (K > 0) {
-        sv::alpha_norm_kernel<<<(unsigned)(B * K), sv::kAlphaThreads, 0, st>>>(A);
+        // one cluster of kAlphaCluster CTAs per row pair (its dimensions are
+        // compiled into the kernel); the dynamic shared memory caps the CTAs
+        // resident per SM
+        if (!alpha_attr_set() ) return SV_ECUDA;
+        sv::alpha_pair_kernel<<<(unsigned)ctas, sv::kAlphaThreads, sv::kAlphaSmemBytes, st>>>(A);
         if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
-        int rc = launch_dependent(sv::alpha_min_kernel, (unsigned)(B * K), sv::kAlphaThreads, 0, A, st);
-        if (rc != SV_OK) return rc;
-        g_last_kernels = 2;
+        g_last_kernels = 1;
     }
     if (A.expected) {
         if (K == 0) {
@@ -609,7 +625,7 @@ int sv_alpha(const float *p, int64_t p_row_stride, const float *q, int64_t q_row
             int rc = launch_dependent(sv::alpha_length_kernel, (unsigned)((B + 255) / 256), 256u, 0,
                                       A, st);
             if (rc != SV_OK) return rc;
-            g_last_kernels = 3;
+            g_last_kernels = 2;
         }
     }
     return SV_OK;
@@ -645,6 +661,7 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     L.V = V;
     L.nseg = (int32_t)num_segments(V);
     L.c = (float)(1.4426950408889634 / (double)temperature);
+    L.tau = (double)temperature;
     L.n_out = P.n_out;
     L.next_out = P.next_out;
     L.status = P.status;
@@ -657,7 +674,7 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     L.tail = reinterpret_cast<unsigned long long *>(ws + kLgTail);
     L.ndone = reinterpret_cast<uint32_t *>(ws + kLgDone);
     L.nexit = reinterpret_cast<uint32_t *>(ws + kLgExit);
-    L.ngroups = (int64_t)B * (K + 2);
+    L.ngroups = (int64_t)B * (2 * K + 2);
     // one persistent grid of as many CTAs as the SMs hold: bulk-copy workers
     // for 16-byte-aligned device rows, plain-load workers otherwise
     int sms = 0, task_occ = 0, ring_occ = 0;
@@ -720,10 +737,13 @@ int sv_version(void) { return 1; }
 
 int sv_trace_reset(sv_stream_t stream) {
 #if SV_TRACE
-    void *buf = nullptr;
-    if (cudaGetSymbolAddress(&buf, sv::sv_trace_buf) != cudaSuccess) return SV_ECUDA;
-    if (cudaMemsetAsync(buf, 0, sizeof(ulonglong2) * sv::kTraceRecords,
-                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    void *buf = nullptr, *next = nullptr;
+    if (cudaGetSymbolAddress(&buf, sv::sv_trace_buf) != cudaSuccess ||
+        cudaGetSymbolAddress(&next, sv::sv_trace_next) != cudaSuccess)
+        return SV_ECUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(buf, 0, sizeof(ulonglong2) * sv::kTraceRecords, st) != cudaSuccess ||
+        cudaMemsetAsync(next, 0, sizeof(unsigned int) * sv::kTraceMaxCtas, st) != cudaSuccess)
         return SV_ECUDA;
     return SV_OK;
 #else

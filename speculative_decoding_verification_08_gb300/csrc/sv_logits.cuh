@@ -55,7 +55,7 @@ namespace sv {
 constexpr int kLgWarps = 8;
 constexpr int kLgThreads = kLgWarps * 32;
 constexpr float kNegInf = -__builtin_huge_valf();
-constexpr uint32_t kLgNorm = 1u, kLgMass = 2u;  // group kinds
+constexpr uint32_t kLgNorm = 1u, kLgMass = 2u, kLgPrecise = 3u;  // group kinds
 
 struct LogitsParams {
     const float *zp;
@@ -69,6 +69,7 @@ struct LogitsParams {
     int64_t V;
     int32_t nseg;
     float c;            // log2(e) / tau
+    double tau;         // the temperature (the precise recomputation's exp((z - M) / tau))
     int32_t *n_out;
     int32_t *next_out;
     uint32_t *status;
@@ -77,14 +78,15 @@ struct LogitsParams {
                         // sequence's mass pass the first half of its rows holds the
                         // norm tasks' (max, sum) pairs, two float4 per segment
     float4 *fnorm;      // workspace [B][2] normalisers of the chosen row (pair)
-    unsigned long long *grp;    // workspace [B * (K + 2)] groups (0 = not appended)
+    unsigned long long *grp;    // workspace [B * (2K + 2)] groups (0 = not appended)
     int32_t *arrive;    // workspace [B] finished tasks of the sequence's groups so far (every
                         // group has nseg tasks, so a group is complete at a multiple of nseg)
     unsigned long long *head;   // next task (plain-load workers) or chunk (bulk-copy workers)
     unsigned long long *tail;   // groups appended after the first B
     uint32_t *ndone;    // sequences finished
     uint32_t *nexit;    // workers that left
-    int64_t ngroups;    // B * (K + 2): a sequence appends at most K + 1 groups
+    int64_t ngroups;    // B * (2K + 2): a sequence appends at most 2K + 1 groups (a norm
+                        // group per position, a precise one per near-threshold test, a mass one)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -197,6 +199,63 @@ __device__ __forceinline__ float lg_mass(float za, float zb, bool pair, const Ro
     if (!pair) return pa;
     const float qb = __fmul_rn(warp_e(zb, nb.m, c), ib);
     return fmaxf(__fsub_rn(pa, qb), 0.f);
+}
+
+// The fp32 accept test u * qt < pt decides only when its margin is larger
+// than the error of the fast probabilities can be; every other test is made
+// again in fp64 (a precise group).  Relative error of a fast probability
+// exp2(a) / S_hi, first order, with slack:
+//   the argument a: three fp32 roundings (z - M, c = log2(e) / tau, the
+//     product), |da| <= 3 * 2^-24 * |a|, so ln 2 * 3 * 2^-24 * |a| (kLn2ArgRel);
+//   ex2.approx.f32: at most kEx2Rel (2^-20; the GPU tests measure its error
+//     over a dense sweep of arguments against fp64 and require half of it);
+//   the normaliser S: every term carries its own argument error -- at most
+//     ln 2 * 3 * 2^-24 * 64 relative for the terms with |a| <= 64; the others
+//     are below 2^-64 each and cannot matter at 2^-31 terms -- and ex2
+//     error, plus up to nine rescalings by exp2 factors and fp32 sums of four
+//     and of eight (kRowRel);
+//   the reciprocal, S_lo and the product: 3 * 2^-24.
+// Results below 2^-100 (where subnormal outputs lose relative accuracy) are
+// never decided in fp32.
+constexpr float kU24 = 5.9604645e-08f;          // 2^-24
+constexpr float kLn2ArgRel = 1.2395e-07f;       // ln 2 * 3 * 2^-24, rounded up
+constexpr float kEx2Rel = 9.5367432e-07f;       // 2^-20
+constexpr float kRowRel = 64.f * kLn2ArgRel + 10.f * kEx2Rel + 48.f * kU24 + 1e-12f;
+constexpr float kTiny = 7.8886091e-31f;         // 2^-100
+
+// True when u * qt < pt (fp32, as accepts() decides it) is certain to agree
+// with the exact test on the exact softmax; ap, aq are the tokens' fp32
+// arguments.
+__device__ __forceinline__ bool lg_fast_decides(float u, float pt, float qt, float ap, float aq) {
+    const float rp = kLn2ArgRel * fabsf(ap) + kEx2Rel + kRowRel + 3.f * kU24;
+    const float rq = kLn2ArgRel * fabsf(aq) + kEx2Rel + kRowRel + 3.f * kU24;
+    const float uq = u * qt;
+    const float margin = fabsf(fmaf(-u, qt, pt));
+    const float bound = 1.01f * (pt * rp + uq * rq) + 2.f * kU24 * fmaxf(pt, uq) + kTiny;
+    return margin > bound;  // false for NaN too
+}
+
+// fp64 sum of exp((x - M) / tau) over a lane's elements of one segment
+// (-inf marks padding): the precise recomputation's terms, the oracle's
+// formula.
+__device__ __forceinline__ double precise_terms(const float4 (&x)[kVecPerLane], float M, double tau) {
+    double s = 0.0;
+    const double m = (double)M;
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k) {
+        if (x[k].x != kNegInf) s += exp(((double)x[k].x - m) / tau);
+        if (x[k].y != kNegInf) s += exp(((double)x[k].y - m) / tau);
+        if (x[k].z != kNegInf) s += exp(((double)x[k].z - m) / tau);
+        if (x[k].w != kNegInf) s += exp(((double)x[k].w - m) / tau);
+    }
+    return s;
+}
+
+// Sum over the warp in a fixed butterfly (every lane ends with the same bits).
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    return v;
 }
 
 // Masses of segment s of a row (pair) into its segment and block sums (one warp).
@@ -424,9 +483,16 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
         atomicExch(L.arrive + b, 0);  // no later group: the counter is back at zero
         lg_finish(L, b, 0, -1, kStatusBadToken);
     } else if (c) {
-        const float pt = __fmul_rn(warp_e(gp, na.m, L.c), __frcp_rn(na.s.hi));
-        const float qt = __fmul_rn(warp_e(gq, nb.m, L.c), __frcp_rn(nb.s.hi));
-        if (accepts(u, qt, pt)) {
+        const float ap = __fmul_rn(__fsub_rn(gp, na.m), L.c), aq = __fmul_rn(__fsub_rn(gq, nb.m), L.c);
+        const float pt = __fmul_rn(ex2(ap), __frcp_rn(na.s.hi));  // warp_e(gp, na.m, L.c) / S
+        const float qt = __fmul_rn(ex2(aq), __frcp_rn(nb.s.hi));
+        if (!lg_fast_decides(u, pt, qt, ap, aq)) {
+            // too close to call in fp32: the position is decided again in fp64
+            // (the fast normalisers are kept for a later mass group)
+            L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
+            L.fnorm[2 * b + 1] = make_float4(nb.m, nb.s.hi, nb.s.lo, 0.f);
+            lg_append(L, lg_group(b, i, kLgPrecise));
+        } else if (accepts(u, qt, pt)) {
             lg_append(L, lg_group(b, i + 1, kLgNorm));
         } else {
             L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
@@ -453,6 +519,45 @@ __device__ __forceinline__ void lg_load_norms(const LogitsParams &L, int b, bool
           {__shfl_sync(0xffffffffu, f0.y, 0), __shfl_sync(0xffffffffu, f0.z, 0)}};
     nq = {__shfl_sync(0xffffffffu, f1.x, 0),
           {__shfl_sync(0xffffffffu, f1.y, 0), __shfl_sync(0xffffffffu, f1.z, 0)}};
+}
+
+// The precise group's per-segment fp64 sums (p, q), in a segment's pair slot.
+__device__ __forceinline__ double2 *lg_precise_slot(const LogitsParams &L, int b, int64_t s) {
+    return reinterpret_cast<double2 *>(lg_pair(L, b, s));
+}
+
+// `tasks` precise tasks of group g (sequence b, position i) have stored their
+// sums: arrives for them; the group's last arrival adds the segments' sums in
+// segment order (lane l takes segments l, l + 32, ..., then a fixed
+// butterfly), forms p_i(t_i) and q_i(t_i) in fp64 as the oracle does --
+// exp((z - M) / tau) / S with M the row's maximum -- and makes the accept
+// test (double)u * q < p; then the sequence goes on as after a fast test.
+__device__ __noinline__ void lg_precise_arrive(const LogitsParams &L, int b, int i, uint64_t g,
+                                               int tasks, int lane) {
+    int last = 0;
+    if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();  // lane 0's acquire, before every lane's reads below
+    double sp = 0.0, sq = 0.0;
+    for (int64_t k = lane; k < L.nseg; k += 32) {
+        const double2 v = __ldcg(lg_precise_slot(L, b, k));
+        sp += v.x;
+        sq += v.y;
+    }
+    sp = warp_sum_f64(sp);
+    sq = warp_sum_f64(sq);
+    if (lane != 0) return;
+    const int32_t x = L.t[(int64_t)b * L.K + i];  // checked at position 0
+    const float u = L.u_acc[(int64_t)b * L.K + i];
+    const float Mp = __ldcg(L.fnorm + 2 * b).x, Mq = __ldcg(L.fnorm + 2 * b + 1).x;
+    const double zp = (double)__ldcg(lg_row_p(L, b, i) + x), zq = (double)__ldcg(lg_row_q(L, b, i) + x);
+    const double p = exp((zp - (double)Mp) / L.tau) / sp;
+    const double q = exp((zq - (double)Mq) / L.tau) / sq;
+    if ((double)u * q < p)
+        lg_append(L, lg_group(b, i + 1, kLgNorm));
+    else
+        lg_append(L, lg_group(b, i, kLgMass));  // the fast normalisers are in fnorm
+    L.grp[g] = 0ull;  // every task of the group has read it (a precise group is never one of the first B)
 }
 
 // `tasks` mass tasks of group g have stored their sums (and every lane's
@@ -533,6 +638,35 @@ __device__ void lg_mass_task(const LogitsParams &L, int b, int n, int64_t s, uin
     lg_mass_arrive(L, b, n, g, 1, vec, np, nq, ia, ib, lane);
 }
 
+__device__ __noinline__ void lg_precise_task(const LogitsParams &L, int b, int i, int64_t s, uint64_t g,
+                                             bool vec, int lane) {
+    const float *a = lg_row_p(L, b, i);
+    const float *c = lg_row_q(L, b, i);
+    const int64_t base = s * kSeg;
+    const int64_t end = min(L.V, base + kSeg);
+    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+    float4 xa[kVecPerLane], xb[kVecPerLane];
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k) {
+        const int64_t e = base + 4 * (lane + 32 * k);
+        xa[k] = e < end ? load4(a, e, end, vec) : none;
+        xb[k] = e < end ? load4(c, e, end, vec) : none;
+    }
+    float Mp = 0.f, Mq = 0.f;
+    if (lane == 0) {  // after lane 0's acquire of the group
+        Mp = __ldcg(L.fnorm + 2 * b).x;
+        Mq = __ldcg(L.fnorm + 2 * b + 1).x;
+    }
+    Mp = __shfl_sync(0xffffffffu, Mp, 0);
+    Mq = __shfl_sync(0xffffffffu, Mq, 0);
+    const double sp = warp_sum_f64(precise_terms(xa, Mp, L.tau));
+    const double sq = warp_sum_f64(precise_terms(xb, Mq, L.tau));
+    if (lane == 0) *lg_precise_slot(L, b, s) = make_double2(sp, sq);
+    __threadfence();
+    __syncwarp();
+    lg_precise_arrive(L, b, i, g, 1, lane);
+}
+
 __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const LogitsParams L) {
     const int lane = threadIdx.x & 31;
     const bool vec = lg_vec(L);
@@ -554,8 +688,11 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const Logits
         const int b = (int)(uint32_t)d;
         const int i = (int)((d >> 32) & 0xffu);
         const int64_t s = (int64_t)(h % nseg);
-        if (((d >> 40) & 3u) == kLgNorm)
+        const uint32_t kind = (uint32_t)((d >> 40) & 3u);
+        if (kind == kLgNorm)
             lg_norm_task(L, b, i, s, g, vec, lane);
+        else if (kind == kLgPrecise)
+            lg_precise_task(L, b, i, s, g, vec, lane);
         else
             lg_mass_task(L, b, i, s, g, vec, lane);
         h = __shfl_sync(0xffffffffu, hn, 0);
@@ -765,7 +902,7 @@ __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *b
         unsigned long long d = 0;
         if (lane == 0) {
             d = lg_wait_group(L, ch.g);
-            if (d && ((d >> 40) & 3u) == kLgMass) {  // after the group's acquire
+            if (d && ((d >> 40) & 3u) >= kLgMass) {  // mass and precise; after the group's acquire
                 const int b = (int)(uint32_t)d;
                 ch.np = __ldcg(L.fnorm + 2 * b);
                 if ((int)((d >> 32) & 0xffu) < L.K) ch.nq = __ldcg(L.fnorm + 2 * b + 1);
@@ -842,6 +979,29 @@ __device__ __noinline__ void lg_ragged_mass(const float *sp, const float *sq, co
     store_sums(seg, blk, m.s, v, lane);
 }
 
+// A precise stage's segment j (offset o in the stage): its fp64 sums into the
+// segment's slot, the stage released as soon as the elements are in registers
+// (out of line: a rare path, kept out of the consumer loop's registers).
+__device__ __noinline__ void lg_precise_stage(const LogitsParams &L, const LgStage &m, const float *sp,
+                                              const float *sq, int o, int j,
+                                              unsigned long long *empty, int k, int lane) {
+    if (j >= m.ns) {
+        release_stage(empty, k, lane);
+        return;
+    }
+    const int n = min(kSeg, m.n - o), c = max(0, min(kSeg, m.c - o));
+    float4 xa[kVecPerLane], xb[kVecPerLane];
+#pragma unroll
+    for (int v = 0; v < kVecPerLane; ++v) {
+        xa[v] = lg_stage4(sp + o, m.g0 + o, n, c, 4 * (lane + 32 * v), kNegInf);
+        xb[v] = lg_stage4(sq + o, m.g1 + o, n, c, 4 * (lane + 32 * v), kNegInf);
+    }
+    release_stage(empty, k, lane);
+    const double s0 = warp_sum_f64(precise_terms(xa, m.np.x, L.tau));
+    const double s1 = warp_sum_f64(precise_terms(xb, m.nq.x, L.tau));
+    if (lane == 0) *lg_precise_slot(L, m.b, m.s + j) = make_double2(s0, s1);
+}
+
 // Waits (bounded) until the stage of share ticket t holds its fill (the same
 // two-step wait as wait_ticket, per stage ticket t / kLgShares, on this ring's
 // size; kLgConsumers keeps it unambiguous).
@@ -914,6 +1074,9 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
                 release_stage(sh.empty, k, lane);
             }
             if (lg_chunk_done(sh, m.slot, lane)) lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
+        } else if (m.kind == (int)kLgPrecise) {
+            lg_precise_stage(L, m, sp, sq, o, j, sh.empty, k, lane);
+            if (lg_chunk_done(sh, m.slot, lane)) lg_precise_arrive(L, m.b, m.i, m.g, m.tasks, lane);
         } else {
             const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};
             const float ia = __frcp_rn(np.s.hi), ib = pair ? __frcp_rn(nq.s.hi) : 0.f;
