@@ -170,12 +170,16 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride,
  * SV_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the library: every GPU that
  * loads the library holds that array until the process exits.  Sizes whose
  * sv_workspace_size(B, K, V) exceeds it are rejected with SV_ETOOLARGE before
- * anything is enqueued (at V = 128256, K = 5 that is 449 sequences).
+ * anything is enqueued (at V = 128256, K = 5 that is 447 sequences).
  * The call allocates nothing: it issues one cudaMemsetAsync that clears the
  * part of the array that must start at zero, then the kernel launch.
- * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture.  All calls share the one array, which keeps the previous call's
+ * Every call looks up the array's device address in the current device's
+ * context (a host-side lookup), so a device reset, or a different context on
+ * the same device, never leaves the call with a stale address.  The first
+ * call on a device (or in a new context) also loads the library's device
+ * code there, which the CUDA runtime does with an allocation of its own:
+ * make that first call before any stream capture, and before the point after
+ * which nothing may allocate.  All calls share the one array, which keeps the previous call's
  * contents: two calls whose work overlaps on the GPU (different streams, or
  * different host threads without ordering) race on it and give wrong results.
  * Device-detected errors show up as next_token = -1; their status bits are not

@@ -781,25 +781,20 @@ static __device__ __align__(256) unsigned char sv_noalloc_scratch[SV_NOALLOC_SCR
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_addr[kNoAllocMaxDevices] = {};
-
-// Device address of sv_noalloc_scratch on the current device, looked up once
-// per device.  In host code the array's name is only a host-side stand-in, so
-// the kernel must be given this address, never the name.
+// Device address of sv_noalloc_scratch in the current device's context.  In
+// host code the array's name is only a host-side stand-in, so the kernel must
+// be given this address, never the name.  It is looked up on every call: a
+// cached address would outlive a device reset (the array is then placed
+// again, possibly elsewhere) and would be wrong in another context on the same
+// device.  Once the library's device code is loaded in the context, the lookup
+// allocates nothing.
 int noalloc_scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return SV_ECUDA;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, sv_noalloc_scratch) != cudaSuccess || !ptr)
-            return SV_ECUDA;
-        g_noalloc_addr[dev] = ptr;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, sv_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return SV_ECUDA;
     }
-    *out = g_noalloc_addr[dev];
+    *out = ptr;
     return SV_OK;
 }
 
