@@ -386,3 +386,78 @@ def test_device_verifier_reuses_a_workspace_per_k_and_v(monkeypatch):
     call(4, 4, 10)
     assert made == [(5, 4, 10), (6, 4, 10), (2, 0, 10)]
     assert used[0] is used[1] is used[2] and used[3] is used[5] and used[3] is not used[0]
+
+
+def _batched_callbacks(noise, seed=0):
+    """Batched draft/target callbacks over the toy target: every running
+    sequence draws its drafts from its own draft row (any draft is valid
+    for both rules; the rule is the verifier's)."""
+    rng = np.random.default_rng(seed)
+
+    def draft_step(prefixes, k):
+        toks, probs = [], []
+        for pre in prefixes:
+            p = list(pre)
+            tt, pp = [], []
+            for _ in range(k):
+                q = draft_row(p, noise)
+                x = int(rng.choice(V, p=q / q.sum()))
+                tt.append(x)
+                pp.append(q)
+                p.append(x)
+            toks.append(tt)
+            probs.append(np.stack(pp))
+        return toks, np.stack(probs)
+
+    def target_step(prefixes, proposed):
+        out = []
+        for pre, prop in zip(prefixes, proposed):
+            p = list(pre)
+            rows = [target_row(p)]
+            for x in prop:
+                p.append(int(x))
+                rows.append(target_row(p))
+            out.append(np.stack(rows))
+        return np.stack(out)
+
+    return draft_step, target_step
+
+
+@pytest.mark.gpu
+def test_batched_driver_on_the_gpu_matches_the_oracle_every_round():
+    """64 sequences, half greedy and half sampling, through the device round
+    (sv_verify_round with the commit) until each has 30 new tokens: every
+    round's (n_accepted, next_token) equals the oracle's on the same rows and
+    uniforms, and every greedy sequence is exactly plain greedy decoding."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from oracle.compare import compare
+    from speculative_decoding_verification_08_gb300.decoder import DeviceVerifier
+    B = 64
+    flags = [b % 2 == 0 for b in range(B)]
+    prompts = [[1 + b % 7, 2 + b % 5, b % 11] for b in range(B)]
+    draft_step, target_step = _batched_callbacks(0.3)
+    device_verify = DeviceVerifier()
+    rounds = []
+
+    def checked_verify(mode, p, q, t, ua, ur, tokens, lengths):
+        host = [x.cpu().numpy() for x in (mode, p, q, t, ua, ur)]
+        n, x = device_verify(mode, p, q, t, ua, ur, tokens, lengths)
+        n0, x0, s0 = oracle.verify_round(*host)
+        assert s0 == 0
+        compare(host[1], host[2], host[5], host[0], host[3].shape[1], n0, x0, n.cpu().numpy(),
+                x.cpu().numpy(), label="batched driver round")
+        rounds.append(int(mode.shape[0]))
+        return n, x
+
+    dec = BatchedSpeculativeDecoder(draft_step, target_step, k=4, greedy=flags, seed=5,
+                                    verify=checked_verify)
+    outs = dec.generate(prompts, max_new=30)
+    assert len(rounds) >= 8 and rounds[0] == B
+    for b in range(B):
+        assert len(outs[b]) == 30
+        if flags[b]:
+            assert outs[b] == plain_greedy(prompts[b], 30), b
+    # sampled rounds accepted some drafts and rejected some
+    ns = [n for _, per in dec.trace for _, n, _ in per]
+    assert 0 in ns and 4 in ns
