@@ -564,7 +564,12 @@ __device__ __noinline__ void lg_precise_arrive(const LogitsParams &L, int b, int
 // stores are ordered before this call): arrives for them; the group's last
 // arrival draws and finishes the sequence.
 __device__ __noinline__ void lg_mass_arrive(const LogitsParams &L, int b, int n, uint64_t g, int tasks, bool vec,
-                               const RowNorm &np, const RowNorm &nq, float ia, float ib, int lane) {
+                               const RowNorm &np, const RowNorm &nq, float ia, float ib, int lane,
+                               int kind = (int)kLgMass) {
+    if (kind == (int)kLgPrecise) {  // (the bulk-copy workers' precise chunks arrive here)
+        lg_precise_arrive(L, b, n, g, tasks, lane);
+        return;
+    }
     const float *a = lg_row_p(L, b, n);
     const float *c = lg_row_q(L, b, n);
     float2 *seg = L.seg + (int64_t)b * L.nseg;
@@ -871,12 +876,17 @@ __device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &
     m.nq = ch.nq;
     const float *a = lg_row_p(L, m.b, m.i);
     const float *c = lg_row_q(L, m.b, m.i);
+    // a precise stage (rare) is read by its consumer from global memory and
+    // takes the consumers' out-of-line path: no copy, and the temperature in
+    // np.w (an fp32 value, so exact)
+    const bool precise = m.kind == (int)kLgPrecise;
+    if (precise) m.np.w = (float)L.tau;
     for (int64_t s = s0; s < s1; s += kLgStageSegs) {
         const int64_t base = s * kSeg;
         m.s = s;
         m.ns = (int)min((int64_t)kLgStageSegs, s1 - s);
         m.n = (int)min((int64_t)m.ns * kSeg, L.V - base);
-        m.c = m.n & ~3;
+        m.c = precise ? 0 : m.n & ~3;
         m.g0 = a + base;
         m.g1 = c ? c + base : nullptr;
         pr.issue(m);
@@ -960,6 +970,23 @@ __device__ __noinline__ void lg_ragged_mass(const float *sp, const float *sq, co
                                             const RowNorm &np, const RowNorm &nq, float ia,
                                             float ib, float2 *seg, float2 *blk, float cc,
                                             int lane) {
+    if (m.kind == (int)kLgPrecise) {
+        // a precise stage (no copy, so it always comes here): the segment's
+        // fp64 sums from global memory into its slot; m.np.x and m.nq.x are
+        // the rows' maxima, m.np.w the temperature (a float, exactly)
+        float4 xa[kVecPerLane], xb[kVecPerLane];
+#pragma unroll
+        for (int v = 0; v < kVecPerLane; ++v) {
+            xa[v] = lg_stage4(sp, m.g0, m.n, 0, 4 * (lane + 32 * v), kNegInf);
+            xb[v] = lg_stage4(sq, m.g1, m.n, 0, 4 * (lane + 32 * v), kNegInf);
+        }
+        const double tau = (double)m.np.w;
+        const double s0 = warp_sum_f64(precise_terms(xa, m.np.x, tau));
+        const double s1 = warp_sum_f64(precise_terms(xb, m.nq.x, tau));
+        if (lane == 0)
+            *reinterpret_cast<double2 *>(reinterpret_cast<float4 *>(blk) + 2 * m.s) = make_double2(s0, s1);
+        return;
+    }
     const bool pair = m.g1 != nullptr;
     dd v[kBlocks];
 #pragma unroll
@@ -977,29 +1004,6 @@ __device__ __noinline__ void lg_ragged_mass(const float *sp, const float *sq, co
         v[j] = dd{sum4(ms), 0.f};
     }
     store_sums(seg, blk, m.s, v, lane);
-}
-
-// A precise stage's segment j (offset o in the stage): its fp64 sums into the
-// segment's slot, the stage released as soon as the elements are in registers
-// (out of line: a rare path, kept out of the consumer loop's registers).
-__device__ __noinline__ void lg_precise_stage(const LogitsParams &L, const LgStage &m, const float *sp,
-                                              const float *sq, int o, int j,
-                                              unsigned long long *empty, int k, int lane) {
-    if (j >= m.ns) {
-        release_stage(empty, k, lane);
-        return;
-    }
-    const int n = min(kSeg, m.n - o), c = max(0, min(kSeg, m.c - o));
-    float4 xa[kVecPerLane], xb[kVecPerLane];
-#pragma unroll
-    for (int v = 0; v < kVecPerLane; ++v) {
-        xa[v] = lg_stage4(sp + o, m.g0 + o, n, c, 4 * (lane + 32 * v), kNegInf);
-        xb[v] = lg_stage4(sq + o, m.g1 + o, n, c, 4 * (lane + 32 * v), kNegInf);
-    }
-    release_stage(empty, k, lane);
-    const double s0 = warp_sum_f64(precise_terms(xa, m.np.x, L.tau));
-    const double s1 = warp_sum_f64(precise_terms(xb, m.nq.x, L.tau));
-    if (lane == 0) *lg_precise_slot(L, m.b, m.s + j) = make_double2(s0, s1);
 }
 
 // Waits (bounded) until the stage of share ticket t holds its fill (the same
@@ -1074,10 +1078,7 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
                 release_stage(sh.empty, k, lane);
             }
             if (lg_chunk_done(sh, m.slot, lane)) lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
-        } else if (m.kind == (int)kLgPrecise) {
-            lg_precise_stage(L, m, sp, sq, o, j, sh.empty, k, lane);
-            if (lg_chunk_done(sh, m.slot, lane)) lg_precise_arrive(L, m.b, m.i, m.g, m.tasks, lane);
-        } else {
+        } else {  // mass and precise stages (a precise one has no copy: see lg_issue_chunk)
             const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};
             const float ia = __frcp_rn(np.s.hi), ib = pair ? __frcp_rn(nq.s.hi) : 0.f;
             float2 *seg = L.seg + (int64_t)m.b * L.nseg;
@@ -1111,7 +1112,7 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
                 release_stage(sh.empty, k, lane);
             }
             if (lg_chunk_done(sh, m.slot, lane))
-                lg_mass_arrive(L, m.b, m.i, m.g, m.tasks, true, np, nq, ia, ib, lane);
+                lg_mass_arrive(L, m.b, m.i, m.g, m.tasks, true, np, nq, ia, ib, lane, m.kind);
         }
     }
 }
