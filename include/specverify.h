@@ -170,7 +170,7 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride,
  * SV_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the library: every GPU that
  * loads the library holds that array until the process exits.  Sizes whose
  * sv_workspace_size(B, K, V) exceeds it are rejected with SV_ETOOLARGE before
- * anything is enqueued (at V = 128256, K = 5 that is 447 sequences).
+ * anything is enqueued (at V = 128256, K = 5 that is more than 446 sequences).
  * The call allocates nothing: it issues one cudaMemsetAsync that clears the
  * part of the array that must start at zero, then the kernel launch.
  * Every call looks up the array's device address in the current device's
@@ -274,7 +274,14 @@ int sv_version(void);
  * Events: 0 CTA start (after the wait for the previous grid), 1 item start
  * (sequence), 2 stage issued (count), 3 item fully issued (stages), 4 item
  * retired (sequence), 5 decision start (sequence), 6 decision end
- * (sequence), 7 producer done, 8 CTA placed (before that wait), 9 CTA exit.
+ * (sequence), 7 producer done, 8 CTA placed (before that wait), 9 CTA exit;
+ * and for the bulk-copy workers of sv_verify_sample_logits: 10 chunk claimed
+ * (group | chunk << 24), 11 its group appended (group), 12 its stages issued
+ * (group), 13 chunk completed by a consumer (group), 14 a group's last
+ * arrival decided (sequence | position << 16 | kind << 24; kinds 1 normalisers,
+ * 2 masses and draw, 3 fp64 recheck), 15 an arrival found it is its group's
+ * last (sequence | position << 16; normaliser groups), 16 that arrival has
+ * merged its lane's segment normalisers (the same argument).
  *   sv_trace_reset: enqueues the clearing of the buffer and of the per-CTA
  *     slot counts on `stream` (empty records have time 0).  Calls that
  *     record while another is traced mix their records.

@@ -86,17 +86,20 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
 
 // Workspace layout:
 // [header | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] | arrive[B] |
-//  groups[B][K+2] | seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2] |
+//  groups[B][2K+2] | pend[B] | seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2] |
 //  fnorm[B][2] | order[B]], every region 256-byte aligned; everything before seg
 // must start at zero (and every call leaves it so).  Header: status (u32 at 0), the
 // chunk queue and its exit count (u32 at 4 and 8), the logits path's task
 // counter and appended groups (u64 at 16 and 24), finished sequences and
-// exited workers (u32 at 32 and 36).
+// exited workers (u32 at 32 and 36), deferred mass groups moved into the queue
+// and deferred (u64 at 40 and 48).
 struct Layout {
-    size_t status, queue, miss, nstate, done, ptok, best, arrive, groups, seg, blk, udd, norm,
-        fnorm, order, total;
+    size_t status, queue, miss, nstate, done, ptok, best, arrive, groups, pend, seg, blk, udd,
+        norm, fnorm, order, total;
 };
-constexpr size_t kLgHead = 16, kLgTail = 24, kLgDone = 32, kLgExit = 36;
+constexpr size_t kLgHead = 16, kLgTail = 24, kLgDone = 32, kLgExit = 36, kLgPendHead = 40,
+                 kLgPendTail = 48;
+
 
 Layout layout(int32_t B, int32_t K, int64_t V) {
     Layout L;
@@ -118,6 +121,8 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     off += round_up((size_t)B * sizeof(int32_t));
     L.groups = off;
     off += round_up((size_t)B * (size_t)(2 * K + 2) * sizeof(unsigned long long));
+    L.pend = off;
+    off += round_up((size_t)B * sizeof(unsigned long long));
     L.seg = off;
     off += round_up((size_t)B * (size_t)num_segments(V) * sizeof(float2));
     L.blk = off;
@@ -674,6 +679,9 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     L.tail = reinterpret_cast<unsigned long long *>(ws + kLgTail);
     L.ndone = reinterpret_cast<uint32_t *>(ws + kLgDone);
     L.nexit = reinterpret_cast<uint32_t *>(ws + kLgExit);
+    L.pend = reinterpret_cast<unsigned long long *>(ws + W.pend);
+    L.pend_head = reinterpret_cast<unsigned long long *>(ws + kLgPendHead);
+    L.pend_tail = reinterpret_cast<unsigned long long *>(ws + kLgPendTail);
     L.ngroups = (int64_t)B * (2 * K + 2);
     // one persistent grid of as many CTAs as the SMs hold: bulk-copy workers
     // for 16-byte-aligned device rows, plain-load workers otherwise
@@ -686,6 +694,11 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     const unsigned grid = (unsigned)sms * (unsigned)(forced > 0 ? std::min(forced, occ) : occ);
     g_last_grid = grid;
     g_last_kernels = 1;
+    // mass groups are deferred when the first B groups alone give every
+    // worker a claim (otherwise no chain waits behind another's mass group)
+    const int64_t claims = ring ? (L.nseg + sv::kLgChunkSegs - 1) / sv::kLgChunkSegs : L.nseg;
+    const int64_t workers = (int64_t)grid * (ring ? 1 : sv::kLgWarps);
+    L.defer = (int64_t)B * claims >= workers;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (ring)
         return launch_dependent(sv::logits_ring_kernel, grid, sv::kLgRingThreads,

@@ -49,6 +49,7 @@
 
 #include "sv_device.cuh"
 #include "sv_tma.cuh"
+#include "sv_trace.cuh"
 
 namespace sv {
 
@@ -87,6 +88,10 @@ struct LogitsParams {
     uint32_t *nexit;    // workers that left
     int64_t ngroups;    // B * (2K + 2): a sequence appends at most 2K + 1 groups (a norm
                         // group per position, a precise one per near-threshold test, a mass one)
+    unsigned long long *pend;       // workspace [B] deferred mass groups (0 = not yet written)
+    unsigned long long *pend_head;  // deferred mass groups moved into the queue so far
+    unsigned long long *pend_tail;  // mass groups deferred so far
+    int32_t defer;      // nonzero: mass groups are deferred (see lg_append_mass)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -379,15 +384,83 @@ __device__ __forceinline__ void lg_append(const LogitsParams &L, unsigned long l
     st_release(L.grp + slot, gdesc);
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The mass group that ends sequence b's chain (one lane; the normalisers it
+// needs are in fnorm).  A sequence's normaliser groups form its chain of
+// dependent steps, and a mass group has no successor: when the call defers,
+// the mass group waits in the pending list, so that the chains' next groups
+// are not queued behind it, until a worker that finds no work moves it in
+// (lg_release_mass).
+__device__ void lg_append_mass(const LogitsParams &L, unsigned long long gdesc) {
+    if (!L.defer) {
+        lg_append(L, gdesc);
+        return;
+    }
+    const unsigned long long slot = atomicAdd(L.pend_tail, 1ull);
+    if (slot >= (unsigned long long)L.B) {  // cannot happen: one mass group per sequence
+        atomicOr(L.status, kStatusOverflow);
+        return;
+    }
+    st_release(L.pend + slot, gdesc);
+}
+
+// Deferred mass groups moved into the queue at once (one claim of the
+// pending list and one of the queue for all of them).
+constexpr int kLgReleaseBatch = 4;
+
+// Moves the oldest deferred mass groups, up to kLgReleaseBatch of them, into
+// the queue (one lane), unless there are none or another worker takes them
+// first.
+__device__ void lg_release_mass(const LogitsParams &L) {
+    const unsigned long long h = ld_relaxed64(L.pend_head);
+    const unsigned long long t = ld_relaxed64(L.pend_tail);
+    if (h >= t) return;
+    const unsigned long long n = t - h < (unsigned long long)kLgReleaseBatch ? t - h : kLgReleaseBatch;
+    if (atomicCAS(L.pend_head, h, h + n) != h) return;
+    const unsigned long long slot = (unsigned long long)L.B + atomicAdd(L.tail, n);
+    for (unsigned long long k = 0; k < n; ++k) {
+        // a pending slot is taken just before it is written: wait for it (bounded)
+        IdleClock clk;
+        unsigned long long d;
+        while (!(d = ld_acquire(L.pend + h + k))) {
+            if (!clk.idle(64)) {
+                atomicOr(L.status, kStatusTimeout);
+                return;
+            }
+        }
+        L.pend[h + k] = 0ull;  // zero again for the next call
+        if (slot + k >= (unsigned long long)L.ngroups) {  // cannot happen (see ngroups)
+            atomicOr(L.status, kStatusOverflow);
+            return;
+        }
+        st_release(L.grp + slot + k, d);
+    }
+}
+
+// A worker that has waited this long for its claimed group moves deferred
+// mass groups into the queue (a shorter wait would let them in while the
+// chains' groups are still on their way; a longer one idles the worker).
+constexpr uint64_t kLgReleaseNs = 3000;
+
 // Group g (one lane): the first B are implicit; a later one is waited for
-// until appended, or until every sequence is finished (0).
+// until appended, or until every sequence is finished (0).  Once the wait
+// has lasted kLgReleaseNs, the worker moves deferred mass groups into the
+// queue, so a wait always ends: every unfinished sequence either has a group
+// in the queue or a deferred mass group that a waiting worker appends.
 __device__ unsigned long long lg_wait_group(const LogitsParams &L, uint64_t g) {
     if (g < (uint64_t)L.B) return lg_group((int)g, 0, kLgNorm);
     IdleClock clk;
+    const uint64_t t0 = global_ns();
     while (true) {
         const unsigned long long d = ld_acquire(L.grp + g);
         if (d) return d;
         if (ld_relaxed(L.ndone) >= (uint32_t)L.B) return 0ull;
+        if (L.defer && global_ns() - t0 >= kLgReleaseNs) lg_release_mass(L);
         if (!clk.idle(256)) {
             atomicOr(L.status, kStatusTimeout);
             return 0ull;
@@ -439,6 +512,7 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
     if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
+    if (lane == 0) SV_TRACE_EVENT(kTrLgLast, (uint32_t)b | ((uint32_t)i << 16));
     // the group's last arrival: the draft token, its uniform and (position 0)
     // every draft id are loaded together with the pairs, the token's logits
     // as soon as its id is in
@@ -469,6 +543,7 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
             nb.merge(pb.x, dd{pb.y, pb.z}, L.c);
         }
     }
+    if (lane == 0) SV_TRACE_EVENT(kTrLgMerged, (uint32_t)b | ((uint32_t)i << 16));
     na.warp_merge(L.c);
     if (c) nb.warp_merge(L.c);
     bool bad = false;
@@ -479,6 +554,7 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
         bad = __any_sync(0xffffffffu, bad);
     }
     if (lane != 0) return;
+    SV_TRACE_EVENT(kTrLgDecide, (uint32_t)b | ((uint32_t)i << 16) | (kLgNorm << 24));
     if (bad) {
         atomicExch(L.arrive + b, 0);  // no later group: the counter is back at zero
         lg_finish(L, b, 0, -1, kStatusBadToken);
@@ -497,11 +573,11 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
         } else {
             L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
             L.fnorm[2 * b + 1] = make_float4(nb.m, nb.s.hi, nb.s.lo, 0.f);
-            lg_append(L, lg_group(b, i, kLgMass));
+            lg_append_mass(L, lg_group(b, i, kLgMass));
         }
     } else {
         L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
-        lg_append(L, lg_group(b, i, kLgMass));
+        lg_append_mass(L, lg_group(b, i, kLgMass));
     }
     if (g >= (uint64_t)L.B) L.grp[g] = 0ull;  // every task of the group has read it
 }
@@ -547,6 +623,7 @@ __device__ __noinline__ void lg_precise_arrive(const LogitsParams &L, int b, int
     sp = warp_sum_f64(sp);
     sq = warp_sum_f64(sq);
     if (lane != 0) return;
+    SV_TRACE_EVENT(kTrLgDecide, (uint32_t)b | ((uint32_t)i << 16) | (kLgPrecise << 24));
     const int32_t x = L.t[(int64_t)b * L.K + i];  // checked at position 0
     const float u = L.u_acc[(int64_t)b * L.K + i];
     const float Mp = __ldcg(L.fnorm + 2 * b).x, Mq = __ldcg(L.fnorm + 2 * b + 1).x;
@@ -556,7 +633,7 @@ __device__ __noinline__ void lg_precise_arrive(const LogitsParams &L, int b, int
     if ((double)u * q < p)
         lg_append(L, lg_group(b, i + 1, kLgNorm));
     else
-        lg_append(L, lg_group(b, i, kLgMass));  // the fast normalisers are in fnorm
+        lg_append_mass(L, lg_group(b, i, kLgMass));  // the fast normalisers are in fnorm
     L.grp[g] = 0ull;  // every task of the group has read it (a precise group is never one of the first B)
 }
 
@@ -578,7 +655,10 @@ __device__ __noinline__ void lg_mass_arrive(const LogitsParams &L, int b, int n,
     if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
-    if (lane == 0) atomicExch(L.arrive + b, 0);  // the sequence's last group: back to zero
+    if (lane == 0) {
+        atomicExch(L.arrive + b, 0);  // the sequence's last group: back to zero
+        SV_TRACE_EVENT(kTrLgDecide, (uint32_t)b | ((uint32_t)n << 16) | (kLgMass << 24));
+    }
     DrawInputs in = {};
     in.u = split_uniform(L.u_res[b]);
     int next = draw_core(L.nseg, L.V, seg, blk, nullptr, nullptr, in, lane,
@@ -708,6 +788,8 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const Logits
         if (atomicAdd(L.nexit, 1u) == gridDim.x * kLgWarps - 1) {
             atomicExch(L.head, 0ull);
             atomicExch(L.tail, 0ull);
+            atomicExch(L.pend_head, 0ull);
+            atomicExch(L.pend_tail, 0ull);
             atomicExch(L.ndone, 0u);
             atomicExch(L.nexit, 0u);
         }
@@ -894,16 +976,17 @@ __device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &
 }
 
 // Chunks are taken in queue order (the first B groups, then the appended
-// ones as they come); the claim after the current one is always in flight.
+// ones as they come).  The next chunk is claimed only once the current one's
+// stages are issued: a claim taken earlier would tie an appended group's
+// chunk to a worker that is still busy while others wait for work, and that
+// worker's delay would be the group's (the ring's stages in flight cover the
+// claim's round trip).
 __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *buf, int lane) {
     LgProducer pr(sh, buf, L.status, lane);
     const uint64_t nchunk = (uint64_t)((L.nseg + kLgChunkSegs - 1) / kLgChunkSegs);
     uint32_t nchunks_here = 0;
-    unsigned long long h = 0, hn = 0;
-    if (lane == 0) {
-        h = atomicAdd(L.head, 1ull);
-        hn = atomicAdd(L.head, 1ull);
-    }
+    unsigned long long h = 0;
+    if (lane == 0) h = atomicAdd(L.head, 1ull);
     h = __shfl_sync(0xffffffffu, h, 0);
     while (pr.ok) {
         LgChunk ch = {};
@@ -911,7 +994,9 @@ __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *b
         if (ch.g >= (uint64_t)L.ngroups) break;
         unsigned long long d = 0;
         if (lane == 0) {
+            SV_TRACE_EVENT(kTrLgClaim, (uint32_t)ch.g | ((uint32_t)(h % nchunk) << 24));
             d = lg_wait_group(L, ch.g);
+            SV_TRACE_EVENT(kTrLgReady, (uint32_t)ch.g);
             if (d && ((d >> 40) & 3u) >= kLgMass) {  // mass and precise; after the group's acquire
                 const int b = (int)(uint32_t)d;
                 ch.np = __ldcg(L.fnorm + 2 * b);
@@ -925,9 +1010,12 @@ __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *b
         ch.nq = make_float4(__shfl_sync(0xffffffffu, ch.nq.x, 0), __shfl_sync(0xffffffffu, ch.nq.y, 0),
                             __shfl_sync(0xffffffffu, ch.nq.z, 0), 0.f);
         ch.ci = h % nchunk;
-        h = __shfl_sync(0xffffffffu, hn, 0);
-        if (lane == 0) hn = atomicAdd(L.head, 1ull);
         lg_issue_chunk(L, sh, pr, ch, nchunks_here, lane);
+        if (lane == 0) {
+            SV_TRACE_EVENT(kTrLgIssued, (uint32_t)ch.g);
+            h = atomicAdd(L.head, 1ull);
+        }
+        h = __shfl_sync(0xffffffffu, h, 0);
     }
     // tell every consumer to stop (each stop stage serves kLgShares of them)
     for (int w = 0; w < (kLgConsumers + kLgShares - 1) / kLgShares; ++w) {
@@ -1077,7 +1165,10 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
             } else {
                 release_stage(sh.empty, k, lane);
             }
-            if (lg_chunk_done(sh, m.slot, lane)) lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
+            if (lg_chunk_done(sh, m.slot, lane)) {
+                if (lane == 0) SV_TRACE_EVENT(kTrLgChunkDone, (uint32_t)m.g);
+                lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
+            }
         } else {  // mass and precise stages (a precise one has no copy: see lg_issue_chunk)
             const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};
             const float ia = __frcp_rn(np.s.hi), ib = pair ? __frcp_rn(nq.s.hi) : 0.f;
@@ -1111,8 +1202,10 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
             } else {
                 release_stage(sh.empty, k, lane);
             }
-            if (lg_chunk_done(sh, m.slot, lane))
+            if (lg_chunk_done(sh, m.slot, lane)) {
+                if (lane == 0) SV_TRACE_EVENT(kTrLgChunkDone, (uint32_t)m.g);
                 lg_mass_arrive(L, m.b, m.i, m.g, m.tasks, true, np, nq, ia, ib, lane, m.kind);
+            }
         }
     }
 }
@@ -1128,11 +1221,13 @@ __global__ void __launch_bounds__(kLgRingThreads, 2) logits_ring_kernel(const Lo
             mbar_init(&sh.empty[i], kLgShares);  // released by every share
         }
         sh.ticket = 0;
+        SV_TRACE_INIT();
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (threadIdx.x < kLgSlots) sh.left[threadIdx.x] = 0;
     __syncthreads();
     wait_for_primary_grid();
+    SV_TRACE_START(false);
     if (warp == kLgProducerWarp)
         lg_produce(L, sh, buf, lane);
     else
@@ -1144,10 +1239,13 @@ __global__ void __launch_bounds__(kLgRingThreads, 2) logits_ring_kernel(const Lo
         if (atomicAdd(L.nexit, 1u) == gridDim.x - 1) {
             atomicExch(L.head, 0ull);
             atomicExch(L.tail, 0ull);
+            atomicExch(L.pend_head, 0ull);
+            atomicExch(L.pend_tail, 0ull);
             atomicExch(L.ndone, 0u);
             atomicExch(L.nexit, 0u);
         }
     }
+    SV_TRACE_FINISH();
 }
 
 }  // namespace sv

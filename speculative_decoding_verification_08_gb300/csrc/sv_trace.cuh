@@ -37,6 +37,14 @@ enum TraceEvent : uint32_t {
     kTrProducerEnd = 7,  // the producer issued its stop stages (argument 0)
     kTrCtaPlaced = 8,    // the CTA began its set-up, before the wait (argument 0)
     kTrCtaEnd = 9,       // every warp of the CTA is done (argument 0)
+    // sampling from logits (the bulk-copy workers)
+    kTrLgClaim = 10,     // a producer claimed a chunk (argument: group | chunk << 24)
+    kTrLgReady = 11,     // ... and its group is appended (argument: group)
+    kTrLgIssued = 12,    // ... and every stage of it is issued (argument: group)
+    kTrLgChunkDone = 13, // a consumer completed a chunk (argument: group)
+    kTrLgDecide = 14,    // a group's last arrival decided (argument: sequence | position << 16 | kind << 24)
+    kTrLgLast = 15,      // an arrival found it is its group's last (argument: sequence | position << 16)
+    kTrLgMerged = 16,    // ... and has merged its lane's segment pairs (argument: sequence | position << 16)
 };
 
 constexpr int kTraceCtaCap = 2048;  // records per CTA over all traced launches

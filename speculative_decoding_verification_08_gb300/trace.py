@@ -9,7 +9,9 @@ records of a CTA opening with its "cta_placed" record.
 from __future__ import annotations
 
 TRACE_EVENTS = ("cta_begin", "item_begin", "stage", "item_issued", "item_retired",
-                "decide_begin", "decide_end", "producer_end", "cta_placed", "cta_end")
+                "decide_begin", "decide_end", "producer_end", "cta_placed", "cta_end",
+                # sampling from logits (bulk-copy workers)
+                "lg_claim", "lg_ready", "lg_issued", "lg_chunk_done", "lg_decide", "lg_last", "lg_merged")
 
 
 def _fields(records):

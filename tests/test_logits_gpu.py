@@ -152,6 +152,37 @@ def test_plain_load_workers_at_a_large_batch():
     assert len(set(n0.tolist())) > 2
 
 
+@pytest.mark.parametrize("aligned", [True, False])
+def test_deferred_mass_groups_on_both_worker_kernels(aligned):
+    """At batches whose first groups alone give every worker a claim, each
+    sequence's mass group (its chain's last step) waits in a pending list
+    until a worker finds no other work.  On both worker kernels the outputs
+    equal the oracle's, and a second call on the same workspace gives the same
+    outputs (the pending list and its counters are back at zero after a call)."""
+    K, tau = 4, 1.0
+    B, V = (400, 40000) if aligned else (240, 40001)
+    zp, zq, t, ua, ur = make_logits(B, V + (0 if aligned else 1), K, tau, seed=8100 + B)
+    if not aligned:
+        zp = zp[..., 1:]   # rows off a 16-byte boundary: the plain-load workers
+        zq = zq[..., 1:]
+        t = torch.clamp(t, max=V - 1)
+    ws = sv.Workspace(B, K, V)
+    n1, x1 = sv.verify_sample_logits(zp, zq, t, ua, ur, tau, ws=ws)
+    grid = sv.last_grid_size()
+    nseg = -(-V // 1024)
+    claims, workers = (-(-nseg // 16), grid) if aligned else (nseg, grid * 8)
+    assert B * claims >= workers, "this size must take the deferring schedule"
+    h = [x.cpu().numpy() for x in (zp, zq, t, ua, ur)]
+    n0, x0, s0 = oracle.verify_sample_logits(*h, tau32(tau))
+    assert s0 == 0
+    expl = compare_logits(h[0], h[1], tau32(tau), h[2], h[3], h[4], n0, x0, n1.cpu().numpy(),
+                          x1.cpu().numpy())
+    assert len(draws(expl)) <= 2, expl
+    n2, x2 = sv.verify_sample_logits(zp, zq, t, ua, ur, tau, ws=ws)
+    assert torch.equal(n1, n2) and torch.equal(x1, x2)
+    assert ws.status() == 0
+
+
 def test_empty_batch():
     zp, zq, t, ua, ur = make_logits(1, 100, 3, 1.0, seed=5)
     n, nx = sv.verify_sample_logits(zp[:0], zq[:0], t[:0], ua[:0], ur[:0], 1.0)
