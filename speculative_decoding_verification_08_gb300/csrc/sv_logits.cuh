@@ -92,6 +92,7 @@ struct LogitsParams {
     unsigned long long *pend_head;  // deferred mass groups moved into the queue so far
     unsigned long long *pend_tail;  // mass groups deferred so far
     int32_t defer;      // nonzero: mass groups are deferred (see lg_append_mass)
+    int32_t chunk;      // bulk-copy workers: segments per chunk (a multiple of kLgStageSegs)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -508,29 +509,32 @@ __device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i,
                                int lane) {
     const float *a = lg_row_p(L, b, i);
     const float *c = lg_row_q(L, b, i);
+    // the decision's inputs that no task writes -- the draft token, its
+    // uniform and (position 0) every draft id -- are loaded while lane 0's
+    // arrival is in flight, so the last arrival waits for one round trip
+    // (the token's logits and the segment pairs together), not two
+    int32_t x = -1, y0 = 0, y1 = 0;
+    float u = 0.f, gp = 0.f, gq = 0.f;
+    if (c) {
+        if (lane == 1) {
+            x = __ldg(L.t + (int64_t)b * L.K + i);
+            u = __ldg(L.u_acc + (int64_t)b * L.K + i);
+        }
+        if (i == 0) {
+            if (lane < L.K) y0 = __ldg(L.t + (int64_t)b * L.K + lane);
+            if (lane + 32 < L.K) y1 = __ldg(L.t + (int64_t)b * L.K + lane + 32);
+        }
+    }
     int last = 0;
     if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
     if (lane == 0) SV_TRACE_EVENT(kTrLgLast, (uint32_t)b | ((uint32_t)i << 16));
-    // the group's last arrival: the draft token, its uniform and (position 0)
-    // every draft id are loaded together with the pairs, the token's logits
-    // as soon as its id is in
-    int32_t x = -1, y0 = 0, y1 = 0;
-    float u = 0.f, gp = 0.f, gq = 0.f;
-    if (c) {
-        if (lane == 0) {
-            x = L.t[(int64_t)b * L.K + i];
-            u = L.u_acc[(int64_t)b * L.K + i];
-        }
-        if (i == 0) {
-            if (lane < L.K) y0 = L.t[(int64_t)b * L.K + lane];
-            if (lane + 32 < L.K) y1 = L.t[(int64_t)b * L.K + lane + 32];
-        }
-        if (lane == 0 && x >= 0 && (int64_t)x < L.V) {
-            gp = __ldcg(a + x);
-            gq = __ldcg(c + x);
-        }
+    x = __shfl_sync(0xffffffffu, x, 1);
+    u = __shfl_sync(0xffffffffu, u, 1);
+    if (c && lane == 0 && x >= 0 && (int64_t)x < L.V) {
+        gp = __ldcg(a + x);
+        gq = __ldcg(c + x);
     }
     Online na, nb;
 #pragma unroll 4
@@ -798,7 +802,7 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const Logits
 
 // ---------------------------------------------------------------------------
 // bulk-copy workers (16-byte-aligned device rows): per CTA one producer warp
-// takes chunks of kLgChunkSegs segment tasks of one group from the queue and
+// takes chunks of L.chunk segment tasks of one group from the queue and
 // moves their row segments into a ring of shared-memory stages (kLgStageSegs
 // segments of each row per stage) with cp.async.bulk; kLgConsumers consumer
 // warps take the stages' segments in order, one segment per ticket, and run
@@ -821,11 +825,6 @@ struct LgStage {
     float4 np, nq;    // mass stages: the row (pair)'s normalisers (m, s.hi, s.lo)
 };
 
-// Segments per chunk (one queue claim, one group read, one global arrival).
-#ifndef SV_LG_CHUNK
-#define SV_LG_CHUNK 16
-#endif
-constexpr int kLgChunkSegs = SV_LG_CHUNK;
 // Chunks whose stages are counted in shared memory at once: a chunk's counter
 // is reused kLgSlots chunks later, and only once it is back at zero.
 constexpr int kLgSlots = 32;
@@ -842,7 +841,6 @@ constexpr int kLgStageSegs = SV_LG_STAGE_SEGS;
 constexpr int kLgStages = SV_LG_STAGES;
 constexpr int kLgPartBytes = kLgStageSegs * kSeg * 4;
 constexpr int kLgStageBytes = 2 * kLgPartBytes;
-static_assert(kLgChunkSegs % kLgStageSegs == 0, "a chunk is whole stages");
 static_assert(kLgStages <= 32, "stage bookkeeping is a 32-bit mask");
 // A stage is taken by kLgStageSegs consumers, one segment each (a ticket is a
 // share of a stage), so no warp holds a stage for more than one segment's
@@ -920,13 +918,13 @@ struct LgProducer {
     }
 };
 
-// Issues the stages of chunk ci (segments [ci * kLgChunkSegs, ...)) of group g.
+// Issues the stages of chunk ci (segments [ci * L.chunk, ...)) of group g.
 __device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &pr,
                                const LgChunk &ch, uint32_t &nchunks_here, int lane) {
     const uint64_t g = ch.g, ci = ch.ci;
     const unsigned long long d = ch.d;
-    const int64_t s0 = (int64_t)ci * kLgChunkSegs;
-    const int64_t s1 = min((int64_t)L.nseg, s0 + kLgChunkSegs);
+    const int64_t s0 = (int64_t)ci * L.chunk;
+    const int64_t s1 = min((int64_t)L.nseg, s0 + L.chunk);
     // the chunk's stage counter: free once the chunk kLgSlots before it is done
     const int slot = (int)(nchunks_here++ % kLgSlots);
     bool free = true;
@@ -983,7 +981,7 @@ __device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &
 // claim's round trip).
 __device__ void lg_produce(const LogitsParams &L, LgShared &sh, unsigned char *buf, int lane) {
     LgProducer pr(sh, buf, L.status, lane);
-    const uint64_t nchunk = (uint64_t)((L.nseg + kLgChunkSegs - 1) / kLgChunkSegs);
+    const uint64_t nchunk = (uint64_t)((L.nseg + L.chunk - 1) / L.chunk);
     uint32_t nchunks_here = 0;
     unsigned long long h = 0;
     if (lane == 0) h = atomicAdd(L.head, 1ull);

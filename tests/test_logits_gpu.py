@@ -183,6 +183,19 @@ def test_deferred_mass_groups_on_both_worker_kernels(aligned):
     assert ws.status() == 0
 
 
+def test_large_batch_takes_whole_chunks():
+    """A batch whose first groups give every bulk-copy worker at least 16
+    claims of 16 segments moves 16-segment chunks (smaller batches take 8 or
+    4, which the other tests cover); the outputs equal the oracle's."""
+    B, V, K, tau = 6000, 16384, 2, 1.0
+    zp, zq, t, ua, ur = make_logits(B, V, K, tau, seed=8300)
+    n0, expl = run(zp, zq, t, ua, ur, tau)
+    nseg = -(-V // 1024)
+    assert B * -(-nseg // 16) >= 16 * sv.last_grid_size(), "this size must take 16-segment chunks"
+    assert len(draws(expl)) <= max(1, B // 2000), expl
+    assert len(set(n0.tolist())) == K + 1
+
+
 def test_empty_batch():
     zp, zq, t, ua, ur = make_logits(1, 100, 3, 1.0, seed=5)
     n, nx = sv.verify_sample_logits(zp[:0], zq[:0], t[:0], ua[:0], ur[:0], 1.0)
