@@ -444,7 +444,7 @@ def run_reference(args):
     rps, nb, rounds, el = time_oracle(host, args.mode, K, float("inf"), ncpu,
                                       max_rounds=args.steps, seqs=seqs)
     sample = (f"{nb} of the {B} sequences of input set 0 per step, {rounds} steps, "
-              f"{el:.1f} s on {ncpu} threads; value scaled to full {B}-sequence rounds")
+              f"{el:.3g} s on {ncpu} threads; value scaled to full {B}-sequence rounds")
     line = {
         "impl": "reference", "metric": METRIC, "value": rps, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / rps,
