@@ -170,7 +170,7 @@ int sv_verify_round(const uint8_t *mode, const float *p, int64_t p_row_stride,
  * SV_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the library: every GPU that
  * loads the library holds that array until the process exits.  Sizes whose
  * sv_workspace_size(B, K, V) exceeds it are rejected with SV_ETOOLARGE before
- * anything is enqueued (at V = 128256, K = 5 that is more than 446 sequences).
+ * anything is enqueued (at V = 128256, K = 5 that is more than 444 sequences).
  * The call allocates nothing: it issues one cudaMemsetAsync that clears the
  * part of the array that must start at zero, then the kernel launch.
  * Every call looks up the array's device address in the current device's

@@ -86,7 +86,7 @@ bool sizes_ok(int32_t B, int32_t K, int64_t V) {
 
 // Workspace layout:
 // [header | miss[B] | nstate[B] | done[B] | ptok[B][K] | best[B][K+1] | arrive[B] |
-//  groups[B][2K+2] | pend[B] | seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2] |
+//  groups[B][3K+2] | pend[B] | seg[B][nseg] | blk[B][nseg][8] | udd[B] | norm[B][K][2] |
 //  fnorm[B][2] | order[B]], every region 256-byte aligned; everything before seg
 // must start at zero (and every call leaves it so).  Header: status (u32 at 0), the
 // chunk queue and its exit count (u32 at 4 and 8), the logits path's task
@@ -104,6 +104,7 @@ constexpr size_t kLgHead = 16, kLgTail = 24, kLgDone = 32, kLgExit = 36, kLgPend
 // worker at least kLgChunkSmall claims of 8, else 4 (a measured rule: 16 is
 // best at B=1024 V=128256, 8 at B=256, 4 at B <= 64 with V=32000)
 constexpr int64_t kLgChunkBig = 16, kLgChunkSmall = 1;
+
 
 
 Layout layout(int32_t B, int32_t K, int64_t V) {
@@ -125,7 +126,7 @@ Layout layout(int32_t B, int32_t K, int64_t V) {
     L.arrive = off;
     off += round_up((size_t)B * sizeof(int32_t));
     L.groups = off;
-    off += round_up((size_t)B * (size_t)(2 * K + 2) * sizeof(unsigned long long));
+    off += round_up((size_t)B * (size_t)(3 * K + 2) * sizeof(unsigned long long));
     L.pend = off;
     off += round_up((size_t)B * sizeof(unsigned long long));
     L.seg = off;
@@ -687,7 +688,7 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     L.pend = reinterpret_cast<unsigned long long *>(ws + W.pend);
     L.pend_head = reinterpret_cast<unsigned long long *>(ws + kLgPendHead);
     L.pend_tail = reinterpret_cast<unsigned long long *>(ws + kLgPendTail);
-    L.ngroups = (int64_t)B * (2 * K + 2);
+    L.ngroups = (int64_t)B * (3 * K + 2);
     // one persistent grid of as many CTAs as the SMs hold: bulk-copy workers
     // for 16-byte-aligned device rows, plain-load workers otherwise
     int sms = 0, task_occ = 0, ring_occ = 0;
@@ -711,6 +712,14 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     if (chunks(16) < kLgChunkBig * workers) L.chunk = 8;
     if (chunks(8) < kLgChunkSmall * workers) L.chunk = 4;
     const int64_t claims = ring ? (L.nseg + L.chunk - 1) / L.chunk : L.nseg;
+    L.claims = claims;
+    // a norm group spans two positions while fewer claims than workers wait
+    // in the queue, in calls whose chains (K decisions) are long against each
+    // worker's share of the first groups (B x claims / workers): there the
+    // workers run short of work for much of the call, and a second
+    // position's reads are cheap next to a step of the chain
+    const bool spans = (int64_t)K * workers >= (int64_t)B * claims;
+    L.spec_claims = spans ? workers : 0;
     L.defer = (int64_t)B * claims >= workers;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (ring)

@@ -79,20 +79,24 @@ struct LogitsParams {
                         // sequence's mass pass the first half of its rows holds the
                         // norm tasks' (max, sum) pairs, two float4 per segment
     float4 *fnorm;      // workspace [B][2] normalisers of the chosen row (pair)
-    unsigned long long *grp;    // workspace [B * (2K + 2)] groups (0 = not appended)
-    int32_t *arrive;    // workspace [B] finished tasks of the sequence's groups so far (every
-                        // group has nseg tasks, so a group is complete at a multiple of nseg)
+    unsigned long long *grp;    // workspace [B * (3K + 2)] group slots (0 = not appended)
+    int32_t *arrive;    // workspace [B] the sequence's arrivals so far, weighted so that every
+                        // group adds 2 nseg (a group is complete at a multiple of 2 nseg)
     unsigned long long *head;   // next task (plain-load workers) or chunk (bulk-copy workers)
     unsigned long long *tail;   // groups appended after the first B
     uint32_t *ndone;    // sequences finished
     uint32_t *nexit;    // workers that left
-    int64_t ngroups;    // B * (2K + 2): a sequence appends at most 2K + 1 groups (a norm
-                        // group per position, a precise one per near-threshold test, a mass one)
+    int64_t ngroups;    // B * (3K + 2): a sequence appends at most 3K + 1 slots (a norm group
+                        // of at most two slots per position after the first, a precise group
+                        // per near-threshold test, a mass one)
     unsigned long long *pend;       // workspace [B] deferred mass groups (0 = not yet written)
     unsigned long long *pend_head;  // deferred mass groups moved into the queue so far
     unsigned long long *pend_tail;  // mass groups deferred so far
     int32_t defer;      // nonzero: mass groups are deferred (see lg_append_mass)
     int32_t chunk;      // bulk-copy workers: segments per chunk (a multiple of kLgStageSegs)
+    int64_t claims;     // queue claims per group slot (chunks, or tasks for the plain-load workers)
+    int64_t spec_claims;  // a norm group spans two positions while fewer claims than this are
+                          // appended and not yet taken (0: never)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -367,11 +371,33 @@ __device__ __forceinline__ int arrive_acq_rel(int32_t *p, int n) {
     return v;
 }
 
-// A group: bit 63 marks it present, then kind (bits 40-41), position (32-39)
-// and sequence (0-31).
-__device__ __forceinline__ unsigned long long lg_group(int b, int i, uint32_t kind) {
-    return (1ull << 63) | ((unsigned long long)kind << 40) |
-           ((unsigned long long)(uint32_t)i << 32) | (unsigned long long)(uint32_t)b;
+// A group slot: bit 63 marks it present, then the slot's place in its span
+// (bit 44), the span less one (bits 42-43), kind (bits 40-41), the slot's
+// position (32-39) and sequence (0-31).  A norm group of span 2 is two
+// consecutive slots, positions i and i + 1, whose tasks count as one group.
+__device__ __forceinline__ unsigned long long lg_group(int b, int i, uint32_t kind, int span = 1,
+                                                       int r = 0) {
+    return (1ull << 63) | ((unsigned long long)r << 44) | ((unsigned long long)(span - 1) << 42) |
+           ((unsigned long long)kind << 40) | ((unsigned long long)(uint32_t)i << 32) |
+           (unsigned long long)(uint32_t)b;
+}
+
+// The span bits of a slot: span - 1, and the slot's place r in bit 2.
+__device__ __forceinline__ int lg_span_bits(unsigned long long d) { return (int)((d >> 42) & 7u); }
+
+// One arrival of `tasks` tasks on sequence b's count (lane 0; acquire and
+// release): every group adds 2 nseg in all (a task of a span-2 group counts
+// 1, any other 2), so a group is complete when the count reaches a multiple
+// of 2 nseg.
+__device__ __forceinline__ bool lg_arrive(const LogitsParams &L, int b, int tasks, int span) {
+    const int w = span == 2 ? tasks : 2 * tasks;
+    return (arrive_acq_rel(L.arrive + b, w) + w) % (2 * L.nseg) == 0;
+}
+
+// The queue's claim counter and appended slots as one snapshot (relaxed;
+// only a hint).
+__device__ __forceinline__ ulonglong2 lg_queue_snapshot(const LogitsParams &L) {
+    return __ldcg(reinterpret_cast<const ulonglong2 *>(L.head));  // head, then tail
 }
 
 // Appends a group (one lane; its earlier stores are visible to every reader
@@ -383,6 +409,27 @@ __device__ __forceinline__ void lg_append(const LogitsParams &L, unsigned long l
         return;
     }
     st_release(L.grp + slot, gdesc);
+}
+
+// Appends sequence b's norm group at position i (one lane).  While the queue,
+// as seen in the snapshot ht, holds fewer than spec_claims claims that no
+// worker has taken, workers are about to wait for work: the group then also
+// covers position i + 1 (when there is one), whose normalisers are ready if
+// position i is accepted and are not used otherwise.
+__device__ __forceinline__ void lg_append_norm(const LogitsParams &L, int b, int i, ulonglong2 ht) {
+    const long long appended =
+        (long long)(((unsigned long long)L.B + ht.y) * (unsigned long long)L.claims);
+    if (i < L.K && appended - (long long)ht.x < L.spec_claims) {
+        const unsigned long long slot = (unsigned long long)L.B + atomicAdd(L.tail, 2ull);
+        if (slot + 1 >= (unsigned long long)L.ngroups) {  // cannot happen (see ngroups)
+            atomicOr(L.status, kStatusOverflow);
+            return;
+        }
+        st_release(L.grp + slot, lg_group(b, i, kLgNorm, 2, 0));
+        st_release(L.grp + slot + 1, lg_group(b, i + 1, kLgNorm, 2, 1));
+    } else {
+        lg_append(L, lg_group(b, i, kLgNorm));
+    }
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
@@ -487,103 +534,154 @@ __device__ __forceinline__ const float *lg_row_q(const LogitsParams &L, int b, i
     return i < L.K ? L.zq + ((int64_t)b * L.K + i) * L.qs : nullptr;
 }
 
-// The (max, sum) slot of segment s of sequence b: two float4, p then q.
-__device__ __forceinline__ float4 *lg_pair(const LogitsParams &L, int b, int64_t s) {
-    return reinterpret_cast<float4 *>(L.blk + (int64_t)b * L.nseg * kBlocks) + 2 * s;
+// The (max, sum) slot of segment s of sequence b for the r-th position of a
+// span: two float4, p then q (the two places fill the sequence's block sums).
+__device__ __forceinline__ float4 *lg_pair(const LogitsParams &L, int b, int64_t s, int r = 0) {
+    return reinterpret_cast<float4 *>(L.blk + (int64_t)b * L.nseg * kBlocks) + 2 * (s + r * (int64_t)L.nseg);
 }
 
 // Stores a norm task's segment pairs (oa, ob), the same in every lane (lane 0).
-__device__ __forceinline__ void lg_store_pair(const LogitsParams &L, int b, int64_t s,
+__device__ __forceinline__ void lg_store_pair(const LogitsParams &L, int b, int64_t s, int r,
                                               const RowNorm &oa, const RowNorm &ob) {
-    float4 *pr = lg_pair(L, b, s);
+    float4 *pr = lg_pair(L, b, s, r);
     pr[0] = make_float4(oa.m, oa.s.hi, oa.s.lo, 0.f);
     pr[1] = make_float4(ob.m, ob.s.hi, ob.s.lo, 0.f);
 }
 
-// `tasks` norm tasks of group g (sequence b, position i) have stored their
-// pairs: arrives for them; the group's last arrival merges every segment's
-// pair in segment order (lane l takes segments l, l + 32, ..., then a fixed
-// butterfly), makes the accept test on the gathered logits and appends the
-// sequence's next group (or finishes it on an invalid draft id).
-__device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i, uint64_t g, int tasks,
-                               int lane) {
-    const float *a = lg_row_p(L, b, i);
-    const float *c = lg_row_q(L, b, i);
-    // the decision's inputs that no task writes -- the draft token, its
-    // uniform and (position 0) every draft id -- are loaded while lane 0's
-    // arrival is in flight, so the last arrival waits for one round trip
-    // (the token's logits and the segment pairs together), not two
-    int32_t x = -1, y0 = 0, y1 = 0;
-    float u = 0.f, gp = 0.f, gq = 0.f;
-    if (c) {
-        if (lane == 1) {
-            x = __ldg(L.t + (int64_t)b * L.K + i);
-            u = __ldg(L.u_acc + (int64_t)b * L.K + i);
-        }
-        if (i == 0) {
-            if (lane < L.K) y0 = __ldg(L.t + (int64_t)b * L.K + lane);
-            if (lane + 32 < L.K) y1 = __ldg(L.t + (int64_t)b * L.K + lane + 32);
-        }
+// Decides position i of sequence b from its row (pair)'s normalisers na, nb
+// and the draft token's logits gp, gq (lane 0): true if the fast test accepts
+// the draft token; otherwise the sequence's next group is appended (a precise
+// one for a test too close to call in fp32, a mass one after a rejection or
+// at the bonus position K) with the normalisers it needs in fnorm.
+__device__ __forceinline__ bool lg_decide_fast(const LogitsParams &L, int b, int i, const Online &na,
+                                               const Online &nb, float gp, float gq, float u) {
+    SV_TRACE_EVENT(kTrLgDecide, (uint32_t)b | ((uint32_t)i << 16) | (kLgNorm << 24));
+    if (i == L.K) {
+        L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
+        lg_append_mass(L, lg_group(b, i, kLgMass));
+        return false;
     }
-    int last = 0;
-    if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __syncwarp();  // lane 0's acquire, before every lane's reads below
-    if (lane == 0) SV_TRACE_EVENT(kTrLgLast, (uint32_t)b | ((uint32_t)i << 16));
-    x = __shfl_sync(0xffffffffu, x, 1);
-    u = __shfl_sync(0xffffffffu, u, 1);
-    if (c && lane == 0 && x >= 0 && (int64_t)x < L.V) {
-        gp = __ldcg(a + x);
-        gq = __ldcg(c + x);
+    const float ap = __fmul_rn(__fsub_rn(gp, na.m), L.c), aq = __fmul_rn(__fsub_rn(gq, nb.m), L.c);
+    const float pt = __fmul_rn(ex2(ap), __frcp_rn(na.s.hi));  // warp_e(gp, na.m, L.c) / S
+    const float qt = __fmul_rn(ex2(aq), __frcp_rn(nb.s.hi));
+    const bool sure = lg_fast_decides(u, pt, qt, ap, aq);
+    if (sure && accepts(u, qt, pt)) return true;
+    // too close to call in fp32 (the position is decided again in fp64; the
+    // fast normalisers are kept for a later mass group), or rejected
+    L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
+    L.fnorm[2 * b + 1] = make_float4(nb.m, nb.s.hi, nb.s.lo, 0.f);
+    if (sure)
+        lg_append_mass(L, lg_group(b, i, kLgMass));
+    else
+        lg_append(L, lg_group(b, i, kLgPrecise));
+    return false;
+}
+
+// The last arrival of sequence b's norm group of kSpan positions from i0
+// (slots g0, ...): merges the segment pairs of each position in segment order
+// (lane l takes segments l, l + 32, ..., then a fixed butterfly), makes the
+// accept tests in position order and appends the sequence's next group (or
+// finishes it on an invalid draft id).  Lane 1 + k holds position i0 + k's
+// draft token x and uniform u; y0, y1 the draft ids (position 0).
+template <int kSpan>
+__device__ __forceinline__ void lg_norm_decide(const LogitsParams &L, int b, int i0, uint64_t g0,
+                                               int32_t x, float u, int32_t y0, int32_t y1, int lane) {
+    const int p = i0 + lane - 1;
+    float gp = 0.f, gq = 0.f;
+    if (lane >= 1 && lane <= kSpan && p < L.K && x >= 0 && (int64_t)x < L.V) {
+        gp = __ldcg(lg_row_p(L, b, p) + x);
+        gq = __ldcg(lg_row_q(L, b, p) + x);
     }
-    Online na, nb;
+    // the queue's state, for the next group's span (with the pairs' round trip)
+    ulonglong2 ht = make_ulonglong2(0ull, 0ull);
+    if (lane == 3 && L.spec_claims > 0) ht = lg_queue_snapshot(L);
+    const bool c0 = i0 < L.K, c1 = kSpan == 2 && i0 + 1 < L.K;
+    Online na, nb, ma, mb;
 #pragma unroll 4
     for (int64_t k = lane; k < L.nseg; k += 32) {
-        const float4 *pr = lg_pair(L, b, k);
+        const float4 *pr = lg_pair(L, b, k, 0);
         const float4 pa = __ldcg(pr);
-        na.merge(pa.x, dd{pa.y, pa.z}, L.c);
-        if (c) {
-            const float4 pb = __ldcg(pr + 1);
-            nb.merge(pb.x, dd{pb.y, pb.z}, L.c);
+        const float4 pb = c0 ? __ldcg(pr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (kSpan == 2) {
+            const float4 *qr = lg_pair(L, b, k, 1);
+            const float4 qa = __ldcg(qr);
+            const float4 qb = c1 ? __ldcg(qr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ma.merge(qa.x, dd{qa.y, qa.z}, L.c);
+            if (c1) mb.merge(qb.x, dd{qb.y, qb.z}, L.c);
         }
+        na.merge(pa.x, dd{pa.y, pa.z}, L.c);
+        if (c0) nb.merge(pb.x, dd{pb.y, pb.z}, L.c);
     }
-    if (lane == 0) SV_TRACE_EVENT(kTrLgMerged, (uint32_t)b | ((uint32_t)i << 16));
+    if (lane == 0) SV_TRACE_EVENT(kTrLgMerged, (uint32_t)b | ((uint32_t)i0 << 16));
     na.warp_merge(L.c);
-    if (c) nb.warp_merge(L.c);
+    if (c0) nb.warp_merge(L.c);
+    if constexpr (kSpan == 2) {
+        ma.warp_merge(L.c);
+        if (c1) mb.warp_merge(L.c);
+    }
     bool bad = false;
-    if (c && i == 0) {  // every draft id is checked once, before the first decision
+    if (i0 == 0 && L.K > 0) {  // every draft id is checked once, before the first decision
         static_assert(kMaxK <= 64, "two draft ids per lane");
         bad = (lane < L.K && (y0 < 0 || (int64_t)y0 >= L.V)) ||
               (lane + 32 < L.K && (y1 < 0 || (int64_t)y1 >= L.V));
         bad = __any_sync(0xffffffffu, bad);
     }
-    if (lane != 0) return;
-    SV_TRACE_EVENT(kTrLgDecide, (uint32_t)b | ((uint32_t)i << 16) | (kLgNorm << 24));
-    if (bad) {
-        atomicExch(L.arrive + b, 0);  // no later group: the counter is back at zero
-        lg_finish(L, b, 0, -1, kStatusBadToken);
-    } else if (c) {
-        const float ap = __fmul_rn(__fsub_rn(gp, na.m), L.c), aq = __fmul_rn(__fsub_rn(gq, nb.m), L.c);
-        const float pt = __fmul_rn(ex2(ap), __frcp_rn(na.s.hi));  // warp_e(gp, na.m, L.c) / S
-        const float qt = __fmul_rn(ex2(aq), __frcp_rn(nb.s.hi));
-        if (!lg_fast_decides(u, pt, qt, ap, aq)) {
-            // too close to call in fp32: the position is decided again in fp64
-            // (the fast normalisers are kept for a later mass group)
-            L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
-            L.fnorm[2 * b + 1] = make_float4(nb.m, nb.s.hi, nb.s.lo, 0.f);
-            lg_append(L, lg_group(b, i, kLgPrecise));
-        } else if (accepts(u, qt, pt)) {
-            lg_append(L, lg_group(b, i + 1, kLgNorm));
-        } else {
-            L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
-            L.fnorm[2 * b + 1] = make_float4(nb.m, nb.s.hi, nb.s.lo, 0.f);
-            lg_append_mass(L, lg_group(b, i, kLgMass));
-        }
-    } else {
-        L.fnorm[2 * b] = make_float4(na.m, na.s.hi, na.s.lo, 0.f);
-        lg_append_mass(L, lg_group(b, i, kLgMass));
+    const float u0 = __shfl_sync(0xffffffffu, u, 1), gp0 = __shfl_sync(0xffffffffu, gp, 1),
+                gq0 = __shfl_sync(0xffffffffu, gq, 1);
+    float u1 = 0.f, gp1 = 0.f, gq1 = 0.f;
+    if constexpr (kSpan == 2) {
+        u1 = __shfl_sync(0xffffffffu, u, 2);
+        gp1 = __shfl_sync(0xffffffffu, gp, 2);
+        gq1 = __shfl_sync(0xffffffffu, gq, 2);
     }
-    if (g >= (uint64_t)L.B) L.grp[g] = 0ull;  // every task of the group has read it
+    ht.x = __shfl_sync(0xffffffffu, ht.x, 3);
+    ht.y = __shfl_sync(0xffffffffu, ht.y, 3);
+    if (lane != 0) return;
+    if (bad) {
+        atomicExch(L.arrive + b, 0);  // no later group: the count is back at zero
+        lg_finish(L, b, 0, -1, kStatusBadToken);
+    } else if (lg_decide_fast(L, b, i0, na, nb, gp0, gq0, u0) &&
+               (kSpan == 1 || lg_decide_fast(L, b, i0 + 1, ma, mb, gp1, gq1, u1))) {
+        lg_append_norm(L, b, i0 + kSpan, ht);
+    }
+    if (g0 >= (uint64_t)L.B) {  // every task of the group has read its slots
+        L.grp[g0] = 0ull;
+        if (kSpan == 2) L.grp[g0 + 1] = 0ull;
+    }
+}
+
+// `tasks` norm tasks of slot g (sequence b, position i; span bits sj) have
+// stored their pairs: arrives for them, and the group's last arrival decides
+// (lg_norm_decide).  The decision's inputs that no task writes -- the span's
+// draft tokens, their uniforms and, at position 0, every draft id -- are
+// loaded while lane 0's arrival is in flight, so the last arrival waits for
+// one round trip (the tokens' logits, the segment pairs and the queue's state
+// together), not two.
+__device__ __noinline__ void lg_norm_arrive(const LogitsParams &L, int b, int i, uint64_t g, int sj,
+                                            int tasks, int lane) {
+    const int span = (sj & 3) + 1, r = sj >> 2;
+    const int i0 = i - r;  // the span's first position; its slots are g - r, ...
+    // lane 1 + k loads position i0 + k's draft token and uniform
+    int32_t x = -1, y0 = 0, y1 = 0;
+    float u = 0.f;
+    const int p = i0 + lane - 1;
+    if (lane >= 1 && lane <= span && p < L.K) {
+        x = __ldg(L.t + (int64_t)b * L.K + p);
+        u = __ldg(L.u_acc + (int64_t)b * L.K + p);
+    }
+    if (i0 == 0 && L.K > 0) {
+        if (lane < L.K) y0 = __ldg(L.t + (int64_t)b * L.K + lane);
+        if (lane + 32 < L.K) y1 = __ldg(L.t + (int64_t)b * L.K + lane + 32);
+    }
+    int last = 0;
+    if (lane == 0) last = lg_arrive(L, b, tasks, span);
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();  // lane 0's acquire, before every lane's reads below
+    if (lane == 0) SV_TRACE_EVENT(kTrLgLast, (uint32_t)b | ((uint32_t)i0 << 16));
+    if (span == 1)
+        lg_norm_decide<1>(L, b, i0, g, x, u, y0, y1, lane);
+    else
+        lg_norm_decide<2>(L, b, i0, g - r, x, u, y0, y1, lane);
 }
 
 // The chosen row (pair)'s normalisers, read by lane 0 (after the group's
@@ -615,9 +713,11 @@ __device__ __forceinline__ double2 *lg_precise_slot(const LogitsParams &L, int b
 __device__ __noinline__ void lg_precise_arrive(const LogitsParams &L, int b, int i, uint64_t g,
                                                int tasks, int lane) {
     int last = 0;
-    if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
+    if (lane == 0) last = lg_arrive(L, b, tasks, 1);
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
+    ulonglong2 ht = make_ulonglong2(0ull, 0ull);
+    if (L.spec_claims > 0) ht = lg_queue_snapshot(L);  // (only lane 0 uses it)
     double sp = 0.0, sq = 0.0;
     for (int64_t k = lane; k < L.nseg; k += 32) {
         const double2 v = __ldcg(lg_precise_slot(L, b, k));
@@ -635,7 +735,7 @@ __device__ __noinline__ void lg_precise_arrive(const LogitsParams &L, int b, int
     const double p = exp((zp - (double)Mp) / L.tau) / sp;
     const double q = exp((zq - (double)Mq) / L.tau) / sq;
     if ((double)u * q < p)
-        lg_append(L, lg_group(b, i + 1, kLgNorm));
+        lg_append_norm(L, b, i + 1, ht);
     else
         lg_append_mass(L, lg_group(b, i, kLgMass));  // the fast normalisers are in fnorm
     L.grp[g] = 0ull;  // every task of the group has read it (a precise group is never one of the first B)
@@ -656,7 +756,7 @@ __device__ __noinline__ void lg_mass_arrive(const LogitsParams &L, int b, int n,
     float2 *seg = L.seg + (int64_t)b * L.nseg;
     float2 *blk = L.blk + (int64_t)b * L.nseg * kBlocks;
     int last = 0;
-    if (lane == 0) last = (arrive_acq_rel(L.arrive + b, tasks) + tasks) % L.nseg == 0;
+    if (lane == 0) last = lg_arrive(L, b, tasks, 1);
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __syncwarp();  // lane 0's acquire, before every lane's reads below
     if (lane == 0) {
@@ -693,8 +793,8 @@ __device__ __noinline__ void lg_mass_arrive(const LogitsParams &L, int b, int n,
 // plain-load workers (rows that are not 16-byte aligned, or in host memory):
 // every warp takes one segment task at a time and loads it itself
 
-__device__ void lg_norm_task(const LogitsParams &L, int b, int i, int64_t s, uint64_t g, bool vec,
-                             int lane) {
+__device__ void lg_norm_task(const LogitsParams &L, int b, int i, int64_t s, uint64_t g, int sj,
+                             bool vec, int lane) {
     const float *a = lg_row_p(L, b, i);
     const float *c = lg_row_q(L, b, i);
     const int64_t base = s * kSeg;
@@ -709,8 +809,8 @@ __device__ void lg_norm_task(const LogitsParams &L, int b, int i, int64_t s, uin
     }
     const RowNorm oa = seg_norm(xa, L.c);
     const RowNorm ob = c ? seg_norm(xb, L.c) : RowNorm{kNegInf, {0.f, 0.f}};
-    if (lane == 0) lg_store_pair(L, b, s, oa, ob);
-    lg_norm_arrive(L, b, i, g, 1, lane);
+    if (lane == 0) lg_store_pair(L, b, s, sj >> 2, oa, ob);
+    lg_norm_arrive(L, b, i, g, sj, 1, lane);
 }
 
 __device__ void lg_mass_task(const LogitsParams &L, int b, int n, int64_t s, uint64_t g, bool vec,
@@ -779,7 +879,7 @@ __global__ void __launch_bounds__(kLgThreads, 2) logits_task_kernel(const Logits
         const int64_t s = (int64_t)(h % nseg);
         const uint32_t kind = (uint32_t)((d >> 40) & 3u);
         if (kind == kLgNorm)
-            lg_norm_task(L, b, i, s, g, vec, lane);
+            lg_norm_task(L, b, i, s, g, lg_span_bits(d), vec, lane);
         else if (kind == kLgPrecise)
             lg_precise_task(L, b, i, s, g, vec, lane);
         else
@@ -822,6 +922,7 @@ struct LgStage {
     int c;            // elements delivered by the copies (a multiple of 4)
     int slot;         // the chunk's counter in LgShared::left
     int tasks;        // stages of the chunk
+    int sj;           // the slot's span bits (norm stages)
     float4 np, nq;    // mass stages: the row (pair)'s normalisers (m, s.hi, s.lo)
 };
 
@@ -950,6 +1051,7 @@ __device__ void lg_issue_chunk(const LogitsParams &L, LgShared &sh, LgProducer &
     m.b = (int)(uint32_t)d;
     m.i = (int)((d >> 32) & 0xffu);
     m.kind = (int)((d >> 40) & 3u);
+    m.sj = lg_span_bits(d);
     m.slot = slot;
     m.tasks = (int)(s1 - s0);
     m.np = ch.np;
@@ -1159,13 +1261,13 @@ __device__ void lg_consume(const LogitsParams &L, LgShared &sh, unsigned char *b
                     if (pair) ob = lg_ragged_norm(sq + o, m.g1 + o, n, c, L.c, lane);
                     release_stage(sh.empty, k, lane);
                 }
-                if (lane == 0) lg_store_pair(L, m.b, m.s + j, oa, ob);
+                if (lane == 0) lg_store_pair(L, m.b, m.s + j, m.sj >> 2, oa, ob);
             } else {
                 release_stage(sh.empty, k, lane);
             }
             if (lg_chunk_done(sh, m.slot, lane)) {
                 if (lane == 0) SV_TRACE_EVENT(kTrLgChunkDone, (uint32_t)m.g);
-                lg_norm_arrive(L, m.b, m.i, m.g, m.tasks, lane);
+                lg_norm_arrive(L, m.b, m.i, m.g, m.sj, m.tasks, lane);
             }
         } else {  // mass and precise stages (a precise one has no copy: see lg_issue_chunk)
             const RowNorm np = {m.np.x, {m.np.y, m.np.z}}, nq = {m.nq.x, {m.nq.y, m.nq.z}};

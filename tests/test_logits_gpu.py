@@ -245,15 +245,18 @@ def test_timeout_is_reported_and_the_context_stays_usable():
     assert len(draws(expl)) <= 1
 
 
-@pytest.mark.parametrize("shift", [0, 1])
-def test_near_threshold_accept_tests_are_decided_exactly(shift):
-    """Uniforms placed within an ulp of the accept threshold p/q of position 0
-    (p, q the oracle's fp64 softmax at the draft token): far inside the fast
-    fp32 test's error bound, so every such test is made again in fp64, and n
-    must equal the oracle's for every sequence but inside the 1e-9 band.
-    shift=1 starts the rows off a 16-byte boundary (plain-load workers)."""
+@pytest.mark.parametrize("shift,pos", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_near_threshold_accept_tests_are_decided_exactly(shift, pos):
+    """Uniforms placed within an ulp of the accept threshold p/q of position
+    pos (p, q the oracle's fp64 softmax at the draft token): far inside the
+    fast fp32 test's error bound, so every such test is made again in fp64,
+    and n must equal the oracle's for every sequence but inside the 1e-9
+    band.  shift=1 starts the rows off a 16-byte boundary (plain-load
+    workers).  pos=1 accepts position 0 (u = 0) and tests position 1, whose
+    group may also cover position 2 at this small batch: a recheck there
+    leaves the second position's normalisers unused."""
     B, V, K, tau = 96, 7001, 3, 0.9
-    zp, zq, t, ua, ur = make_logits(B, V + shift, K, tau, seed=4242 + shift)
+    zp, zq, t, ua, ur = make_logits(B, V + shift, K, tau, seed=4242 + shift + 10 * pos)
     if shift:
         zp, zq = zp[..., shift:], zq[..., shift:]
         t = torch.clamp(t, max=V - 1)
@@ -261,16 +264,18 @@ def test_near_threshold_accept_tests_are_decided_exactly(shift):
     u = ua.cpu().numpy().copy()
     placed = 0
     for b in range(B):
-        x = int(ht[b, 0])
-        r = oracle.softmax(hp[b, 0], tau32(tau))[x] / oracle.softmax(hq[b, 0], tau32(tau))[x]
+        if pos == 1:
+            u[b, 0] = 0.0
+        x = int(ht[b, pos])
+        r = oracle.softmax(hp[b, pos], tau32(tau))[x] / oracle.softmax(hq[b, pos], tau32(tau))[x]
         if r < 0.999:
             u0 = np.float32(r)
-            u[b, 0] = [np.nextafter(u0, np.float32(0)), u0, np.nextafter(u0, np.float32(1))][b % 3]
+            u[b, pos] = [np.nextafter(u0, np.float32(0)), u0, np.nextafter(u0, np.float32(1))][b % 3]
             placed += 1
     assert placed >= B // 5
     n0, expl = run(zp, zq, t, torch.from_numpy(u).cuda(), ur, tau)
     assert not [e for e in expl if e[1] == "accept"], expl
-    assert 0 < (n0 == 0).sum() < B
+    assert 0 < (n0 == pos).sum() < B and (n0 >= pos).all()
 
 
 def test_ex2_approx_error_is_within_the_assumed_bound(tmp_path):

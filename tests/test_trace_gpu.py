@@ -2,8 +2,8 @@
 build's, and its records obey what every launch must show -- each CTA placed,
 started and gone once per launch; the sampling item kernel retires each
 sequence's items and writes one decision per sequence; the logits workers
-record one mass decision per sequence (every sequence ends in one draw) and at
-least one normaliser decision per sequence.  Tracing is a diagnostic build:
+record one mass decision per sequence (every sequence ends in one draw), at
+least one normaliser decision per sequence, and one or two per group.  Tracing is a diagnostic build:
 these tests check that it records what happened, not how fast."""
 import ctypes
 
@@ -114,7 +114,9 @@ def test_logits_timeline(libs):
     assert np.array_equal(pos[mass][np.argsort(seq[mass])], want[0])
     norm = dec & (kind == 1)
     assert set(seq[norm]) == set(range(B))
-    # a normaliser group's last arrival is recorded, then its merge, then its decision
-    assert (ev == EV["lg_last"]).sum() == norm.sum()
-    assert (ev == EV["lg_merged"]).sum() == (ev == EV["lg_last"]).sum()
+    # a normaliser group's last arrival is recorded, then its merge, then one
+    # decision per position it covers (one or two)
+    last = int((ev == EV["lg_last"]).sum())
+    assert last <= int(norm.sum()) <= 2 * last
+    assert (ev == EV["lg_merged"]).sum() == last
     assert (ev == EV["lg_claim"]).sum() >= (ev == EV["lg_issued"]).sum() > 0
