@@ -21,9 +21,10 @@
 //     |alpha - exact| <= 2 * 2^-24 * alpha ~ 1.2e-7; the partials go to the
 //     cluster's first CTA, which adds them in rank order;
 //  3. a dependent launch, one thread per sequence, forms E[b] in fp64.
-// The launch holds kAlphaCtasPerSm CTAs per SM (set by its shared memory),
-// so that the row pairs being read at once stay well inside L2 until their
-// second read.
+// The launch's shared memory (which also keeps the first segments of each
+// CTA's slice for the second sweep) and registers bound the CTAs resident
+// per SM, so that the row pairs being read at once stay mostly inside L2
+// until their second read.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -64,19 +65,34 @@ __device__ __forceinline__ dd cta_sum_dd(dd v, dd *sh, int warp, int lane) {
 
 // Per-lane sums over segments [s0, s1) of a row pair: f(pv, qv) takes the
 // four terms of a float4 pair; aligned full segments take 16-byte loads, the
-// rest scalar loads.
-template <class F>
+// rest scalar loads.  kKeep: the first kAlphaKeepSegs full segments of the
+// slice are also stored in (1) or read from (2) the shared-memory copy, so the
+// second sweep reads them from shared memory instead of L2.
+constexpr int kAlphaKeepSegs = 4;  // 2 rows x 4 x 4 KB = 32 KB of the shared memory reserved
+template <int kKeep, class F>
 __device__ __forceinline__ void slice_pair_sums(const float *pr, const float *qr, int64_t V, int s0,
                                                 int s1, bool vec, int warp, int lane, F f, dd &x0,
-                                                dd &x1) {
+                                                dd &x1, float4 *keep) {
     for (int s = s0 + warp; s < s1; s += kAlphaWarps) {
         const int64_t base = (int64_t)s * kSeg;
         const int64_t n = V - base < kSeg ? V - base : kSeg;
-        if (vec && n == kSeg) {
+        const int j = s - s0;  // the segment's place in the slice
+        if (vec && n == kSeg && kKeep == 2 && j < kAlphaKeepSegs) {
+            const float4 *kp = keep + (size_t)j * 2 * (kSeg / 4);
+#pragma unroll 4
+            for (int k = 0; k < kVecPerLane; ++k)
+                f(kp[lane + 32 * k], kp[kSeg / 4 + lane + 32 * k], x0, x1);
+        } else if (vec && n == kSeg) {
+            float4 *kp = keep + (size_t)j * 2 * (kSeg / 4);
 #pragma unroll 4
             for (int k = 0; k < kVecPerLane; ++k) {
                 const int64_t e = base + 4 * (lane + 32 * k);
-                f(ld_stream4(pr + e), ld_stream4(qr + e), x0, x1);
+                const float4 a = ld_stream4(pr + e), c = ld_stream4(qr + e);
+                if (kKeep == 1 && j < kAlphaKeepSegs) {
+                    kp[lane + 32 * k] = a;
+                    kp[kSeg / 4 + lane + 32 * k] = c;
+                }
+                f(a, c, x0, x1);
             }
         } else {
             for (int64_t e = base + 4 * lane; e < base + n; e += 128) {
@@ -97,12 +113,17 @@ __device__ __forceinline__ bool alpha_vec(const AlphaParams &A) {
 }
 
 constexpr int kAlphaCluster = 8;
-// Resident CTAs per SM, set through the launch's dynamic shared memory: at 4,
-// 76 row pairs (78 MB at V = 128256) are being read at once, well inside the
-// 136 MB L2, and the second sweeps re-read 6 % from DRAM (at 6 per SM, 32 %,
-// for a call 2 % faster; at 2 or 3 per SM the calls were 30 % and 5 % slower).
-constexpr int kAlphaCtasPerSm = 4;
+// The launch's dynamic shared memory, sized for kAlphaCtasPerSm CTAs per SM,
+// holds each CTA's first kAlphaKeepSegs segments for the second sweep, which
+// spares that sweep a quarter of its L2 re-reads.  Registers (42 a thread)
+// and the shared-memory carveout hold the residency to 5 CTAs per SM (ncu's
+// occupancy limits), 95 row pairs read at once.  Measured per call at B=256
+// V=128256 K=5: sized for 4 per SM without kept segments 441.5 us, for 4
+// keeping 6 segments 373.0, for 6 keeping 4 343.3; 7 or 8 per SM need at most
+// 32 registers and spill (446.4, 440.8).
+constexpr int kAlphaCtasPerSm = 6;
 constexpr int kAlphaSmemBytes = 200 * 1024 / kAlphaCtasPerSm;
+static_assert(kAlphaKeepSegs * 2 * kSeg * 4 <= kAlphaSmemBytes, "the kept segments fit the reserved memory");
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -134,14 +155,15 @@ __global__ void __cluster_dims__(kAlphaCluster, 1, 1) __launch_bounds__(kAlphaTh
     const float *pr = A.p + ((int64_t)b * (A.K + 1) + i) * A.ps;
     const float *qr = A.q + ((int64_t)b * A.K + i) * A.qs;
     const bool vec = alpha_vec(A);
+    extern __shared__ __align__(16) float4 keep[];
     dd sp = {0.f, 0.f}, sq = {0.f, 0.f};
-    slice_pair_sums(pr, qr, A.V, s0, s1, vec, warp, lane,
+    slice_pair_sums<1>(pr, qr, A.V, s0, s1, vec, warp, lane,
                     [](float4 a, float4 c, dd &x0, dd &x1) {
                         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
                         x0 = dd_add(x0, quad_mass<false>(a, z));
                         x1 = dd_add(x1, quad_mass<false>(c, z));
                     },
-                    sp, sq);
+                    sp, sq, keep);
     sp = warp_sum_dd(sp);
     sq = warp_sum_dd(sq);
     const dd P_part = cta_sum_dd(sp, sh[0], warp, lane);
@@ -168,13 +190,13 @@ __global__ void __cluster_dims__(kAlphaCluster, 1, 1) __launch_bounds__(kAlphaTh
     const float ip = recip[0], iq = recip[1];
     dd m = {0.f, 0.f}, unused = {0.f, 0.f};
     if (ip != 0.f)
-        slice_pair_sums(pr, qr, A.V, s0, s1, vec, warp, lane,
+        slice_pair_sums<2>(pr, qr, A.V, s0, s1, vec, warp, lane,
                         [ip, iq](float4 a, float4 c, dd &x0, dd &) {
                             const float4 v = make_float4(fminf(a.x * ip, c.x * iq), fminf(a.y * ip, c.y * iq),
                                                          fminf(a.z * ip, c.z * iq), fminf(a.w * ip, c.w * iq));
                             x0 = dd_add(x0, quad_mass<false>(v, make_float4(0.f, 0.f, 0.f, 0.f)));
                         },
-                        m, unused);
+                        m, unused, keep);
     m = warp_sum_dd(m);
     const dd M_part = cta_sum_dd(m, sh[0], warp, lane);
     if (threadIdx.x == 0) cluster.map_shared_rank(&am[0], 0)[rank] = M_part;
