@@ -62,8 +62,11 @@ def draws(expl):
     return [e for e in expl if e[1] == "draw"]
 
 
+# (64, 32000, 4): mass groups deferred and two-position groups at once; (8, 2000, 48): chains of up
+# to 49 steps, draft ids past the first 32
 @pytest.mark.parametrize("B,V,K,tau", [(64, 4096, 4, 1.0), (33, 20011, 5, 0.7), (8, 1, 3, 1.0),
-                                       (16, 50000, 8, 1.6), (5, 3000, 0, 1.0), (9, 777, 16, 0.5)])
+                                       (16, 50000, 8, 1.6), (5, 3000, 0, 1.0), (9, 777, 16, 0.5),
+                                       (64, 32000, 4, 1.0), (8, 2000, 48, 1.0)])
 def test_logits_match_oracle(B, V, K, tau):
     zp, zq, t, ua, ur = make_logits(B, V, K, tau, seed=7000 + V + K)
     n0, expl = run(zp, zq, t, ua, ur, tau)
