@@ -21,30 +21,38 @@
 //                      row (pair), formed in fp32 from the normalisers, summed
 //                      in fours and stored as double-fp32 block and segment
 //                      sums.
-// One queue counter hands tasks out in order.  The first B groups are
+// One queue counter hands tasks (bulk-copy workers: chunks of 4, 8 or 16
+// segments, chosen per call) out in order.  The first B groups are
 // norm(b, 0); every later group is appended by the worker that finishes the
 // last task of the sequence's previous group (an arrival counter per
 // sequence).  That worker merges the segment pairs in segment order -- so the
 // normalisers do not depend on which worker ran which task -- and decides:
 // after norm(b, i) it makes the accept test u * q_i(t_i) < p_i(t_i) on the
-// gathered logits and appends norm(b, i + 1) on acceptance, else mass(b, i);
-// after norm(b, K) it appends mass(b, K); after mass(b, n) it draws with the
-// same segment -> block -> element search as the probability path, its
-// element step recomputing the masses with the same instructions.  A
-// sequence's groups run one after another while other sequences' groups fill
-// the machine.  The only wait is that of a worker whose next task belongs to
-// a group not yet appended; it is bounded (kStatusTimeout) and ends once every
-// sequence has its token.
+// gathered logits and appends norm(b, i + 1) on acceptance, else mass(b, i)
+// (a precise group first when the fp32 test is too close to call); after
+// norm(b, K) it appends mass(b, K); after mass(b, n) it draws with the same
+// segment -> block -> element search as the probability path, its element
+// step recomputing the masses with the same instructions.  A sequence's
+// groups form a chain that runs while other sequences' groups fill the
+// machine.  To shorten the chains: mass groups, which end a chain, wait in a
+// pending list while the first groups alone occupy every worker; producers
+// claim their next chunk only once the current one is issued; and where the
+// chains are long against the batch, a norm group appended while workers run
+// short of work covers two positions.  The only wait is that of a worker whose
+// next task belongs to a group not yet appended; it is bounded
+// (kStatusTimeout), moves pending mass groups into the queue, and ends once
+// every sequence has its token.
 //
 // Accuracy: each mass carries the error of exp2.approx (~2^-22), of the fp32
 // subtraction and scaling of its argument (about |z - max| * c * 2^-24 in the
 // exponent) and of the fp32 normalisation -- around 1e-6 relative at most for
 // the elements that carry mass; the fp32 sums within a lane (four masses, or a
 // lane's 32 normaliser terms) add at most 3 * 2^-24 and 5 * 2^-24 relative,
-// and everything above them is summed in double-fp32.  Accept decisions can therefore differ
-// from an fp64 softmax only when |u*q - p| is within ~1e-5 of p, and drawn
-// tokens only when u*R lies within ~2e-6 (in units of normalised mass) of a
-// boundary.
+// and everything above them is summed in double-fp32.  An accept test whose
+// margin is inside the fast probabilities' error bound is made again in fp64
+// (lg_fast_decides), so accept decisions equal an fp64 softmax's; drawn
+// tokens may differ only when u*R lies within ~2e-6 (in units of normalised
+// mass) of a boundary.
 #pragma once
 
 #include "sv_device.cuh"
