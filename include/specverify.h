@@ -209,7 +209,11 @@ int sv_set_ctas_per_sm(int32_t ctas_per_sm);
  * warped rows are never written to memory.  zp holds B*(K+1) rows and zq B*K
  * rows of V f32 logits, laid out like p and q above.  Rows are read in order:
  * the pair (zp_i, zq_i) once for its normalisers and the accept test of
- * position i, the rejected pair (or zp_K) a second time for the draw.
+ * position i, the rejected pair (or zp_K) a second time for the draw.  In
+ * calls whose chains of positions are long against the batch (K x resident
+ * workers >= B x claims per row pair), the next position's pair may be read
+ * together with position i's while the GPU would otherwise wait, and is then
+ * not used if position i is rejected.
  * Arithmetic is fp32 with exp2.approx and double-fp32 sums.  An accept test
  * is decided in fp32 only when its margin |u*q - p| exceeds a bound on the
  * fast probabilities' error (derived from the fp32 exponent arguments, an
