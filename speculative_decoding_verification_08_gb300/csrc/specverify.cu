@@ -99,11 +99,13 @@ struct Layout {
 };
 constexpr size_t kLgHead = 16, kLgTail = 24, kLgDone = 32, kLgExit = 36, kLgPendHead = 40,
                  kLgPendTail = 48;
-// sv_verify_sample_logits' chunk size: 16 segments when the first groups give
-// every worker at least kLgChunkBig claims of 16, else 8 when they give every
-// worker at least kLgChunkSmall claims of 8, else 4 (a measured rule: 16 is
-// best at B=1024 V=128256, 8 at B=256, 4 at B <= 64 with V=32000)
-constexpr int64_t kLgChunkBig = 16, kLgChunkSmall = 1;
+// sv_verify_sample_logits' chunk size: 32 segments when the first groups give
+// every worker at least kLgChunkBig claims of 32, else 8 when they give every
+// worker at least kLgChunkSmall claims of 8, else 4 (a measured rule at
+// V=128256: 32 is best at B=512, 768 and 1024, where the first groups give
+// each worker 6.7 to 13.5 claims of 32; 8 at B=256, 3.4 claims, where 16
+// measured slower than 8; 4 at B <= 64 with V=32000)
+constexpr int64_t kLgChunkBig = 4, kLgChunkSmall = 1;
 
 
 
@@ -704,13 +706,11 @@ int sv_verify_sample_logits(const float *zp, int64_t zp_row_stride, const float 
     // worker a claim (otherwise no chain waits behind another's mass group)
     const int64_t workers = (int64_t)grid * (ring ? 1 : sv::kLgWarps);
     // segments per chunk (one claim, one group read and one arrival each):
-    // 16 while the first groups give every worker many claims, fewer when
+    // 32 while the first groups give every worker several claims, fewer when
     // they do not, so that a group spreads over more workers and its
     // sequence's steps are shorter
     auto chunks = [&](int64_t c) { return (int64_t)B * ((L.nseg + c - 1) / c); };
-    L.chunk = 16;
-    if (chunks(16) < kLgChunkBig * workers) L.chunk = 8;
-    if (chunks(8) < kLgChunkSmall * workers) L.chunk = 4;
+    L.chunk = chunks(32) >= kLgChunkBig * workers ? 32 : chunks(8) >= kLgChunkSmall * workers ? 8 : 4;
     const int64_t claims = ring ? (L.nseg + L.chunk - 1) / L.chunk : L.nseg;
     L.claims = claims;
     // a norm group spans two positions while fewer claims than workers wait

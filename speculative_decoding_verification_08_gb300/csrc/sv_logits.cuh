@@ -21,7 +21,7 @@
 //                      row (pair), formed in fp32 from the normalisers, summed
 //                      in fours and stored as double-fp32 block and segment
 //                      sums.
-// One queue counter hands tasks (bulk-copy workers: chunks of 4, 8 or 16
+// One queue counter hands tasks (bulk-copy workers: chunks of 4, 8 or 32
 // segments, chosen per call) out in order.  The first B groups are
 // norm(b, 0); every later group is appended by the worker that finishes the
 // last task of the sequence's previous group (an arrival counter per

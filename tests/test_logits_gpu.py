@@ -186,19 +186,20 @@ def test_deferred_mass_groups_on_both_worker_kernels(aligned):
     assert ws.status() == 0
 
 
-def test_large_batch_takes_whole_chunks():
-    """A batch whose first groups give every bulk-copy worker at least 16
-    claims of 16 segments moves 16-segment chunks (smaller batches take 8 or
-    4, which the other tests cover); here each row is one whole chunk and a
-    ragged one (4 segments, the last of them partial).  The outputs equal the
-    oracle's."""
-    B, V, K, tau = 6000, 20011, 2, 1.0
-    zp, zq, t, ua, ur = make_logits(B, V + 1, K, tau, seed=8300)
+@pytest.mark.parametrize("B,V", [(6000, 20011), (1400, 40011)])
+def test_large_batch_takes_whole_chunks(B, V):
+    """A batch whose first groups give every bulk-copy worker at least 4
+    claims of 32 segments moves 32-segment chunks (smaller batches take 8 or
+    4, which the other tests cover).  V=20011: each row is one ragged chunk of
+    20 segments, the last of them partial; V=40011: a whole chunk and a ragged
+    one.  The outputs equal the oracle's."""
+    K, tau = 2, 1.0
+    zp, zq, t, ua, ur = make_logits(B, V + 1, K, tau, seed=8300 + B)
     zp, zq = zp[..., :V], zq[..., :V]   # row stride V + 1: 16-byte aligned rows
     t = torch.clamp(t, max=V - 1)
     n0, expl = run(zp, zq, t, ua, ur, tau)
     nseg = -(-V // 1024)
-    assert B * -(-nseg // 16) >= 16 * sv.last_grid_size(), "this size must take 16-segment chunks"
+    assert B * -(-nseg // 32) >= 4 * sv.last_grid_size(), "this size must take 32-segment chunks"
     assert len(draws(expl)) <= max(1, B // 2000), expl
     assert len(set(n0.tolist())) == K + 1
 
